@@ -1,0 +1,119 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch each.
+
+This is what makes the pins worth trusting: a mistake that no pin notices would let a
+wrong oracle certify a wrong kernel.  Each mutation replaces one internal step of
+``oracle.dense_kl`` for the duration of one test.
+"""
+import numpy as np
+import pytest
+
+import oracle.dense_kl as dk
+from tests import test_oracle_pins as pins
+
+PIN_CALLS = [
+    lambda: [pins.test_closed_form_cases(c) for c in pins.json.load(open(pins.GOLDEN))["cases"]],
+    lambda: pins.test_kl_zero_when_teacher_is_student(2.0),
+    lambda: pins.test_kl_nonnegative(1),
+    lambda: pins.test_single_slot_is_cross_entropy(1.5),
+    pins.test_dense_grid_matches_torch_kl_div_and_logsumexp,
+    pins.test_tau_identity,
+    lambda: pins.test_gradient_finite_differences(1.7, True),
+    lambda: pins.test_gradient_finite_differences(1.0, False),
+    pins.test_gradient_matches_autograd_on_dense_formula,
+    pins.test_chunk_invariance,
+    pins.test_masked_rows_change_nothing,
+    pins.test_no_valid_token,
+]
+
+
+def failing_pins():
+    failed = 0
+    for call in PIN_CALLS:
+        try:
+            with np.errstate(all="ignore"):
+                call()
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            failed += 1
+    return failed
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert failing_pins() == 0
+
+
+orig_row_terms = dk._row_terms
+orig_ds_block = dk._ds_block
+orig_teacher_probs = dk.teacher_probs
+
+
+def row_terms_no_student_tau(s, idx, p, logp, tau):
+    return orig_row_terms(s * tau, idx, p, logp, tau)
+
+
+def row_terms_drop_entropy(s, idx, p, logp, tau):
+    return orig_row_terms(s, idx, p, np.zeros_like(logp), tau)
+
+
+def row_terms_wrong_index(s, idx, p, logp, tau):
+    return orig_row_terms(s, (idx + 1) % s.shape[1], p, logp, tau)
+
+
+def ds_sign_flip(s, idx, p, valid, tau, scale):
+    return -orig_ds_block(s, idx, p, valid, tau, scale)
+
+
+def ds_scatter_assign(s, idx, p, valid, tau, scale):
+    a = s / tau
+    q = np.exp(a - a.max(1, keepdims=True))
+    q /= q.sum(1, keepdims=True)
+    pt = np.zeros_like(q)
+    np.put_along_axis(pt, idx, p, axis=1)  # assignment: repeated ids lose mass
+    ds = scale * (q - pt)
+    ds[~valid] = 0
+    return ds
+
+
+def ds_missing_tau(s, idx, p, valid, tau, scale):
+    return orig_ds_block(s, idx, p, valid, tau, scale / tau)
+
+
+def ds_ignores_mask(s, idx, p, valid, tau, scale):
+    return orig_ds_block(s, idx, p, np.ones_like(valid), tau, scale)
+
+
+def probs_no_teacher_tau(z, tau):
+    return orig_teacher_probs(z, 1.0)
+
+
+def lse_log2(s, idx, p, logp, tau):
+    lse, kl = orig_row_terms(s, idx, p, logp, tau)
+    return lse / np.log(2.0), kl
+
+
+MUTATIONS = {
+    "_row_terms": [row_terms_no_student_tau, row_terms_drop_entropy, row_terms_wrong_index, lse_log2],
+    "_ds_block": [ds_sign_flip, ds_scatter_assign, ds_missing_tau, ds_ignores_mask],
+    "teacher_probs": [probs_no_teacher_tau],
+}
+
+
+@pytest.mark.parametrize("target,mutant", [(t, m) for t, ms in MUTATIONS.items() for m in ms],
+                         ids=lambda x: getattr(x, "__name__", x))
+def test_planted_mistake_is_caught(monkeypatch, target, mutant):
+    monkeypatch.setattr(dk, target, mutant)
+    assert failing_pins() >= 1
+
+
+def test_loss_normaliser_mistake_is_caught(monkeypatch):
+    orig_forward = dk.forward
+
+    def forward_over_all_tokens(H, W, idx, z, mask, tau, chunk=64, rows=None):
+        out = orig_forward(H, W, idx, z, mask, tau, chunk, rows)
+        if out["loss"] is not None and out["n_valid"]:
+            out["loss"] *= out["n_valid"] / len(out["lse"])  # divides by T, not N_valid
+        return out
+
+    monkeypatch.setattr(dk, "forward", forward_over_all_tokens)
+    import oracle
+    monkeypatch.setattr(oracle, "forward", forward_over_all_tokens)
+    assert failing_pins() >= 1
