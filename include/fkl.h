@@ -1,0 +1,125 @@
+/*
+ * fkl.h - C ABI of the fused chunked KL distillation loss for GB300 (sm_103a).
+ *
+ * The operation is the loss of "Efficient Knowledge Distillation for LLMs: Offline Top-K
+ * Logits and a Fused Chunked KL Loss" (Hugging Face blog post, section "Two systems
+ * changes", paragraphs "Offline distillation" and "Fused chunked KL"): the student's
+ * final hidden states H are projected through the LM head W chunk by chunk, each chunk of
+ * logits is folded into a running loss against the teacher's cached top-K logits and then
+ * discarded, and the backward pass recomputes each chunk instead of storing it.  The
+ * pages print no formula; the one implemented is
+ *
+ *     s = H W^T (bf16 inputs, fp32 accumulation),  a = s / tau
+ *     lse_t = log sum_v exp(a_tv)                   over the whole vocabulary
+ *     p_t   = softmax(z_t / tau)                    over the K cached teacher slots
+ *     KL_t  = sum_k p_tk (log p_tk - (a_{t,id_tk} - lse_t))
+ *     L     = tau^2 / N * sum_{t : mask_t = 1} KL_t,     N = number of valid tokens
+ *
+ * and its gradient (the post's "closed-form gradient", not printed there)
+ *
+ *     dS_tv = g * tau / N * (exp(a_tv - lse_t) - ptilde_tv)  for valid t, else 0
+ *     dH = dS W,  dW = dS^T H                                  (fp32 outputs)
+ *
+ * where ptilde_t is p_t added at the ids of row t and g the upstream gradient of L.
+ * N = 0 gives L = 0 and zero gradients.  No T x V tensor is ever written to memory:
+ * logits live only in tensor memory, one tile at a time; the backward writes dS one
+ * vocabulary slab at a time into the caller's workspace, bounded by `chunk` (below).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device memory of the current device; all buffers are
+ *     row-major and contiguous.  The caller owns every buffer, including the workspace;
+ *     the library allocates no device memory.
+ *   - H and W are bfloat16 bit patterns (uint16_t).  H, W, dH and dW must be 16-byte
+ *     aligned, the workspace 256-byte aligned, everything else 4-byte aligned; d must be a
+ *     multiple of 8 (TMA rows are whole 16-byte units).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous
+ *     on `stream`; they never synchronise the device.
+ *   - Shape limits: 0 <= T < 2^31, 1 <= V < 2^31, 8 <= d < 2^20, d % 8 == 0,
+ *     1 <= K <= 1024, chunk >= 1, tau > 0 and finite.
+ *   - Errors found on the host (bad argument, alignment, workspace too small, a CUDA
+ *     launch failure) are returned at once and nothing is enqueued after the failing
+ *     step; fkl_last_error() gives a message.  Errors found on the device (a teacher id
+ *     outside [0, V), a teacher row with no finite logit, a pipeline wait that exceeded
+ *     its time limit) are recorded in a status word inside the workspace, make the loss
+ *     NaN (forward) or fill dH and dW with NaN (backward), and are reported by
+ *     fkl_read_status().  No device code traps.
+ *   - Results are deterministic: the same inputs give bitwise the same outputs.
+ */
+#ifndef FKL_H_
+#define FKL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fkl_status {
+  FKL_OK = 0,
+  FKL_ERR_INVALID_ARG = 1,  /* NULL pointer, bad shape, non-positive tau or chunk */
+  FKL_ERR_ALIGNMENT = 2,    /* a pointer or d breaks the alignment rules above */
+  FKL_ERR_UNSUPPORTED = 3,  /* the current device is not sm_103 */
+  FKL_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than fkl_workspace_size() */
+  FKL_ERR_CUDA = 5,         /* a CUDA runtime or driver call failed */
+  FKL_ERR_BAD_TOPK_ID = 6,  /* device: a teacher id is outside [0, V) */
+  FKL_ERR_BAD_TOPK_ROW = 7, /* device: a teacher row has no finite logit */
+  FKL_ERR_TIMEOUT = 8       /* device: a pipeline wait exceeded its time limit */
+} fkl_status;
+
+/*
+ * Bytes of workspace that fkl_forward and fkl_backward need for this shape (one buffer
+ * serves both; no state is carried between calls in it).  `chunk` bounds the backward's
+ * dS buffer: it holds at most chunk * V bfloat16 values (rounded so that a vocabulary
+ * slab is a whole number of 256-column tiles, and at least one tile wide).  The result
+ * does not depend on `chunk` beyond floating-point summation order.  Returns 0 for
+ * invalid shapes.
+ */
+size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
+
+/*
+ * Forward pass: writes the scalar loss L to *loss (device float) and lse[t] (device
+ * float[T], natural log of sum_v exp(s_tv / tau), defined for masked tokens too).
+ *   H           bf16 [T, d]     student final hidden states
+ *   W           bf16 [V, d]     LM-head weight
+ *   topk_idx    int32 [T, K]    teacher's cached top-K token ids, any slot order
+ *   topk_logits fp32 [T, K]     teacher's logits for those ids (-inf allowed per slot)
+ *   mask        uint8 [T]       1 = token counts, 0 = skipped; NULL = all tokens count
+ *   workspace   device buffer of ws_bytes >= fkl_workspace_size(T, d, V, K, chunk)
+ */
+fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                       const float* topk_logits, const uint8_t* mask, int64_t T, int64_t d,
+                       int64_t V, int64_t K, float tau, int64_t chunk, float* loss, float* lse,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Backward pass: recomputes the projection chunk by chunk and writes dH (device float
+ * [T, d]) and dW (device float [V, d]); both are overwritten, not accumulated into.
+ *   lse        device float [T] from fkl_forward on the same inputs
+ *   grad_loss  device float scalar g (the upstream gradient of L); NULL means g = 1
+ * Other arguments as in fkl_forward.
+ */
+fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                        const float* topk_logits, const uint8_t* mask, const float* lse,
+                        const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K,
+                        float tau, int64_t chunk, float* dH, float* dW, void* workspace,
+                        size_t ws_bytes, void* stream);
+
+/*
+ * Waits for `stream`, then returns the device-side status recorded in `workspace` by the
+ * most recent fkl_forward / fkl_backward call that used it (FKL_OK if none failed), or
+ * FKL_ERR_CUDA if the wait or the read fails.
+ */
+fkl_status fkl_read_status(const void* workspace, void* stream);
+
+/* Static text for a status code. */
+const char* fkl_status_string(int status);
+
+/* Message of the last host-side error on the calling thread ("" if none). */
+const char* fkl_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FKL_H_ */

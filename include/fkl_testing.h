@@ -1,0 +1,47 @@
+/*
+ * fkl_testing.h - test hooks of the fused chunked KL library.
+ *
+ * These entry points expose single building blocks of the loss so that each can be
+ * checked on its own against a float64 host reference.  They are not part of the loss's
+ * API and the pages have no counterpart for them.  Conventions (pointers, alignment,
+ * streams, status codes) are those of fkl.h.
+ */
+#ifndef FKL_TESTING_H_
+#define FKL_TESTING_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "fkl.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * The tensor-core GEMM that the loss is built from, with a plain fp32 epilogue:
+ *   D[M, N] (fp32, row-major, leading dimension N) = A B^T            if accumulate == 0
+ *   D[M, N] += A B^T                                                   if accumulate != 0
+ * A is logically [M, Kd] and B logically [N, Kd], both bfloat16.  a_mn_major = 0 means A is
+ * stored [M][Kd] (Kd contiguous); 1 means stored [Kd][M] (M contiguous).  Likewise for B.
+ * bn selects the tile width along N: 256, 192 or 128.  M, N, Kd >= 1; the contiguous
+ * extent of each operand must be a multiple of 8.  `workspace` needs 256 bytes (the
+ * status word).
+ */
+fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N,
+                         int64_t Kd, int a_mn_major, int b_mn_major, int bn, int accumulate,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Runs one pipeline wait on a barrier that nothing completes, with a time limit of
+ * limit_ns nanoseconds (at most one second), so that the bounded-wait path can be
+ * checked without hanging the GPU: afterwards fkl_read_status(workspace, stream) must
+ * return FKL_ERR_TIMEOUT.  `workspace` needs 256 bytes.
+ */
+fkl_status fkl_test_wait_timeout(uint64_t limit_ns, void* workspace, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FKL_TESTING_H_ */

@@ -1,0 +1,165 @@
+"""Fused chunked KL distillation loss for GB300 (sm_103a): Python binding.
+
+The loss is the one of "Efficient Knowledge Distillation for LLMs: Offline Top-K Logits and a
+Fused Chunked KL Loss" (section "Two systems changes"): the LM-head projection s = H W^T is
+fused into a KL divergence against the teacher's cached top-K logits, chunk by chunk, and
+the backward recomputes each chunk.  Every step runs in the CUDA kernels of ``libfkl.so``
+(C ABI in include/fkl.h); this module only checks and marshals PyTorch tensors (device
+memory and streams) into that ABI.
+
+    loss = fused_kl(H, W, topk_idx, topk_logits, mask=None, tau=1.0, chunk=2048)
+    loss.backward()          # gradients for H and W
+
+or the explicit calls ``forward`` / ``backward`` with a reusable ``Workspace``.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from ._lib import FKL_OK, STATUS, FklError, check, lib  # noqa: F401
+
+__all__ = ["workspace_size", "Workspace", "forward", "backward", "read_status", "fused_kl",
+           "FusedKL", "FklError", "STATUS"]
+
+
+def workspace_size(T: int, d: int, V: int, K: int, chunk: int) -> int:
+    n = lib().fkl_workspace_size(T, d, V, K, chunk)
+    if n == 0:
+        raise FklError(1, "fkl_workspace_size", f"unsupported shape T={T} d={d} V={V} K={K} chunk={chunk}")
+    return int(n)
+
+
+class Workspace:
+    """Device scratch buffer for fkl_forward / fkl_backward, grown on demand and reused."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device) if device is not None else None
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        device = torch.device(device)
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _norm(device) -> torch.device:
+    device = torch.device(device)
+    if device.type == "cuda" and device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    return device
+
+
+def _ws_for(workspace: Optional[Workspace], nbytes: int, device) -> torch.Tensor:
+    device = _norm(device)
+    if workspace is None:
+        workspace = _default_ws.setdefault(device, Workspace(device))
+    return workspace.get(nbytes, device)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_inputs(H, W, topk_idx, topk_logits, mask):
+    if not (H.is_cuda and W.is_cuda and topk_idx.is_cuda and topk_logits.is_cuda):
+        raise ValueError("H, W, topk_idx and topk_logits must be CUDA tensors")
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("H and W must be bfloat16")
+    if topk_idx.dtype != torch.int32 or topk_logits.dtype != torch.float32:
+        raise TypeError("topk_idx must be int32 and topk_logits float32")
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError("H must be [T, d] and W [V, d]")
+    T, K = topk_idx.shape
+    if T != H.shape[0] or tuple(topk_logits.shape) != (T, K):
+        raise ValueError("topk_idx and topk_logits must be [T, K]")
+    for name, t in (("H", H), ("W", W), ("topk_idx", topk_idx), ("topk_logits", topk_logits)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if mask is not None:
+        if mask.dtype not in (torch.uint8, torch.bool) or tuple(mask.shape) != (T,) or not mask.is_cuda:
+            raise ValueError("mask must be a CUDA uint8/bool tensor of shape [T]")
+        mask = mask.contiguous().view(torch.uint8)
+    return mask
+
+
+def forward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
+            mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048,
+            workspace: Optional[Workspace] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Loss (0-dim float32) and lse [T] (float32) on H's device and current stream."""
+    mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
+    T, d = H.shape
+    V, K = W.shape[0], topk_idx.shape[1]
+    ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk), H.device)
+    loss = torch.empty((), dtype=torch.float32, device=H.device)
+    lse = torch.empty(T, dtype=torch.float32, device=H.device)
+    st = lib().fkl_forward(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask), T, d, V, K,
+                           float(tau), chunk, _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(H.device))
+    check(st, "fkl_forward")
+    return loss, lse
+
+
+def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
+             mask: Optional[torch.Tensor], lse: torch.Tensor, grad_loss: Optional[torch.Tensor] = None,
+             tau: float = 1.0, chunk: int = 2048, workspace: Optional[Workspace] = None,
+             out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """dH [T, d] and dW [V, d] (float32), the gradient of g * loss (g = grad_loss or 1)."""
+    mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
+    T, d = H.shape
+    V, K = W.shape[0], topk_idx.shape[1]
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (T,) or not lse.is_cuda:
+        raise ValueError("lse must be a CUDA float32 tensor of shape [T]")
+    if grad_loss is not None:
+        grad_loss = grad_loss.detach().to(device=H.device, dtype=torch.float32).reshape(()).contiguous()
+    ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk), H.device)
+    if out is None:
+        dH = torch.empty((T, d), dtype=torch.float32, device=H.device)
+        dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
+    else:
+        dH, dW = out
+    st = lib().fkl_backward(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask),
+                            _ptr(lse.contiguous()), _ptr(grad_loss), T, d, V, K, float(tau), chunk,
+                            _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(H.device))
+    check(st, "fkl_backward")
+    return dH, dW
+
+
+def read_status(workspace: Optional[Workspace] = None, device=None) -> int:
+    """Device-side status of the last call on ``workspace`` (syncs the current stream)."""
+    if workspace is None:
+        workspace = _default_ws[_norm(device or "cuda")]
+    return int(lib().fkl_read_status(_ptr(workspace.buf), _stream(workspace.buf.device)))
+
+
+class FusedKL(torch.autograd.Function):
+    """Autograd wrapper: forward saves lse; backward recomputes the projection chunk by chunk."""
+
+    @staticmethod
+    def forward(ctx, H, W, topk_idx, topk_logits, mask, tau, chunk):
+        loss, lse = forward(H, W, topk_idx, topk_logits, mask, tau, chunk)
+        ctx.save_for_backward(H, W, topk_idx, topk_logits, lse)
+        ctx.mask = mask
+        ctx.tau, ctx.chunk = tau, chunk
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad):
+        H, W, topk_idx, topk_logits, lse = ctx.saved_tensors
+        dH, dW = backward(H, W, topk_idx, topk_logits, ctx.mask, lse, grad, ctx.tau, ctx.chunk)
+        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None, None
+
+
+def fused_kl(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
+             mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048) -> torch.Tensor:
+    """tau^2 / N * sum over valid tokens of KL(teacher top-K || student), differentiable in H, W."""
+    return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk)

@@ -1,0 +1,430 @@
+// Host side of the C ABI (include/fkl.h, include/fkl_testing.h): argument checks, the
+// workspace plan, tensor-map encoding, the tile schedule and the launch sequences of the
+// forward and backward passes.  All work is enqueued on the caller's stream; nothing here
+// allocates device memory or synchronises, except fkl_read_status.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/fkl.h"
+#include "../../include/fkl_testing.h"
+#include "fkl_internal.h"
+
+namespace fkl {
+
+static thread_local std::string g_last_error;
+
+static fkl_status fail(fkl_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+static fkl_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FKL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p) {
+  if (T < 0 || T >= (int64_t{1} << 31)) return false;
+  if (d < 8 || d % 8 != 0 || d >= (int64_t{1} << 20)) return false;
+  if (V < 1 || V > (int64_t{1} << 30)) return false;
+  if (K < 1 || K > 1024) return false;
+  if (chunk < 1) return false;
+  p->T = T; p->d = d; p->V = V; p->K = K; p->chunk = chunk;
+  const int64_t vpad = cdiv(V, kVocabTile) * kVocabTile;
+  if (T == 0) {
+    p->Vc = kVocabTile;
+    p->nslabs = 0;
+  } else {
+    // The dS slab holds at most chunk * V values: slab width = chunk * V / T columns,
+    // rounded down to whole tiles (at least one), then evened out over the slabs.
+    const int64_t c = chunk < T ? chunk : T;
+    int64_t vc = (c * V) / T;
+    vc = (vc / kVocabTile) * kVocabTile;
+    if (vc < kVocabTile) vc = kVocabTile;
+    if (vc > vpad) vc = vpad;
+    const int64_t ns = cdiv(V, vc);
+    const int64_t even = cdiv(cdiv(V, ns), kVocabTile) * kVocabTile;
+    p->Vc = even < vc ? even : vc;
+    p->nslabs = cdiv(V, p->Vc);
+  }
+  p->nb = cdiv(T, 256);
+  size_t off = 256;  // header
+  p->off_pairs = off; off = align_up(off + static_cast<size_t>(T) * K * 8, 256);
+  p->off_crow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
+  p->off_part = off;  off = align_up(off + static_cast<size_t>(T) * 3 * kMaxSplit * 4, 256);
+  const size_t nbb = static_cast<size_t>(p->nb > 0 ? p->nb : 1);
+  p->off_bsum = off;  off = align_up(off + nbb * 8, 256);
+  p->off_bcnt = off;  off = align_up(off + nbb * 4, 256);
+  p->off_ds = off;    off = align_up(off + static_cast<size_t>(T) * p->Vc * 2, 256);
+  p->total = off;
+  return true;
+}
+
+int plan_splits(int m_tiles, int n_tiles, int sms) {
+  // Pick the number of vocabulary splits per row block that minimises the critical path
+  // (waves of units x tiles per unit).  At least sms/32 splits keep the row blocks in
+  // flight at once (each re-read from L2 for every tile of its unit) to a few dozen.
+  int lo = (sms + 31) / 32;
+  if (lo > n_tiles) lo = n_tiles;
+  if (lo < 1) lo = 1;
+  int hi = n_tiles < kMaxSplit ? n_tiles : kMaxSplit;
+  int best = lo;
+  int64_t best_cost = INT64_MAX;
+  for (int s = lo; s <= hi; ++s) {
+    const int64_t units = static_cast<int64_t>(m_tiles) * s;
+    const int64_t waves = cdiv(units, sms);
+    const int64_t per_unit = cdiv(n_tiles, s);
+    const int64_t cost = waves * per_unit;
+    if (cost < best_cost) { best_cost = cost; best = s; }
+  }
+  return best;
+}
+
+GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status) {
+  GemmShape g;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.Kd = static_cast<int>(Kd);
+  g.m_tiles = static_cast<int>(cdiv(M, 128));
+  g.n_tiles = static_cast<int>(cdiv(N, bn));
+  g.k_blocks = static_cast<int>(cdiv(Kd, 64));
+  g.nsplit = nsplit;
+  g.num_units = g.m_tiles * nsplit;
+  g.status = status;
+  g.limit_ns = kWaitLimitNs;
+  return g;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map with 128-byte swizzle; out-of-range elements of a box read as zero.
+bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- device info
+struct DevInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+static fkl_status device_info(DevInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  static std::mutex mu;
+  static DevInfo cache[128];
+  static bool have[128] = {};
+  if (dev < 0 || dev >= 128) return fail(FKL_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!have[dev]) {
+      DevInfo di;
+      if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+      cache[dev] = di;
+      have[dev] = true;
+    }
+    *out = cache[dev];
+  }
+  if (out->major != 10 || out->minor != 3)
+    return fail(FKL_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                out->major, out->minor);
+  return FKL_OK;
+}
+
+static int choose_bn_d(int64_t d) {
+  const int cand[3] = {256, 192, 128};
+  int best = 256;
+  int64_t best_waste = INT64_MAX;
+  for (int bn : cand) {
+    const int64_t waste = cdiv(d, bn) * bn - d;
+    if (waste < best_waste) { best_waste = waste; best = bn; }
+  }
+  return best;
+}
+
+static fkl_status check_common(const uint16_t* H, const uint16_t* W, const int32_t* idx, const float* z,
+                               int64_t T, int64_t d, int64_t V, int64_t K, float tau, int64_t chunk,
+                               void* ws, size_t ws_bytes, Plan* plan) {
+  if (!make_plan(T, d, V, K, chunk, plan))
+    return fail(FKL_ERR_INVALID_ARG,
+                "unsupported shape T=%lld d=%lld V=%lld K=%lld chunk=%lld (need 0<=T<2^31, d%%8==0, "
+                "8<=d<2^20, 1<=V<=2^30, 1<=K<=1024, chunk>=1)",
+                (long long)T, (long long)d, (long long)V, (long long)K, (long long)chunk);
+  if (!(tau > 0.f) || !std::isfinite(tau)) return fail(FKL_ERR_INVALID_ARG, "tau must be finite and > 0");
+  if (W == nullptr) return fail(FKL_ERR_INVALID_ARG, "W is NULL");
+  if (T > 0 && (H == nullptr || idx == nullptr || z == nullptr))
+    return fail(FKL_ERR_INVALID_ARG, "H, topk_idx and topk_logits must not be NULL");
+  if (ws == nullptr) return fail(FKL_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(FKL_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (ws_bytes < plan->total)
+    return fail(FKL_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, plan->total);
+  if (!aligned(W, 16) || (H && !aligned(H, 16))) return fail(FKL_ERR_ALIGNMENT, "H and W must be 16-byte aligned");
+  if ((idx && !aligned(idx, 4)) || (z && !aligned(z, 4)))
+    return fail(FKL_ERR_ALIGNMENT, "topk_idx and topk_logits must be 4-byte aligned");
+  return FKL_OK;
+}
+
+}  // namespace fkl
+
+using namespace fkl;
+
+extern "C" {
+
+size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk) {
+  Plan p;
+  return make_plan(T, d, V, K, chunk, &p) ? p.total : 0;
+}
+
+const char* fkl_last_error(void) { return g_last_error.c_str(); }
+
+const char* fkl_status_string(int status) {
+  switch (status) {
+    case FKL_OK: return "ok";
+    case FKL_ERR_INVALID_ARG: return "invalid argument";
+    case FKL_ERR_ALIGNMENT: return "misaligned pointer or dimension";
+    case FKL_ERR_UNSUPPORTED: return "unsupported device";
+    case FKL_ERR_WORKSPACE: return "workspace missing or too small";
+    case FKL_ERR_CUDA: return "CUDA error";
+    case FKL_ERR_BAD_TOPK_ID: return "teacher id outside [0, V)";
+    case FKL_ERR_BAD_TOPK_ROW: return "teacher row without a finite logit";
+    case FKL_ERR_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                       const float* topk_logits, const uint8_t* mask, int64_t T, int64_t d,
+                       int64_t V, int64_t K, float tau, int64_t chunk, float* loss, float* lse,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  Plan pl;
+  fkl_status s = check_common(H, W, topk_idx, topk_logits, T, d, V, K, tau, chunk, workspace, ws_bytes, &pl);
+  if (s != FKL_OK) return s;
+  if (loss == nullptr || (T > 0 && lse == nullptr)) return fail(FKL_ERR_INVALID_ARG, "loss and lse must not be NULL");
+  if (!aligned(loss, 4) || (lse && !aligned(lse, 4))) return fail(FKL_ERR_ALIGNMENT, "loss and lse must be 4-byte aligned");
+  DevInfo di;
+  if ((s = device_info(&di)) != FKL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  int2* pairs = reinterpret_cast<int2*>(ws + pl.off_pairs);
+  float* crow = reinterpret_cast<float*>(ws + pl.off_crow);
+  float* part = reinterpret_cast<float*>(ws + pl.off_part);
+  double* bsum = reinterpret_cast<double*>(ws + pl.off_bsum);
+  int* bcnt = reinterpret_cast<int*>(ws + pl.off_bcnt);
+
+  if (T > 0) {
+    if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st)) != cudaSuccess)
+      return cuda_fail(e, "prep kernel");
+    CUtensorMap mH, mW;
+    if (!encode_map_bf16(&mH, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, W, d, V, d * 2, 64, kVocabTile))
+      return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H or W");
+    const int m_tiles = (int)cdiv(T, 128), n_tiles = (int)cdiv(V, kVocabTile);
+    const int nsplit = plan_splits(m_tiles, n_tiles, di.sms);
+    const GemmShape g = make_shape(T, V, d, kVocabTile, nsplit, &hdr->status);
+    FwdParams fp;
+    fp.pairs = pairs;
+    fp.part = part;
+    fp.T = (int)T; fp.K = (int)K; fp.V = (int)V; fp.nsplit = nsplit;
+    fp.scale2 = 1.4426950408889634f / tau;
+    const int grid = g.num_units < di.sms ? g.num_units : di.sms;
+    if ((e = launch_gemm_fwd(mH, mW, g, fp, grid, st)) != cudaSuccess) return cuda_fail(e, "forward GEMM");
+    if ((e = launch_combine(part, nsplit, crow, mask, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st)) != cudaSuccess)
+      return cuda_fail(e, "combine kernels");
+  } else {
+    if ((e = launch_combine(part, 1, crow, mask, 0, tau, lse, bsum, bcnt, 0, hdr, loss, st)) != cudaSuccess)
+      return cuda_fail(e, "combine kernels");
+  }
+  return FKL_OK;
+}
+
+fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                        const float* topk_logits, const uint8_t* mask, const float* lse,
+                        const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K,
+                        float tau, int64_t chunk, float* dH, float* dW, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  Plan pl;
+  fkl_status s = check_common(H, W, topk_idx, topk_logits, T, d, V, K, tau, chunk, workspace, ws_bytes, &pl);
+  if (s != FKL_OK) return s;
+  if (dW == nullptr || (T > 0 && (dH == nullptr || lse == nullptr)))
+    return fail(FKL_ERR_INVALID_ARG, "dH, dW and lse must not be NULL");
+  if (!aligned(dW, 16) || (dH && !aligned(dH, 16))) return fail(FKL_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
+  if ((lse && !aligned(lse, 4)) || (grad_loss && !aligned(grad_loss, 4)))
+    return fail(FKL_ERR_ALIGNMENT, "lse and grad_loss must be 4-byte aligned");
+  DevInfo di;
+  if ((s = device_info(&di)) != FKL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  if (T == 0) {
+    if ((e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * 4, st)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync(dW)");
+    return FKL_OK;
+  }
+  int2* pairs = reinterpret_cast<int2*>(ws + pl.off_pairs);
+  float* crow = reinterpret_cast<float*>(ws + pl.off_crow);
+  uint16_t* ds = reinterpret_cast<uint16_t*>(ws + pl.off_ds);
+
+  if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st)) != cudaSuccess)
+    return cuda_fail(e, "prep kernel");
+  if ((e = launch_bwd_scalars(mask, T, grad_loss, tau, hdr, st)) != cudaSuccess) return cuda_fail(e, "scalars kernel");
+
+  CUtensorMap mH_k, mH_mn;
+  if (!encode_map_bf16(&mH_k, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mH_mn, H, d, T, d * 2, 64, 64))
+    return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
+  const int bnd = choose_bn_d(d);
+  const int64_t Vc = pl.Vc;
+  for (int64_t j = 0; j < pl.nslabs; ++j) {
+    const int64_t v0 = j * Vc;
+    const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
+    const uint16_t* Wj = W + v0 * d;
+    CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
+    if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile) ||
+        !encode_map_bf16(&mW_mn, Wj, d, w, d * 2, 64, 64) ||
+        !encode_map_bf16(&mD_mn, ds, w, T, Vc * 2, 64, 64) ||
+        !encode_map_bf16(&mD_k, ds, w, T, Vc * 2, 64, 128))
+      return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for slab %lld", (long long)j);
+
+    // dS[:, slab] = dscale * (q - ptilde), recomputing S = H W_slab^T.
+    const int m_tiles = (int)cdiv(T, 128), n_tiles = (int)cdiv(w, kVocabTile);
+    const GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms), &hdr->status);
+    DsParams dp;
+    dp.pairs = pairs; dp.lse = lse; dp.mask = mask; dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
+    dp.T = (int)T; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
+    dp.scale2 = 1.4426950408889634f / tau;
+    if ((e = launch_gemm_ds(mH_k, mW_k, g3, dp, g3.num_units < di.sms ? g3.num_units : di.sms, st)) != cudaSuccess)
+      return cuda_fail(e, "dS GEMM");
+
+    // dW[slab] = dS[:, slab]^T H  (complete for this slab: plain store).
+    const GemmShape g4 = make_shape(w, d, T, bnd, (int)cdiv(d, bnd), &hdr->status);
+    F32Params p4;
+    p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d; p4.accumulate = 0; p4.vec_ok = 1;
+    if ((e = launch_gemm_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, g4.num_units < di.sms ? g4.num_units : di.sms, st)) != cudaSuccess)
+      return cuda_fail(e, "dW GEMM");
+
+    // dH (+)= dS[:, slab] W[slab]  (slabs in order: deterministic accumulation).
+    const GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status);
+    F32Params p5;
+    p5.out = dH; p5.ldo = d; p5.M = (int)T; p5.N = (int)d; p5.accumulate = j > 0 ? 1 : 0; p5.vec_ok = 1;
+    if ((e = launch_gemm_f32(bnd, false, true, mD_k, mW_mn, g5, p5, g5.num_units < di.sms ? g5.num_units : di.sms, st)) != cudaSuccess)
+      return cuda_fail(e, "dH GEMM");
+  }
+  if ((e = launch_poison(dH, T * d, dW, V * d, &hdr->status, di.sms, st)) != cudaSuccess)
+    return cuda_fail(e, "poison kernel");
+  return FKL_OK;
+}
+
+fkl_status fkl_read_status(const void* workspace, void* stream) {
+  g_last_error.clear();
+  if (workspace == nullptr) return fail(FKL_ERR_WORKSPACE, "workspace is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (h & kStatusBadIdBit) return FKL_ERR_BAD_TOPK_ID;
+  if (h & kStatusBadRowBit) return FKL_ERR_BAD_TOPK_ROW;
+  if (h & kStatusTimeoutBit) return FKL_ERR_TIMEOUT;
+  return FKL_OK;
+}
+
+fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N,
+                         int64_t Kd, int a_mn_major, int b_mn_major, int bn, int accumulate,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!A || !B || !D) return fail(FKL_ERR_INVALID_ARG, "A, B and D must not be NULL");
+  if (M < 1 || N < 1 || Kd < 1 || M >= (1 << 30) || N >= (1 << 30) || Kd >= (1 << 30))
+    return fail(FKL_ERR_INVALID_ARG, "M, N, Kd must be in [1, 2^30)");
+  if (bn != 256 && bn != 192 && bn != 128) return fail(FKL_ERR_INVALID_ARG, "bn must be 256, 192 or 128");
+  const int64_t a_inner = a_mn_major ? M : Kd, b_inner = b_mn_major ? N : Kd;
+  if (a_inner % 8 != 0 || b_inner % 8 != 0)
+    return fail(FKL_ERR_ALIGNMENT, "the contiguous extent of A and B must be a multiple of 8");
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 4)) return fail(FKL_ERR_ALIGNMENT, "misaligned A, B or D");
+  if (!workspace || ws_bytes < 256) return fail(FKL_ERR_WORKSPACE, "workspace needs 256 bytes");
+  if (!aligned(workspace, 256)) return fail(FKL_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  DevInfo di;
+  fkl_status s = device_info(&di);
+  if (s != FKL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  CUtensorMap mA, mB;
+  bool ok = a_mn_major ? encode_map_bf16(&mA, A, M, Kd, M * 2, 64, 64) : encode_map_bf16(&mA, A, Kd, M, Kd * 2, 64, 128);
+  ok = ok && (b_mn_major ? encode_map_bf16(&mB, B, N, Kd, N * 2, 64, 64)
+                         : encode_map_bf16(&mB, B, Kd, N, Kd * 2, 64, (uint32_t)bn));
+  if (!ok) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for A or B");
+  const GemmShape g = make_shape(M, N, Kd, bn, (int)cdiv(N, bn), &hdr->status);
+  F32Params p;
+  p.out = D; p.ldo = N; p.M = (int)M; p.N = (int)N; p.accumulate = accumulate ? 1 : 0;
+  p.vec_ok = (N % 4 == 0 && aligned(D, 16)) ? 1 : 0;
+  if ((e = launch_gemm_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p,
+                           g.num_units < di.sms ? g.num_units : di.sms, st)) != cudaSuccess)
+    return cuda_fail(e, "test GEMM");
+  return FKL_OK;
+}
+
+fkl_status fkl_test_wait_timeout(uint64_t limit_ns, void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!workspace || ws_bytes < 256) return fail(FKL_ERR_WORKSPACE, "workspace needs 256 bytes");
+  if (!aligned(workspace, 256)) return fail(FKL_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return fail(FKL_ERR_INVALID_ARG, "limit_ns must be in (0, 1e9]");
+  DevInfo di;
+  fkl_status s = device_info(&di);
+  if (s != FKL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
+  if (e == cudaSuccess) e = launch_wait_timeout_test(static_cast<uint32_t*>(workspace), limit_ns, st);
+  if (e != cudaSuccess) return cuda_fail(e, "timeout probe");
+  return FKL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,488 @@
+// Persistent tcgen05 GEMM for sm_103a with fused epilogues.
+//
+// One CTA per SM, 192 threads in three roles:
+//   warp 0      TMA producer: streams 128 x 64 tiles of A and BN x 64 tiles of B into a
+//               STAGES-deep shared-memory ring (128-byte swizzle), one mbarrier per slot;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16 x bf16 -> fp32, 128 x BN
+//               x 16 per instruction) into one of two TMEM accumulators and releases
+//               shared-memory slots with tcgen05.commit;
+//   warps 2..5  epilogue: read the finished accumulator from TMEM (each warp its own 32
+//               lanes), run the fused epilogue, hand the accumulator back.
+// Two accumulators (2 x BN of the 512 TMEM columns) let the epilogue of one tile overlap
+// the MMAs of the next.
+//
+// The work is divided into units: a unit is one 128-row block of A and a contiguous range
+// of n tiles.  Units are dealt round-robin to CTAs in row-block-major order, so CTAs that
+// run at the same time share the same B tiles (and A blocks) in L2.  An epilogue may keep
+// per-row state across the tiles of a unit (the forward's running logsumexp).
+//
+// Every wait is bounded (fkl_ptx.cuh): when one runs out, the kernel records
+// FKL_ERR_TIMEOUT in the status word, every role stops, in-flight copies and MMAs are
+// drained and TMEM is freed before the CTA exits.
+#pragma once
+
+#include <climits>
+#include <cmath>
+
+#include "fkl_ptx.cuh"
+
+namespace fkl {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+
+__host__ __device__ constexpr int stages_for(int bn) { return bn == 256 ? 4 : (bn == 192 ? 5 : 6); }
+__host__ __device__ constexpr size_t smem_bytes_for(int bn) {
+  return static_cast<size_t>(stages_for(bn)) * (kBM * kBK * 2 + bn * kBK * 2) + 1024 + 256;
+}
+
+__device__ __forceinline__ void unit_range(const GemmShape& g, int u, int& m_blk, int& n_begin,
+                                           int& n_end, int& split) {
+  m_blk = u / g.nsplit;
+  split = u - m_blk * g.nsplit;
+  n_begin = static_cast<int>(static_cast<long long>(split) * g.n_tiles / g.nsplit);
+  n_end = static_cast<int>(static_cast<long long>(split + 1) * g.n_tiles / g.nsplit);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void pin(float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) asm volatile("" : "+f"(v[j]));
+}
+
+// ------------------------------------------------------------------ top-K cursor
+// Walks one row's (id, p) pairs, sorted by id, in step with the vocabulary tiles.
+struct TopkCursor {
+  const int2* rowp;
+  int K, kp, nid;
+  float pn;
+
+  __device__ __forceinline__ void next() {
+    ++kp;
+    if (kp < K) {
+      const int2 e = __ldg(rowp + kp);
+      nid = e.x;
+      pn = __int_as_float(e.y);
+    } else {
+      nid = INT_MAX;
+    }
+  }
+  // Positions the cursor on the first pair whose id is >= col.
+  __device__ __forceinline__ void seek(const int2* row, int k, int col) {
+    rowp = row;
+    K = k;
+    int lo = 0, hi = k;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(&row[mid].x) < col) lo = mid + 1; else hi = mid;
+    }
+    kp = lo - 1;
+    next();
+  }
+  __device__ __forceinline__ void none() { nid = INT_MAX; }
+};
+
+// Value of v[j] for a run-time j without indexing registers dynamically.
+__device__ __forceinline__ float pick(const float (&v)[32], int j) {
+  float r = 0.f;
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) r = (jj == j) ? v[jj] : r;
+  return r;
+}
+
+// ------------------------------------------------------------------ forward epilogue
+// Per row of the unit: running base-2 max m2 and sum l of exp2(s * log2(e)/tau - m2) over
+// the vocabulary columns of the unit, and g = sum of p_k * s at the teacher ids that fall
+// in the unit.  Columns >= V (zero rows that TMA filled in) are excluded.
+struct EpiFwd {
+  using Params = FwdParams;
+  const Params& p;
+  int t;
+  bool row_ok;
+  float m2, l, g;
+  TopkCursor cur;
+
+  __device__ explicit EpiFwd(const Params& prm) : p(prm) {}
+
+  __device__ __forceinline__ void begin_unit(int m_blk, int n_begin, int /*split*/, int row) {
+    t = m_blk * kBM + row;
+    row_ok = t < p.T;
+    m2 = -INFINITY;
+    l = 0.f;
+    g = 0.f;
+    if (row_ok) cur.seek(p.pairs + static_cast<size_t>(t) * p.K, p.K, n_begin * kVocabTile);
+    else cur.none();
+  }
+
+  __device__ __forceinline__ void chunk(float (&v)[32], int col0) {
+    if (col0 + 32 > p.V) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j >= p.V) v[j] = -INFINITY;
+    }
+    while (cur.nid < col0 + 32) {  // teacher ids inside this 32-column chunk (rare)
+      g = fmaf(cur.pn, pick(v, cur.nid - col0), g);
+      cur.next();
+    }
+    float c0 = fmaxf(v[0], v[1]), c1 = fmaxf(v[2], v[3]);
+#pragma unroll
+    for (int j = 4; j < 32; j += 2) {
+      c0 = fmaxf(c0, v[j]);
+      c1 = fmaxf(c1, v[j + 1]);
+    }
+    const float new_m = fmaxf(m2, fmaxf(c0, c1) * p.scale2);
+    if (new_m == -INFINITY) return;  // nothing inside the vocabulary yet
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      s0 += ex2_approx(fmaf(v[j + 0], p.scale2, -new_m));
+      s1 += ex2_approx(fmaf(v[j + 1], p.scale2, -new_m));
+      s2 += ex2_approx(fmaf(v[j + 2], p.scale2, -new_m));
+      s3 += ex2_approx(fmaf(v[j + 3], p.scale2, -new_m));
+    }
+    l = fmaf(l, ex2_approx(m2 - new_m), (s0 + s1) + (s2 + s3));
+    m2 = new_m;
+  }
+
+  template <int BN>
+  __device__ __forceinline__ void tile(uint32_t taddr, int n, int /*row*/) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; c += 2) {
+      float v0[32], v1[32];
+      tmem_ld32(taddr + c * 32, v0);
+      tmem_ld32(taddr + c * 32 + 32, v1);
+      tmem_wait_ld();
+      pin(v0);
+      pin(v1);
+      chunk(v0, n * BN + c * 32);
+      chunk(v1, n * BN + c * 32 + 32);
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(int split, int /*row*/) {
+    if (!row_ok) return;
+    const size_t plane = static_cast<size_t>(p.nsplit) * p.T;
+    const size_t i = static_cast<size_t>(split) * p.T + t;
+    p.part[i] = m2;
+    p.part[plane + i] = l;
+    p.part[2 * plane + i] = g;
+  }
+};
+
+// ------------------------------------------------------------------ backward dS epilogue
+// dS[t, v] = dscale * (exp2(s * log2(e)/tau - lse_t * log2(e)) - ptilde[t, v]) for valid
+// rows, 0 for masked rows, rounded to bf16 and written to the slab buffer.
+struct EpiDs {
+  using Params = DsParams;
+  const Params& p;
+  int t;
+  bool row_ok;
+  float lse2, f;
+  uint16_t* dst;
+  TopkCursor cur;
+
+  __device__ explicit EpiDs(const Params& prm) : p(prm) {}
+
+  __device__ __forceinline__ void begin_unit(int m_blk, int n_begin, int /*split*/, int row) {
+    t = m_blk * kBM + row;
+    row_ok = t < p.T;
+    if (row_ok) {
+      lse2 = p.lse[t] * 1.4426950408889634f;
+      const bool valid = (p.mask == nullptr) || (p.mask[t] != 0);
+      f = valid ? p.hdr->dscale : 0.f;
+      dst = p.ds + static_cast<size_t>(t) * p.ld_ds;
+      cur.seek(p.pairs + static_cast<size_t>(t) * p.K, p.K, p.v0 + n_begin * kVocabTile);
+    } else {
+      lse2 = 0.f;
+      f = 0.f;
+      dst = nullptr;
+      cur.none();
+    }
+  }
+
+  __device__ __forceinline__ void chunk(float (&v)[32], int cl0) {
+    const int cg0 = p.v0 + cl0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], p.scale2, -lse2));
+    while (cur.nid < cg0 + 32) {  // subtract p at the teacher ids in this chunk (rare)
+      const int jt = cur.nid - cg0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j == jt) v[j] -= cur.pn;
+      cur.next();
+    }
+    if (cl0 + 32 > p.slab_w) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (cl0 + j >= p.slab_w) v[j] = 0.f;
+    }
+    if (!row_ok) return;
+    uint4* o = reinterpret_cast<uint4*>(dst + cl0);
+    if (f == 0.f) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 w;
+      w.x = pack_bf16x2(f * v[8 * j + 0], f * v[8 * j + 1]);
+      w.y = pack_bf16x2(f * v[8 * j + 2], f * v[8 * j + 3]);
+      w.z = pack_bf16x2(f * v[8 * j + 4], f * v[8 * j + 5]);
+      w.w = pack_bf16x2(f * v[8 * j + 6], f * v[8 * j + 7]);
+      o[j] = w;
+    }
+  }
+
+  template <int BN>
+  __device__ __forceinline__ void tile(uint32_t taddr, int n, int /*row*/) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; c += 2) {
+      float v0[32], v1[32];
+      tmem_ld32(taddr + c * 32, v0);
+      tmem_ld32(taddr + c * 32 + 32, v1);
+      tmem_wait_ld();
+      pin(v0);
+      pin(v1);
+      chunk(v0, n * BN + c * 32);
+      chunk(v1, n * BN + c * 32 + 32);
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(int, int) {}
+};
+
+// ------------------------------------------------------------------ fp32 store epilogue
+struct EpiF32 {
+  using Params = F32Params;
+  const Params& p;
+  bool row_ok;
+  float* rowp;
+
+  __device__ explicit EpiF32(const Params& prm) : p(prm) {}
+
+  __device__ __forceinline__ void begin_unit(int m_blk, int, int, int row) {
+    const int r = m_blk * kBM + row;
+    row_ok = r < p.M;
+    rowp = p.out + static_cast<size_t>(row_ok ? r : 0) * p.ldo;
+  }
+
+  template <int BN>
+  __device__ __forceinline__ void tile(uint32_t taddr, int n, int) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = n * BN + c * 32;
+      if (col0 >= p.N) break;  // same for the whole warp
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      tmem_ld_wait(v);
+      if (!row_ok) continue;
+      float* o = rowp + col0;
+      if (p.vec_ok && col0 + 32 <= p.N) {
+        float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float4 x = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if (p.accumulate) {
+            const float4 y = o4[j];
+            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+          }
+          o4[j] = x;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (col0 + j < p.N) o[j] = p.accumulate ? o[j] + v[j] : v[j];
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(int, int) {}
+};
+
+// ------------------------------------------------------------------ the kernel
+template <int BN, bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmShape g, const __grid_constant__ typename Epi::Params ep) {
+  constexpr int STAGES = stages_for(BN);
+  constexpr uint32_t A_BYTES = kBM * kBK * 2;  // 16 KB
+  constexpr uint32_t B_BYTES = BN * kBK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t BOX_BYTES = 64 * kBK * 2;  // one 64 x 64 MN-major box, 8 KB
+  constexpr uint32_t IDESC = instr_desc_bf16(kBM, BN, A_MN, B_MN);
+  static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators must fit in TMEM");
+  static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column boxes");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);  // [0] TMEM base, [1] abort
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t stage0 = smem_addr(smem);
+  const uint32_t full0 = smem_addr(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 4 * 32);
+    }
+    mbar_init(drain, 1);
+    misc[1] = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const WaitCtl ctl{reinterpret_cast<volatile uint32_t*>(&misc[1]), g.status, g.limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+        int m_blk, nb, ne, split;
+        unit_range(g, u, m_blk, nb, ne, split);
+        for (int n = nb; ok && n < ne; ++n) {
+          for (int kb = 0; kb < g.k_blocks; ++kb) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, ctl)) { ok = false; break; }
+            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t sa = stage0 + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+            const int k0 = kb * kBK;
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            if (!A_MN) {
+              tma_load_2d(sa, &tmA, fb, k0, m_blk * kBM);
+            } else {
+              tma_load_2d(sa, &tmA, fb, m_blk * kBM, k0);
+              tma_load_2d(sa + BOX_BYTES, &tmA, fb, m_blk * kBM + 64, k0);
+            }
+            if (!B_MN) {
+              tma_load_2d(sb, &tmB, fb, k0, n * BN);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmB, fb, n * BN + j * 64, k0);
+            }
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+      // Every copy this thread started must land before the CTA may exit.
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) mbar_wait_drain(full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+        int m_blk, nb, ne, split;
+        unit_range(g, u, m_blk, nb, ne, split);
+        for (int n = nb; ok && n < ne; ++n) {
+          if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kb = 0; kb < g.k_blocks; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = stage0 + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              // K-major: the 16-element step moves 32 bytes along the swizzled 128-byte row.
+              // MN-major: it moves 16 rows of 128 bytes; 64-wide MN blocks are 8 KB apart.
+              const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, BOX_BYTES, 1024)
+                                       : smem_desc_sw128(sa + k * 32, 16, 1024);
+              const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, BOX_BYTES, 1024)
+                                       : smem_desc_sw128(sb + k * 32, 16, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
+            tc_commit(empty0 + 8 * stage);  // slot is free once these MMAs have read it
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit(tfull0 + 8 * acc);  // accumulator complete
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      // Every MMA issued must finish before TMEM is released.
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0u, g.limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane = row of the 128-row tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    Epi epi(ep);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+      int m_blk, nb, ne, split;
+      unit_range(g, u, m_blk, nb, ne, split);
+      epi.begin_unit(m_blk, nb, split, row);
+      for (int n = nb; n < ne; ++n) {
+        const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, ctl);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after();
+        epi.template tile<BN>(tmem_base + lane_base + static_cast<uint32_t>(acc * BN), n, row);
+        tc_fence_before();
+        mbar_arrive(tempty0 + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (ok) epi.end_unit(split, row);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BN, bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
+                          const typename Epi::Params& ep, int grid, cudaStream_t st) {
+  constexpr size_t SMEM = smem_bytes_for(BN);
+  auto kern = gemm_kernel<BN, A_MN, B_MN, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, SMEM, st>>>(a, b, g, ep);
+  return cudaGetLastError();
+}
+
+}  // namespace fkl

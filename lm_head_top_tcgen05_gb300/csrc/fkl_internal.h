@@ -1,0 +1,109 @@
+// Declarations shared by the translation units of the fused chunked KL library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fkl {
+
+// Bits of the device status word (first 4 bytes of the workspace).
+constexpr uint32_t kStatusBadIdBit = 1u;
+constexpr uint32_t kStatusBadRowBit = 2u;
+constexpr uint32_t kStatusTimeoutBit = 4u;
+
+// Workspace header (first 256 bytes): status word, valid-token count, dS scale.
+struct WsHeader {
+  uint32_t status;
+  int32_t n_valid;
+  float dscale;  // g * tau / N (0 when N = 0)
+  float pad;
+};
+
+constexpr int kVocabTile = 256;                   // tile width of the vocabulary axis
+constexpr int kMaxSplit = 32;                     // most vocabulary splits per row block
+constexpr uint64_t kWaitLimitNs = 5000000000ull;  // per pipeline wait
+
+// Where each buffer lives inside the caller's workspace, and the backward's slabbing.
+struct Plan {
+  int64_t T, d, V, K, chunk;
+  int64_t Vc;      // vocabulary columns per backward slab (multiple of kVocabTile)
+  int64_t nslabs;  // number of backward slabs
+  int64_t nb;      // row blocks of the combine step (256 rows each)
+  size_t off_pairs, off_crow, off_part, off_bsum, off_bcnt, off_ds, total;
+};
+
+bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p);
+
+// Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.
+int plan_splits(int m_tiles, int n_tiles, int sms);
+
+// ---------------------------------------------------------------- small kernels
+cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t T, int K, int V, float tau,
+                        int2* pairs, float* crow, uint32_t* status, cudaStream_t st);
+cudaError_t launch_combine(const float* part, int nsplit, const float* crow, const uint8_t* mask,
+                           int64_t T, float tau, float* lse, double* bsum, int* bcnt, int64_t nb,
+                           WsHeader* hdr, float* loss, cudaStream_t st);
+cudaError_t launch_bwd_scalars(const uint8_t* mask, int64_t T, const float* grad, float tau,
+                               WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_poison(float* a, int64_t na, float* b, int64_t nb, const uint32_t* status,
+                          int sms, cudaStream_t st);
+cudaError_t launch_wait_timeout_test(uint32_t* status, uint64_t limit_ns, cudaStream_t st);
+
+// ---------------------------------------------------------------- GEMMs
+// Problem of one persistent tcgen05 GEMM launch: D[M, N] = A[M, Kd] * B[N, Kd]^T in
+// 128 x BN tiles.  A unit is one 128-row block and a contiguous range of n tiles.
+struct GemmShape {
+  int M, N, Kd;
+  int m_tiles, n_tiles, k_blocks;
+  int nsplit;     // units per 128-row block
+  int num_units;  // m_tiles * nsplit
+  uint32_t* status;
+  uint64_t limit_ns;
+};
+
+GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status);
+
+// Forward: online base-2 logsumexp and top-K gather per (row, vocabulary split).
+struct FwdParams {
+  const int2* pairs;  // [T][K] (id, p) sorted by id
+  float* part;        // [3][nsplit][T]: running max (base 2), sum, gather
+  int T, K, V, nsplit;
+  float scale2;       // log2(e) / tau
+};
+
+// Backward recompute: dS = dscale * (q - ptilde) for one vocabulary slab, bf16.
+struct DsParams {
+  const int2* pairs;
+  const float* lse;
+  const uint8_t* mask;
+  const WsHeader* hdr;
+  uint16_t* ds;       // [T][ld_ds]
+  int64_t ld_ds;
+  int T, K, V, v0, slab_w;
+  float scale2;       // log2(e) / tau
+};
+
+// Plain fp32 output tile: store or accumulate.
+struct F32Params {
+  float* out;
+  int64_t ldo;
+  int M, N;
+  int accumulate;
+  int vec_ok;  // ldo and base allow 16-byte vector access
+};
+
+bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+cudaError_t launch_gemm_fwd(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
+                            const FwdParams& ep, int grid, cudaStream_t st);
+cudaError_t launch_gemm_ds(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
+                           const DsParams& ep, int grid, cudaStream_t st);
+// F32-output GEMM for bn in {256, 192, 128} and either major-ness of A and B.
+cudaError_t launch_gemm_f32(int bn, bool a_mn, bool b_mn, const CUtensorMap& a,
+                            const CUtensorMap& b, const GemmShape& g, const F32Params& ep,
+                            int grid, cudaStream_t st);
+
+}  // namespace fkl

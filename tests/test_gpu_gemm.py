@@ -1,0 +1,74 @@
+"""The tcgen05 GEMM building block (TMA -> shared memory -> tcgen05.mma -> TMEM -> fp32)
+against a float64 host product of the same bf16 operands, for every operand major-ness
+and tile width the loss uses, on ragged shapes that leave partial tiles on every axis."""
+import ctypes
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L(cuda_device):
+    from lm_head_top_tcgen05_gb300 import build
+    from lm_head_top_tcgen05_gb300._lib import lib
+
+    build.build()
+    return lib()
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(M, Kd, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, Kd, generator=g).to(torch.bfloat16)
+    D0 = torch.randn(M, N, generator=g) if accumulate else torch.zeros(M, N)
+    Ad = (A.t().contiguous() if a_mn else A).cuda()
+    Bd = (B.t().contiguous() if b_mn else B).cuda()
+    D = D0.clone().cuda()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    st = L.fkl_test_gemm(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, Kd, int(a_mn), int(b_mn), bn,
+                         int(accumulate), ws.data_ptr(), 256, _stream())
+    assert st == 0, L.fkl_last_error()
+    assert L.fkl_read_status(ws.data_ptr(), _stream()) == 0
+    ref = A.double() @ B.double().T + D0.double()
+    err = ((D.cpu().double() - ref).abs().max() / ref.abs().max()).item()
+    return err
+
+
+def test_single_tile_k_major(L):
+    assert run_gemm(L, 128, 256, 64, False, False, 256) < 1e-5
+
+
+@pytest.mark.parametrize("bn", [256, 192, 128])
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
+def test_ragged_all_majors(L, a_mn, b_mn, bn):
+    assert run_gemm(L, 304, 520, 200, a_mn, b_mn, bn) < 1e-5
+
+
+@pytest.mark.parametrize("a_mn,b_mn,bn", [(False, False, 256), (True, True, 192), (False, True, 192)])
+def test_many_waves(L, a_mn, b_mn, bn):
+    # more tiles than SMs: wraps the shared-memory ring and both TMEM accumulators many times
+    assert run_gemm(L, 2048, 3072, 1024, a_mn, b_mn, bn, seed=3) < 2e-5
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, True), (True, True)])
+def test_accumulate(L, a_mn, b_mn):
+    assert run_gemm(L, 256, 384, 136, a_mn, b_mn, 192, accumulate=True, seed=5) < 1e-5
+
+
+def test_long_k(L):
+    # the dW product has K = T, thousands of k-blocks per tile
+    assert run_gemm(L, 256, 192, 16384, True, True, 192, seed=7) < 5e-5
+
+
+def test_timeout_probe_reports_status(L):
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert L.fkl_test_wait_timeout(2_000_000, ws.data_ptr(), 256, _stream()) == 0
+    assert L.fkl_read_status(ws.data_ptr(), _stream()) == 8  # FKL_ERR_TIMEOUT
+    # the context is still usable afterwards
+    assert run_gemm(L, 128, 256, 64, False, False, 256) < 1e-5

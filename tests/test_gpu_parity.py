@@ -1,0 +1,190 @@
+"""CUDA path against the float64 oracle, element by element, on seeded inputs.
+
+Tolerances (fixed for the loss): loss relative error <= 1e-3, lse absolute error <= 1e-3 on
+every row, dH and dW relative Frobenius error <= 2e-2 and max-abs error <= 5e-2 * max|ref|.
+Shapes span several tiles on every axis and leave ragged tails (T not a multiple of 128,
+V not a multiple of 256, d not a multiple of 64), plus the degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+LOSS_RTOL, LSE_ATOL, FRO_RTOL, MAX_FRAC = 1e-3, 1e-3, 2e-2, 5e-2
+
+
+@pytest.fixture(scope="module")
+def fkl(cuda_device):
+    from lm_head_top_tcgen05_gb300 import build
+
+    build.build()
+    import lm_head_top_tcgen05_gb300 as m
+
+    return m
+
+
+def to_dev(x, dev="cuda"):
+    return (x.H.to(dev), x.W.to(dev), x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev))
+
+
+def run_gpu(fkl, x, chunk=None, grad=None):
+    H, W, idx, z, m = to_dev(x)
+    chunk = x.chunk if chunk is None else chunk
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, chunk)
+    g = None if grad is None else torch.tensor(grad, dtype=torch.float32, device="cuda")
+    dH, dW = fkl.backward(H, W, idx, z, m, lse, g, x.tau, chunk)
+    torch.cuda.synchronize()
+    status = fkl.read_status(device="cuda")
+    return dict(loss=loss.item(), lse=lse.cpu().numpy().astype(np.float64), dH=dH.cpu().numpy().astype(np.float64),
+                dW=dW.cpu().numpy().astype(np.float64), status=status)
+
+
+def run_oracle(x, grad=1.0):
+    H64, W64 = oracle.to_f64(x.H), oracle.to_f64(x.W)
+    f = oracle.forward(H64, W64, x.topk_idx, x.topk_logits, x.mask, x.tau)
+    dH, dW = oracle.backward(H64, W64, x.topk_idx, x.topk_logits, x.mask, x.tau, grad=grad)
+    return dict(loss=f["loss"], lse=f["lse"], dH=dH, dW=dW)
+
+
+def assert_grad_close(G, R, name):
+    nr = np.linalg.norm(R)
+    if nr == 0:
+        assert np.max(np.abs(G)) == 0, name
+        return
+    fro = np.linalg.norm(G - R) / nr
+    mx = np.max(np.abs(G - R)) / np.max(np.abs(R))
+    assert fro <= FRO_RTOL, f"{name}: relative Frobenius error {fro:.3e}"
+    assert mx <= MAX_FRAC, f"{name}: max-abs error {mx:.3e} of max|ref|"
+
+
+def assert_parity(gpu, ref):
+    assert gpu["status"] == 0
+    if ref["loss"] == 0:
+        assert gpu["loss"] == 0
+    else:
+        rel = abs(gpu["loss"] - ref["loss"]) / abs(ref["loss"])
+        assert rel <= LOSS_RTOL, f"loss {gpu['loss']} vs {ref['loss']} (rel {rel:.3e})"
+    if len(ref["lse"]):
+        err = np.max(np.abs(gpu["lse"] - ref["lse"]))
+        assert err <= LSE_ATOL, f"lse max abs error {err:.3e}"
+    assert_grad_close(gpu["dH"], ref["dH"], "dH")
+    assert_grad_close(gpu["dW"], ref["dW"], "dW")
+
+
+CASES = {
+    # name: (T, d, V, K, tau, chunk, mask_frac, seed)
+    "one_tile": (128, 64, 256, 4, 1.0, 128, 0.0, 1),
+    "ragged_all_axes": (300, 200, 5000, 16, 2.0, 128, 0.1, 2),
+    "small_vocab_many_slots": (130, 320, 1000, 50, 0.7, 4096, 0.0, 3),
+    "single_slot": (257, 136, 300, 1, 1.0, 64, 0.05, 4),
+    "one_token": (1, 64, 777, 8, 1.0, 1, 0.0, 5),
+    "wide_d": (200, 1152, 3000, 32, 1.3, 512, 0.0, 6),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_parity_small(fkl, name):
+    T, d, V, K, tau, chunk, mf, seed = CASES[name]
+    x = workloads.make_random(T, d, V, K, tau=tau, chunk=chunk, seed=seed, mask_frac=mf)
+    assert_parity(run_gpu(fkl, x), run_oracle(x))
+
+
+def test_parity_tiny_workload(fkl):
+    x = workloads.make_inputs("tiny")
+    assert_parity(run_gpu(fkl, x), run_oracle(x))
+
+
+def test_upstream_gradient_scales(fkl):
+    x = workloads.make_random(160, 128, 2000, 10, seed=8)
+    assert_parity(run_gpu(fkl, x, grad=-0.37), run_oracle(x, grad=-0.37))
+
+
+def test_deterministic(fkl):
+    x = workloads.make_random(300, 200, 5000, 16, tau=2.0, chunk=128, seed=2, mask_frac=0.1)
+    a, b = run_gpu(fkl, x), run_gpu(fkl, x)
+    assert a["loss"] == b["loss"]
+    for k in ("lse", "dH", "dW"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_chunk_invariance(fkl):
+    x = workloads.make_random(300, 200, 5000, 16, tau=1.0, seed=9)
+    ref = run_oracle(x)
+    outs = [run_gpu(fkl, x, chunk=c) for c in (1, 64, 300, 100000)]
+    for o in outs:
+        assert_parity(o, ref)
+    for o in outs[1:]:
+        assert o["loss"] == outs[0]["loss"]  # the forward does not depend on chunk at all
+        assert_grad_close(o["dW"], outs[0]["dW"], "dW across chunks")
+
+
+def test_masked_rows_have_zero_gradient(fkl):
+    x = workloads.make_random(256, 128, 3000, 12, seed=10, mask_frac=0.3)
+    g = run_gpu(fkl, x)
+    masked = x.mask.numpy() == 0
+    assert masked.sum() > 0
+    assert np.all(g["dH"][masked] == 0)
+    assert np.all(np.isfinite(g["lse"]))
+
+
+def test_no_valid_token(fkl):
+    x = workloads.make_random(100, 64, 1000, 8, seed=11)
+    x.mask[:] = 0
+    g = run_gpu(fkl, x)
+    assert g["loss"] == 0 and g["status"] == 0
+    assert not g["dH"].any() and not g["dW"].any()
+
+
+def test_empty_batch(fkl):
+    x = workloads.make_random(0, 64, 1000, 8, seed=12)
+    g = run_gpu(fkl, x)
+    assert g["loss"] == 0 and g["lse"].shape == (0,) and not g["dW"].any()
+
+
+def test_duplicate_ids_follow_per_slot_definition(fkl):
+    x = workloads.make_random(64, 64, 512, 6, seed=13)
+    x.topk_idx[5, 1] = x.topk_idx[5, 0]
+    x.topk_idx[9, 2:] = x.topk_idx[9, 1]
+    assert_parity(run_gpu(fkl, x), run_oracle(x))
+
+
+def test_minus_inf_teacher_slots(fkl):
+    x = workloads.make_random(64, 64, 512, 6, seed=14)
+    x.topk_logits[:, -2:] = -float("inf")
+    assert_parity(run_gpu(fkl, x), run_oracle(x))
+
+
+def test_bad_teacher_id_is_reported(fkl):
+    x = workloads.make_random(64, 64, 512, 6, seed=15)
+    x.topk_idx[3, 2] = 512
+    g = run_gpu(fkl, x)
+    assert g["status"] == 6 and np.isnan(g["loss"]) and np.isnan(g["dH"]).all()
+
+
+def test_teacher_row_without_finite_logit_is_reported(fkl):
+    x = workloads.make_random(64, 64, 512, 6, seed=16)
+    x.topk_logits[7, :] = -float("inf")
+    g = run_gpu(fkl, x)
+    assert g["status"] == 7 and np.isnan(g["loss"])
+
+
+def test_status_clears_on_next_good_call(fkl):
+    x = workloads.make_random(64, 64, 512, 6, seed=17)
+    assert run_gpu(fkl, x)["status"] == 0
+
+
+def test_autograd_wrapper(fkl):
+    x = workloads.make_random(200, 128, 2500, 10, tau=1.5, seed=18, mask_frac=0.1)
+    H, W, idx, z, m = to_dev(x)
+    H.requires_grad_(True)
+    W.requires_grad_(True)
+    loss = fkl.fused_kl(H, W, idx, z, m, tau=x.tau, chunk=64)
+    (2.0 * loss).backward()
+    ref = run_oracle(x, grad=2.0)
+    assert abs(loss.item() - ref["loss"]) / ref["loss"] <= LOSS_RTOL
+    assert H.grad.dtype == torch.bfloat16 and W.grad.dtype == torch.bfloat16
+    assert_grad_close(H.grad.double().cpu().numpy(), ref["dH"], "H.grad")
+    assert_grad_close(W.grad.double().cpu().numpy(), ref["dW"], "W.grad")
