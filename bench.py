@@ -1,0 +1,313 @@
+"""Benchmark of the fused chunked KL loss, forward + backward, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one forward + backward of the loss (every kernel of the path) over one batch of
+the named synthetic workload (default: the gpt-oss-20b-like student at 32K tokens, T=32768,
+d=2880, V=201088, K=100).  Prints one JSON line.
+
+* value: tokens/s over all ranks, inputs resident in HBM, timed with CUDA events on the
+  launching stream over exactly K steps after W warm-up steps, barrier + synchronize on both
+  sides, max over ranks.  Every input is larger than L2 (W alone is 1.16 GB), so no L2 flush
+  is needed between steps.
+* e2e: the same metric with the step's inputs (H, teacher cache, mask) copied host->device
+  from pinned memory and the loss copied back inside the timed region; W stays resident as
+  the model's LM-head weight.
+* roofline: the forward call (teacher prep + the fused projection/logsumexp GEMM + combine;
+  the GEMM is > 98% of it) timed with CUDA events inside the timed steps, against the
+  measured dense-bf16 tensor peak; and the whole step's 8*T*V*d against the same peak.
+* cpu_baseline: the float64 oracle, timed as it stands on the host cores, on a bounded
+  sample of the same workload (the first rows of the batch, full vocabulary).
+* --impl reference: the oracle alone, on the host cores, as the comparison arm.
+
+Under torchrun each rank runs its own batch on its own GPU (weak scaling); the only
+collective is the max over ranks of the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd tokens/s & TFLOP/s (8TVd) at T=32K,V=201088,d=2880; peak GiB"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, busy_mhz_floor: float = 0.0):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_rate(x, rows: int):
+    """Tokens/s of the float64 oracle (forward + backward) on the first `rows` tokens."""
+    import numpy as np
+
+    import oracle
+
+    W64 = oracle.to_f64(x.W)
+    H64 = oracle.to_f64(x.H[:rows])
+    idx, z, m = x.topk_idx[:rows], x.topk_logits[:rows], x.mask[:rows]
+    t0 = time.perf_counter()
+    oracle.forward(H64, W64, idx, z, m, x.tau)
+    oracle.backward(H64, W64, idx, z, m, x.tau)
+    dt = time.perf_counter() - t0
+    del W64, H64
+    cores = len(os.sched_getaffinity(0))
+    return rows / dt, dt, cores, np.__version__
+
+
+def run_reference(args, rank):
+    """The comparison arm: the float64 oracle on the host cores, bounded samples of the batch."""
+    import workloads
+
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w, rows=args.cpu_rows)
+    cpu_oracle_rate(x, min(8, args.cpu_rows))  # warm-up: BLAS threads, page-in
+    rates, secs = [], []
+    for _ in range(args.steps):
+        r, dt, cores, _ = cpu_oracle_rate(x, args.cpu_rows)
+        rates.append(r)
+        secs.append(dt)
+    value = statistics.median(rates)
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * w.T / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "V": w.V, "K": w.K, "tau": w.tau,
+                   "chunk": w.chunk},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {args.cpu_rows} tokens of the batch per step, full "
+                                   f"vocabulary, float64 forward+backward; ms_per_step extrapolates "
+                                   f"to T={w.T}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="gptoss20b_32k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=128, help="tokens in the CPU oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import lm_head_top_tcgen05_gb300 as fkl
+    import workloads
+
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w)
+    T, d, V, K = w.T, w.d, w.V, w.K
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- device-resident run
+    H, Wt = x.H.to(dev), x.W.to(dev)
+    idx, z, m = x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev)
+    ws = fkl.Workspace(dev)
+    dH = torch.empty((T, d), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    inputs_bytes = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+
+    def step():
+        loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws)
+        fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW))
+        return loss
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert fkl.read_status(ws) == 0, "device status not ok after warm-up"
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws)
+            ev[i][1].record(stream)
+            fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW))
+            ev[i][2].record(stream)
+        end.record(stream)
+        barrier()
+    elapsed = start.elapsed_time(end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = t.item()
+    status = fkl.read_status(ws)
+    peak_bytes = torch.cuda.max_memory_allocated(dev)
+    fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
+    bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
+    loss_val = loss.item()
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        hH = x.H.pin_memory()
+        hidx, hz, hm = x.topk_idx.pin_memory(), x.topk_logits.pin_memory(), x.mask.pin_memory()
+        hloss = torch.empty((), dtype=torch.float32).pin_memory()
+        h2d = hH.numel() * 2 + hidx.numel() * 4 + hz.numel() * 4 + hm.numel()
+
+        def e2e_step():
+            Hd = hH.to(dev, non_blocking=True)
+            idd, zd, md = hidx.to(dev, non_blocking=True), hz.to(dev, non_blocking=True), hm.to(dev, non_blocking=True)
+            l, s = fkl.forward(Hd, Wt, idd, zd, md, w.tau, w.chunk, workspace=ws)
+            fkl.backward(Hd, Wt, idd, zd, md, s, None, w.tau, w.chunk, workspace=ws, out=(dH, dW))
+            hloss.copy_(l, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        s1.record(stream)
+        barrier()
+        e2e_t = s0.elapsed_time(s1) / 1e3
+        if world > 1:
+            t = torch.tensor([e2e_t], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_t = t.item()
+        e2e = {"value": world * T * args.steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 4}
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    peaks, peak_kind = load_peaks()
+    ms_per_step = 1e3 * elapsed / args.steps
+    tokens_s = world * T * args.steps / elapsed
+    tflops = world * w.flops_fwd_bwd * args.steps / elapsed / 1e12
+    sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    burst = float(peaks["bf16_tflops"])
+    fwd_tflops = 2.0 * T * V * d / (fwd_ms / 1e3) / 1e12
+    nslabs = int(fkl.lib().fkl_backward_slabs(T, d, V, K, w.chunk))
+    launches_per_step = 4 + 3 + 3 * nslabs  # forward: prep, GEMM, 2 combine; backward: prep, scalars, poison, 3 per slab
+    clk = clocks.summary()
+    out = {
+        "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "chunk": w.chunk,
+                   "l2": "inputs larger than L2 (W is 1.16 GB); no flush"},
+        "tflops": tflops,
+        "tensor_frac_step": tflops / sustained,
+        "peak_gib": peak_bytes / 2**30,
+        "peak_gib_above_inputs": (peak_bytes - inputs_bytes) / 2**30,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "loss": loss_val, "status": status,
+        "roofline": {"bound": "tensor", "kernel": "fkl_forward (projection + logsumexp/top-K GEMM)",
+                     "achieved": fwd_tflops, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": fwd_tflops / sustained, "frac_of_burst": fwd_tflops / burst,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained",
+                     "flops_per_launch": 2.0 * T * V * d, "traffic": None},
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        rate, dt, cores, _ = cpu_oracle_rate(x, args.cpu_rows)
+        out["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": f"first {args.cpu_rows} tokens, full vocabulary, float64 "
+                                         f"forward+backward, {dt:.1f} s"}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -78,6 +78,12 @@ typedef enum fkl_status {
 size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
 
 /*
+ * Number of vocabulary slabs the backward pass walks for this shape: each slab is one
+ * dS-recompute GEMM, one dW GEMM and one dH GEMM launch.  0 for T = 0 or invalid shapes.
+ */
+int64_t fkl_backward_slabs(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
+
+/*
  * Forward pass: writes the scalar loss L to *loss (device float) and lse[t] (device
  * float[T], natural log of sum_v exp(s_tv / tau), defined for masked tokens too).
  *   H           bf16 [T, d]     student final hidden states

@@ -28,6 +28,7 @@ _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _SIGNATURES = {
     "fkl_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, _I64]),
+    "fkl_backward_slabs": (ctypes.c_int64, [_I64, _I64, _I64, _I64, _I64]),
     "fkl_forward": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float, _I64,
                                    _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,

@@ -218,6 +218,11 @@ size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t ch
   return make_plan(T, d, V, K, chunk, &p) ? p.total : 0;
 }
 
+int64_t fkl_backward_slabs(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk) {
+  Plan p;
+  return make_plan(T, d, V, K, chunk, &p) ? p.nslabs : 0;
+}
+
 const char* fkl_last_error(void) { return g_last_error.c_str(); }
 
 const char* fkl_status_string(int status) {
