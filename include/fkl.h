@@ -112,6 +112,32 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
                         size_t ws_bytes, void* stream);
 
 /*
+ * Forward pass for callers that cannot allocate device memory - for example a custom
+ * operator inside another runtime that owns the whole device memory pool and passes the op
+ * only its input and output tensors, or a latency-critical loop that must never call
+ * cudaMalloc.  The pages have no counterpart for this entry point: it is a packaging
+ * option of this library, not part of the method.
+ *
+ * Same results and arguments as fkl_forward, without `chunk` (the forward does not depend
+ * on it) and without a workspace: the scratch lives in a 64 MiB device array inside the
+ * library, which every GPU that loads the library keeps until the process exits.  Shapes
+ * whose forward scratch exceeds it (about T * (8K + 392) bytes; T up to about 56K tokens at
+ * K = 100) are rejected with FKL_ERR_WORKSPACE and a message in fkl_last_error().
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents (each call
+ *     clears what must start at zero): calls that overlap on the GPU - on different
+ *     streams or from different threads - race and must be serialised by the caller.
+ *   - It allocates nothing (no cudaMalloc or allocating library routine).  A device-side
+ *     error (bad teacher id or row, pipeline timeout) makes the loss NaN; its status word
+ *     is internal and cannot be read with fkl_read_status.
+ */
+fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                               const float* topk_logits, const uint8_t* mask, int64_t T,
+                               int64_t d, int64_t V, int64_t K, float tau, float* loss, float* lse,
+                               void* stream);
+
+/*
  * Waits for `stream`, then returns the device-side status recorded in `workspace` by the
  * most recent fkl_forward / fkl_backward call that used it (FKL_OK if none failed), or
  * FKL_ERR_CUDA if the wait or the read fails.

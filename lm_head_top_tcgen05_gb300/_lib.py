@@ -33,6 +33,8 @@ _SIGNATURES = {
                                    _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                     _I64, _P, _P, _P, ctypes.c_size_t, _P]),
+    "fkl_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                           _P, _P, _P]),
     "fkl_read_status": (ctypes.c_int, [_P, _P]),
     "fkl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fkl_last_error": (ctypes.c_char_p, []),

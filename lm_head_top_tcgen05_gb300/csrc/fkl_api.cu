@@ -27,6 +27,8 @@ static fkl_status fail(fkl_status s, const char* fmt, ...) {
   return s;
 }
 
+void set_last_error_message(const char* msg) { g_last_error = msg; }
+
 static fkl_status cuda_fail(cudaError_t e, const char* what) {
   return fail(FKL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }

@@ -34,6 +34,9 @@ struct Plan {
   size_t off_pairs, off_crow, off_part, off_bsum, off_bcnt, off_ds, total;
 };
 
+// Sets the message that fkl_last_error() returns on the calling thread.
+void set_last_error_message(const char* msg);
+
 bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p);
 
 // Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.
