@@ -13,9 +13,12 @@ d=2880, V=201088, K=100).  Prints one JSON line.
 * e2e: the same metric with the step's inputs (H, teacher cache, mask) copied host->device
   from pinned memory and the loss copied back inside the timed region; W stays resident as
   the model's LM-head weight.
-* roofline: the forward call (teacher prep + the fused projection/logsumexp GEMM + combine;
-  the GEMM is > 98% of it) timed with CUDA events inside the timed steps, against the
-  measured dense-bf16 tensor peak; and the whole step's 8*T*V*d against the same peak.
+* roofline: the tensor-core GEMM kind with the largest share of the step (forward
+  projection, dS recompute, dW or dH); each of its launches is timed with a CUDA event pair
+  that the library records on the launching stream during the timed steps (fkl_trace_*),
+  and its algorithmic FLOPs (2*M*N*K) per launch are divided by the mean launch time, against
+  the measured dense-bf16 tensor peak.  `tflops` / `tensor_frac_step` give the whole step's
+  8*T*V*d against the same peak.
 * cpu_baseline: the float64 oracle, timed as it stands on the host cores, on a bounded
   sample of the same workload (the first rows of the batch, full vocabulary).
 * --impl reference: the oracle alone, on the host cores, as the comparison arm.
@@ -26,6 +29,7 @@ collective is the max over ranks of the timing.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -147,6 +151,42 @@ def run_reference(args, rank):
     print(json.dumps(out), flush=True)
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over the ranks of the default process group (the value itself alone)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+KIND_NAMES = {0: "forward projection + logsumexp/top-K", 1: "dS recompute", 2: "dW", 3: "dH"}
+KERNEL_NAMES = {0: "gemm_kernel<256,0,0,EpiFwd>", 1: "gemm_kernel<256,0,0,EpiDs>",
+                2: "gemm_kernel<BN,1,1,EpiF32> (dW)", 3: "gemm_kernel<BN,0,1,EpiF32> (dH)"}
+
+
+def trace_summary(L, cap):
+    import ctypes
+
+    ms = (ctypes.c_float * cap)()
+    kind = (ctypes.c_int32 * cap)()
+    flops = (ctypes.c_double * cap)()
+    n = L.fkl_trace_read(ms, kind, flops, cap)
+    if n < 0:
+        raise RuntimeError("fkl_trace_read failed")
+    per = {}
+    for i in range(n):
+        a = per.setdefault(kind[i], [0, 0.0, 0.0])
+        a[0] += 1
+        a[1] += ms[i]
+        a[2] += flops[i]
+    return {k: {"launches": c, "ms_total": t, "ms_per_launch": t / c, "flops_per_launch": f / c,
+                "tflops": f / (t / 1e3) / 1e12} for k, (c, t, f) in sorted(per.items())}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -157,6 +197,9 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=128, help="tokens in the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="override V (profiling case with the full workload's per-launch GEMM shapes)")
+    ap.add_argument("--chunk", type=int, default=None, help="override chunk")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -180,6 +223,9 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     w = workloads.WORKLOADS[args.workload]
+    if args.vocab is not None or args.chunk is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_V{args.vocab or w.V}_chunk{args.chunk or w.chunk}",
+                                V=args.vocab or w.V, chunk=args.chunk or w.chunk)
     x = workloads.make_inputs(w)
     T, d, V, K = w.T, w.d, w.V, w.K
 
@@ -209,6 +255,9 @@ def main():
     assert fkl.read_status(ws) == 0, "device status not ok after warm-up"
     stream = torch.cuda.current_stream(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    nslabs = int(fkl.lib().fkl_backward_slabs(T, d, V, K, w.chunk))
+    trace_cap = args.steps * (1 + 3 * nslabs)
+    fkl.check(fkl.lib().fkl_trace_start(trace_cap), "fkl_trace_start")
     with ClockSampler(local_rank) as clocks:
         barrier()
         start = torch.cuda.Event(enable_timing=True)
@@ -222,11 +271,9 @@ def main():
             ev[i][2].record(stream)
         end.record(stream)
         barrier()
-    elapsed = start.elapsed_time(end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = t.item()
+    fkl.lib().fkl_trace_stop()
+    elapsed = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
+    kernels = trace_summary(fkl.lib(), trace_cap)
     status = fkl.read_status(ws)
     peak_bytes = torch.cuda.max_memory_allocated(dev)
     fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
@@ -257,11 +304,7 @@ def main():
             e2e_step()
         s1.record(stream)
         barrier()
-        e2e_t = s0.elapsed_time(s1) / 1e3
-        if world > 1:
-            t = torch.tensor([e2e_t], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_t = t.item()
+        e2e_t = max_over_ranks(s0.elapsed_time(s1) / 1e3, dev)
         e2e = {"value": world * T * args.steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": 4}
 
@@ -276,10 +319,9 @@ def main():
     tflops = world * w.flops_fwd_bwd * args.steps / elapsed / 1e12
     sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     burst = float(peaks["bf16_tflops"])
-    fwd_tflops = 2.0 * T * V * d / (fwd_ms / 1e3) / 1e12
-    nslabs = int(fkl.lib().fkl_backward_slabs(T, d, V, K, w.chunk))
     launches_per_step = 4 + 3 + 3 * nslabs  # forward: prep, GEMM, 2 combine; backward: prep, scalars, poison, 3 per slab
     clk = clocks.summary()
+    dom = max(kernels, key=lambda k: kernels[k]["ms_total"])  # largest share of the step
     out = {
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -291,11 +333,15 @@ def main():
         "peak_gib": peak_bytes / 2**30,
         "peak_gib_above_inputs": (peak_bytes - inputs_bytes) / 2**30,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "loss": loss_val, "status": status,
-        "roofline": {"bound": "tensor", "kernel": "fkl_forward (projection + logsumexp/top-K GEMM)",
-                     "achieved": fwd_tflops, "peak": sustained, "unit": "TFLOP/s",
-                     "frac": fwd_tflops / sustained, "frac_of_burst": fwd_tflops / burst,
-                     "peak_source": f"{peak_kind} bf16_tflops_sustained",
-                     "flops_per_launch": 2.0 * T * V * d, "traffic": None},
+        "roofline": {"bound": "tensor", "kernel": KERNEL_NAMES[dom],
+                     "achieved": kernels[dom]["tflops"], "peak": sustained, "unit": "TFLOP/s",
+                     "frac": kernels[dom]["tflops"] / sustained,
+                     "frac_of_burst": kernels[dom]["tflops"] / burst,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained (timed inside a seconds-long loop)",
+                     "flops_per_launch": kernels[dom]["flops_per_launch"],
+                     "ms_per_launch": kernels[dom]["ms_per_launch"], "traffic": None},
+        "kernels": {KIND_NAMES[k]: {kk: round(vv, 4) if isinstance(vv, float) else vv for kk, vv in v.items()}
+                    for k, v in kernels.items()},
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
     }

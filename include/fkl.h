@@ -144,6 +144,24 @@ fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32
  */
 fkl_status fkl_read_status(const void* workspace, void* stream);
 
+/*
+ * Per-launch timing for profiling.  After fkl_trace_start(capacity) the calling thread's
+ * fkl_forward and fkl_backward calls record a CUDA event pair on the caller's stream around
+ * each of their tensor-core GEMM launches, for the first `capacity` launches (1..65536);
+ * fkl_trace_stop() ends recording.  The events are created by the library when the trace
+ * starts (no device memory is allocated) and are released by the next fkl_trace_start.
+ */
+fkl_status fkl_trace_start(int32_t capacity);
+fkl_status fkl_trace_stop(void);
+
+/*
+ * Waits for the recorded events and writes, for up to `capacity` recorded launches in launch
+ * order, the duration in milliseconds (ms), the kind (0 forward projection + logsumexp,
+ * 1 dS recompute, 2 dW, 3 dH) and the launch's algorithmic FLOPs (2 * M * N * K of its
+ * product).  Any output pointer may be NULL.  Returns the number written, -1 on a CUDA error.
+ */
+int32_t fkl_trace_read(float* ms, int32_t* kind, double* flops, int32_t capacity);
+
 /* Static text for a status code. */
 const char* fkl_status_string(int status);
 

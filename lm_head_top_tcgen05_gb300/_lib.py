@@ -35,6 +35,9 @@ _SIGNATURES = {
                                     _I64, _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_forward_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                            _P, _P, _P]),
+    "fkl_trace_start": (ctypes.c_int, [ctypes.c_int32]),
+    "fkl_trace_stop": (ctypes.c_int, []),
+    "fkl_trace_read": (ctypes.c_int32, [_P, _P, _P, ctypes.c_int32]),
     "fkl_read_status": (ctypes.c_int, [_P, _P]),
     "fkl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fkl_last_error": (ctypes.c_char_p, []),

@@ -280,7 +280,9 @@ fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk
     fp.T = (int)T; fp.K = (int)K; fp.V = (int)V; fp.nsplit = nsplit;
     fp.scale2 = 1.4426950408889634f / tau;
     const int grid = g.num_units < di.sms ? g.num_units : di.sms;
+    trace_launch_begin(st);
     if ((e = launch_gemm_fwd(mH, mW, g, fp, grid, st)) != cudaSuccess) return cuda_fail(e, "forward GEMM");
+    trace_launch_end(st, 0, 2.0 * T * V * d);
     if ((e = launch_combine(part, nsplit, crow, mask, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st)) != cudaSuccess)
       return cuda_fail(e, "combine kernels");
   } else {
@@ -347,22 +349,29 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     dp.pairs = pairs; dp.lse = lse; dp.mask = mask; dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
     dp.T = (int)T; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
     dp.scale2 = 1.4426950408889634f / tau;
+    const double slab_flops = 2.0 * T * w * d;
+    trace_launch_begin(st);
     if ((e = launch_gemm_ds(mH_k, mW_k, g3, dp, g3.num_units < di.sms ? g3.num_units : di.sms, st)) != cudaSuccess)
       return cuda_fail(e, "dS GEMM");
+    trace_launch_end(st, 1, slab_flops);
 
     // dW[slab] = dS[:, slab]^T H  (complete for this slab: plain store).
     const GemmShape g4 = make_shape(w, d, T, bnd, (int)cdiv(d, bnd), &hdr->status);
     F32Params p4;
     p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d; p4.accumulate = 0; p4.vec_ok = 1;
+    trace_launch_begin(st);
     if ((e = launch_gemm_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, g4.num_units < di.sms ? g4.num_units : di.sms, st)) != cudaSuccess)
       return cuda_fail(e, "dW GEMM");
+    trace_launch_end(st, 2, slab_flops);
 
     // dH (+)= dS[:, slab] W[slab]  (slabs in order: deterministic accumulation).
     const GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status);
     F32Params p5;
     p5.out = dH; p5.ldo = d; p5.M = (int)T; p5.N = (int)d; p5.accumulate = j > 0 ? 1 : 0; p5.vec_ok = 1;
+    trace_launch_begin(st);
     if ((e = launch_gemm_f32(bnd, false, true, mD_k, mW_mn, g5, p5, g5.num_units < di.sms ? g5.num_units : di.sms, st)) != cudaSuccess)
       return cuda_fail(e, "dH GEMM");
+    trace_launch_end(st, 3, slab_flops);
   }
   if ((e = launch_poison(dH, T * d, dW, V * d, &hdr->status, di.sms, st)) != cudaSuccess)
     return cuda_fail(e, "poison kernel");

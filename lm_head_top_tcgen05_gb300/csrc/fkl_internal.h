@@ -37,6 +37,11 @@ struct Plan {
 // Sets the message that fkl_last_error() returns on the calling thread.
 void set_last_error_message(const char* msg);
 
+// Event pair around one GEMM launch when a trace is active on this thread (fkl_trace.cu).
+// kind: 0 forward, 1 dS recompute, 2 dW, 3 dH.
+void trace_launch_begin(cudaStream_t st);
+void trace_launch_end(cudaStream_t st, int kind, double flops);
+
 bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p);
 
 // Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.

@@ -1,0 +1,154 @@
+"""CUDA path against the oracle at the workloads' full sizes, in the launch configuration the
+benchmark times (same shapes, chunk, tiles and slabs).
+
+At these sizes the oracle cannot compute every output, so each run is checked on outputs it
+can compute one by one, and through properties that hold at any size:
+
+* lse of sampled rows (a full-vocabulary float64 logsumexp per row);
+* dH of sampled rows (row t of dH needs only row t of the logits);
+* the loss against tau^2/N * sum over valid rows of (sum_k p log p - sum_k p s_id / tau + lse_t),
+  with the teacher terms and the gathered student logits computed in float64 from the
+  inputs and lse from the run (itself checked on samples);
+* dW through the identity sum_t dH_t . H_t = sum_v dW_v . W_v (both equal sum dS * S) and
+  through sum_v dW_v = 0 (every valid row of dS sums to zero);
+* and, on the same shapes with a sparse mask (one valid token per 128-row block), the exact
+  loss and sampled rows of dW, which then need the logits of the valid rows only.
+
+Tolerances as in test_gpu_parity: loss relative 1e-3, lse absolute 1e-3, gradient rows
+relative Frobenius 2e-2 and max-abs 5e-2 of max |ref|."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+LOSS_RTOL, LSE_ATOL, FRO_RTOL, MAX_FRAC = 1e-3, 1e-3, 2e-2, 5e-2
+
+
+@pytest.fixture(scope="module")
+def fkl(cuda_device):
+    from lm_head_top_tcgen05_gb300 import build
+
+    build.build()
+    import lm_head_top_tcgen05_gb300 as m
+
+    return m
+
+
+def run_gpu(fkl, x, mask=None):
+    dev = "cuda"
+    H, W = x.H.to(dev), x.W.to(dev)
+    idx, z = x.topk_idx.to(dev), x.topk_logits.to(dev)
+    m = (x.mask if mask is None else mask).to(dev)
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk)
+    dH, dW = fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk)
+    torch.cuda.synchronize()
+    status = fkl.read_status(device=dev)
+    out = dict(loss=loss.item(), lse=lse.cpu().numpy().astype(np.float64), dH=dH.cpu(), dW=dW.cpu(),
+               status=status)
+    del H, W, idx, z, m, dH, dW
+    torch.cuda.empty_cache()
+    return out
+
+
+def sample_rows(T, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, T - 1, T // 2], rng.choice(T, n, replace=False)]))
+
+
+def close_rows(G, R, name):
+    fro = np.linalg.norm(G - R) / np.linalg.norm(R)
+    mx = np.max(np.abs(G - R)) / np.max(np.abs(R))
+    assert fro <= FRO_RTOL and mx <= MAX_FRAC, f"{name}: fro {fro:.3e}, max {mx:.3e}"
+
+
+def gathered_terms(x, W64, H64):
+    """Per row: c_t = sum_k p log p and g_t = sum_k p_k s_{t, id_k}, in float64."""
+    p, logp = oracle.teacher_probs(x.topk_logits, x.tau)
+    c = np.sum(np.where(p > 0, p * np.where(p > 0, logp, 0.0), 0.0), axis=1)
+    Wt = torch.from_numpy(W64)
+    E = torch.nn.functional.embedding_bag(x.topk_idx.long(), Wt, per_sample_weights=torch.from_numpy(p),
+                                          mode="sum").numpy()  # sum_k p_k W[id_k]
+    g = np.einsum("td,td->t", H64, E)
+    return c, g
+
+
+@pytest.mark.parametrize("name", ["llama3b_8k", "gptoss20b_32k", "packed4x16k_tau2"])
+def test_full_size(fkl, name):
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    gpu = run_gpu(fkl, x)
+    assert gpu["status"] == 0 and np.isfinite(gpu["loss"])
+    W64, H64 = oracle.to_f64(x.W), oracle.to_f64(x.H)
+
+    rows = sample_rows(w.T, 40, 1)
+    ref = oracle.forward(H64, W64, x.topk_idx, x.topk_logits, x.mask, w.tau, rows=rows)
+    assert np.max(np.abs(gpu["lse"][rows] - ref["lse"])) <= LSE_ATOL
+    dH_ref = oracle.dH_rows(H64, W64, x.topk_idx, x.topk_logits, x.mask, w.tau, rows)
+    valid_rows = rows[x.mask.numpy()[rows] != 0]
+    sel = np.isin(rows, valid_rows)
+    close_rows(gpu["dH"].numpy()[rows][sel].astype(np.float64), dH_ref[sel], "dH rows")
+    assert np.all(gpu["dH"].numpy()[rows][~sel] == 0)
+
+    c, g = gathered_terms(x, W64, H64)
+    valid = x.mask.numpy() != 0
+    kl = c - g / w.tau + gpu["lse"]
+    loss_prop = w.tau ** 2 * kl[valid].sum() / valid.sum()
+    assert abs(gpu["loss"] - loss_prop) <= LOSS_RTOL * abs(loss_prop)
+
+    dH64, dW64 = gpu["dH"].double(), gpu["dW"].double()
+    lhs = float((dH64 * x.H.double()).sum())
+    rhs = float((dW64 * x.W.double()).sum())
+    scale = float(dH64.abs().mul(x.H.double().abs()).sum())
+    assert abs(lhs - rhs) <= 1e-3 * scale, (lhs, rhs, scale)
+    colsum = dW64.sum(0).abs().max().item()
+    assert colsum <= 1e-3 * dW64.abs().sum(0).max().item()
+
+
+@pytest.mark.parametrize("name", ["gptoss20b_32k", "packed4x16k_tau2"])
+def test_full_size_sparse_mask_exact(fkl, name):
+    w = workloads.WORKLOADS[name]
+    x = workloads.make_inputs(w)
+    rng = np.random.default_rng(7)
+    mask = torch.zeros(w.T, dtype=torch.uint8)
+    valid = np.arange(0, w.T, 128) + rng.integers(0, 128, size=w.T // 128)
+    mask[valid] = 1
+    gpu = run_gpu(fkl, x, mask=mask)
+    assert gpu["status"] == 0
+    W64, H64 = oracle.to_f64(x.W), oracle.to_f64(x.H)
+    rows = np.unique(np.concatenate([valid, sample_rows(w.T, 16, 2)]))
+    ref = oracle.forward(H64, W64, x.topk_idx, x.topk_logits, mask, w.tau, rows=rows)
+    assert ref["loss"] is not None
+    assert abs(gpu["loss"] - ref["loss"]) <= LOSS_RTOL * abs(ref["loss"])
+    assert np.max(np.abs(gpu["lse"][rows] - ref["lse"])) <= LSE_ATOL
+    some = valid[:: max(1, len(valid) // 24)]
+    dH_ref = oracle.dH_rows(H64, W64, x.topk_idx, x.topk_logits, mask, w.tau, some)
+    close_rows(gpu["dH"].numpy()[some].astype(np.float64), dH_ref, "dH rows")
+    # dW rows: the teacher's ids of the valid rows (where p is scattered), random rows, the tail
+    hot = np.unique(x.topk_idx.numpy()[valid[:4]].ravel())[:24]
+    vr = np.unique(np.concatenate([hot, rng.choice(w.V, 24, replace=False), [0, w.V - 1]]))
+    dW_ref = oracle.dW_rows(H64, W64, x.topk_idx, x.topk_logits, mask, w.tau, vr)
+    close_rows(gpu["dW"].numpy()[vr].astype(np.float64), dW_ref, "dW rows")
+
+
+def test_long_context_256k(fkl):
+    w = workloads.WORKLOADS["gptoss20b_256k"]
+    x = workloads.make_inputs(w)
+    gpu = run_gpu(fkl, x)
+    assert gpu["status"] == 0 and np.isfinite(gpu["loss"])
+    W64 = oracle.to_f64(x.W)
+    rows = sample_rows(w.T, 24, 3)
+    H64 = oracle.to_f64(x.H[rows])
+    sub = dataclasses.replace(x, H=x.H[rows], topk_idx=x.topk_idx[rows], topk_logits=x.topk_logits[rows],
+                              mask=x.mask[rows])
+    ref = oracle.forward(H64, W64, sub.topk_idx, sub.topk_logits, None, w.tau)
+    assert np.max(np.abs(gpu["lse"][rows] - ref["lse"])) <= LSE_ATOL
+    # dH rows scale with 1/N: the oracle's per-row formula with N = T
+    dH_ref = oracle.dH_rows(H64, W64, sub.topk_idx, sub.topk_logits, None, w.tau, np.arange(len(rows)),
+                            grad=len(rows) / w.T)
+    close_rows(gpu["dH"].numpy()[rows].astype(np.float64), dH_ref, "dH rows")

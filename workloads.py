@@ -19,14 +19,19 @@ Every input is synthetic: there is no teacher model and no corpus.  The teacher 
 (top-K ids and logits per position, "Two systems changes", offline distillation) is
 drawn directly: K distinct ids per row and K logits sorted in descending order.
 
-Draw order per workload is fixed: W, H, (vocab permutation,) ids, logits, mask, all
-from ``numpy.random.default_rng(1000 + number)``.  Floats are drawn in float32 and H, W
-are rounded to bfloat16 with round-to-nearest-even (``torch.Tensor.to``).
+Every workload draws from ``numpy.random.SeedSequence(1000 + number)``, split into five
+child streams in a fixed order: W, H, ids (with the vocabulary permutation), logits, mask.
+W and H are drawn in blocks of 4096 rows, block b from child b of their stream, so blocks
+can be drawn on several threads and the first rows of H do not depend on how many rows are
+drawn.  Floats are drawn in float32 and H, W are rounded to bfloat16 with
+round-to-nearest-even (``torch.Tensor.to``).
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 from typing import Optional
 
 import numpy as np
@@ -99,6 +104,31 @@ def _normal_f32(rng: np.random.Generator, shape, std: float, mean: float = 0.0) 
         out *= np.float32(std)
     if mean != 0.0:
         out += np.float32(mean)
+    return out
+
+
+ROW_BLOCK = 4096
+
+
+def _normal_bf16_rows(seq: np.random.SeedSequence, rows: int, cols: int, std: float,
+                      keep: int) -> torch.Tensor:
+    """N(0, std^2) bf16 matrix [keep, cols]: the first `keep` of `rows` rows, block b of
+    ROW_BLOCK rows drawn from child b of `seq` (on several threads)."""
+    nblocks = (rows + ROW_BLOCK - 1) // ROW_BLOCK
+    children = seq.spawn(nblocks)
+    out = torch.empty((keep, cols), dtype=torch.bfloat16)
+    need = (keep + ROW_BLOCK - 1) // ROW_BLOCK
+
+    def block(b):
+        r0 = b * ROW_BLOCK
+        r1 = min(keep, r0 + ROW_BLOCK)
+        full = min(rows, r0 + ROW_BLOCK) - r0
+        x = _normal_f32(np.random.default_rng(children[b]), (full, cols), std)
+        out[r0:r1] = torch.from_numpy(x[: r1 - r0])
+
+    workers = max(1, min(16, len(os.sched_getaffinity(0))))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(block, range(need)))
     return out
 
 
@@ -195,20 +225,21 @@ def make_inputs(w: Workload | str, rows: Optional[int] = None) -> Inputs:
     """
     if isinstance(w, str):
         w = WORKLOADS[w]
-    rng = np.random.default_rng(w.seed)
-    W = torch.from_numpy(_normal_f32(rng, (w.V, w.d), w.w_std)).to(torch.bfloat16)
-    H = torch.from_numpy(_normal_f32(rng, (w.T, w.d), 1.0)).to(torch.bfloat16)
+    n = w.T if rows is None else rows
+    sW, sH, sI, sL, sM = np.random.SeedSequence(w.seed).spawn(5)
+    W = _normal_bf16_rows(sW, w.V, w.d, w.w_std, w.V)
+    H = _normal_bf16_rows(sH, w.T, w.d, 1.0, n)
+    rng = np.random.default_rng(sI)
     if w.ids == "uniform":
         idx = _distinct_uniform(rng, w.T, w.K, w.V)
     elif w.ids == "zipf80":
         idx = _zipf80_uniform20(rng, w.T, w.K, w.V)
     else:
         raise ValueError(w.ids)
-    logits = _normal_f32(rng, (w.T, w.K), w.logit_std, w.logit_mean)
+    logits = _normal_f32(np.random.default_rng(sL), (w.T, w.K), w.logit_std, w.logit_mean)
     logits = -np.sort(-logits, axis=1)
-    mask = _mask(w, rng)
-    n = w.T if rows is None else rows
-    return Inputs(H=H[:n].contiguous(), W=W,
+    mask = _mask(w, np.random.default_rng(sM))
+    return Inputs(H=H, W=W,
                   topk_idx=torch.from_numpy(idx[:n].astype(np.int32)),
                   topk_logits=torch.from_numpy(np.ascontiguousarray(logits[:n])),
                   mask=torch.from_numpy(mask[:n].copy()), tau=w.tau, chunk=w.chunk)
