@@ -20,13 +20,15 @@ extern "C" {
 
 /*
  * The tensor-core GEMM that the loss is built from, with a plain fp32 epilogue:
- *   D[M, N] (fp32, row-major, leading dimension N) = A B^T            if accumulate == 0
- *   D[M, N] += A B^T                                                   if accumulate != 0
+ *   D[M, N] (fp32, row-major, leading dimension N) = A B^T      if (accumulate & 1) == 0
+ *   D[M, N] += A B^T                                             if (accumulate & 1) != 0
  * A is logically [M, Kd] and B logically [N, Kd], both bfloat16.  a_mn_major = 0 means A is
  * stored [M][Kd] (Kd contiguous); 1 means stored [Kd][M] (M contiguous).  Likewise for B.
  * bn selects the tile width along N: 256, 192 or 128.  M, N, Kd >= 1; the contiguous
- * extent of each operand must be a multiple of 8.  `workspace` needs 256 bytes (the
- * status word).
+ * extent of each operand must be a multiple of 8.  An MN-major operand whose extent is a
+ * multiple of 64 is loaded with one 3-D TMA box per tile, unless bit 1 of `accumulate` is
+ * set (then 64-wide 2-D boxes, the path used for other extents).  Bit 0 of `accumulate`
+ * selects accumulation.  `workspace` needs 256 bytes (the status word).
  */
 fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N,
                          int64_t Kd, int a_mn_major, int b_mn_major, int bn, int accumulate,

@@ -104,6 +104,8 @@ GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint3
   g.k_blocks = static_cast<int>(cdiv(Kd, 64));
   g.nsplit = nsplit;
   g.num_units = g.m_tiles * nsplit;
+  g.a_box3d = 0;
+  g.b_box3d = 0;
   g.status = status;
   g.limit_ns = kWaitLimitNs;
   return g;
@@ -143,6 +145,19 @@ bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_map_mn3d(CUtensorMap* map, const void* base, uint64_t mn_extent, uint64_t k_extent,
+                     uint64_t row_stride_bytes, uint32_t tile_mn) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || mn_extent % 64 != 0 || tile_mn % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, k_extent, mn_extent / 64};
+  const cuuint64_t strides[2] = {row_stride_bytes, 128};
+  const cuuint32_t box[3] = {64, 64, tile_mn / 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- device info
 struct DevInfo {
   int sms = 0;
@@ -176,13 +191,17 @@ static fkl_status device_info(DevInfo* out) {
   return FKL_OK;
 }
 
+// Tile width along d for the dW and dH products: the width with the least estimated time,
+// counting padded columns and the measured relative cost per column of each width on GB300
+// (narrower tiles need more operand bytes per FLOP).
 static int choose_bn_d(int64_t d) {
   const int cand[3] = {256, 192, 128};
+  const double cost[3] = {1.0, 1.11, 1.4};
   int best = 256;
-  int64_t best_waste = INT64_MAX;
-  for (int bn : cand) {
-    const int64_t waste = cdiv(d, bn) * bn - d;
-    if (waste < best_waste) { best_waste = waste; best = bn; }
+  double best_t = 1e300;
+  for (int i = 0; i < 3; ++i) {
+    const double t = static_cast<double>(cdiv(d, cand[i]) * cand[i]) * cost[i];
+    if (t < best_t) { best_t = t; best = cand[i]; }
   }
   return best;
 }
@@ -326,19 +345,25 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     return cuda_fail(e, "prep kernel");
   if ((e = launch_bwd_scalars(mask, T, grad_loss, tau, hdr, st)) != cudaSuccess) return cuda_fail(e, "scalars kernel");
 
-  CUtensorMap mH_k, mH_mn;
-  if (!encode_map_bf16(&mH_k, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mH_mn, H, d, T, d * 2, 64, 64))
-    return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
   const int bnd = choose_bn_d(d);
+  CUtensorMap mH_k, mH_mn;
+  if (!encode_map_bf16(&mH_k, H, d, T, d * 2, 64, 128)) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
+  const bool h3d = encode_map_mn3d(&mH_mn, H, d, T, d * 2, bnd);
+  if (!h3d && !encode_map_bf16(&mH_mn, H, d, T, d * 2, 64, 64))
+    return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
   const int64_t Vc = pl.Vc;
   for (int64_t j = 0; j < pl.nslabs; ++j) {
     const int64_t v0 = j * Vc;
     const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
     const uint16_t* Wj = W + v0 * d;
     CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
+    // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
+    // 3-D view may span round_up(w, 64) columns.
+    const bool w3d = encode_map_mn3d(&mW_mn, Wj, d, w, d * 2, bnd);
+    const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, T, Vc * 2, 128);
     if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile) ||
-        !encode_map_bf16(&mW_mn, Wj, d, w, d * 2, 64, 64) ||
-        !encode_map_bf16(&mD_mn, ds, w, T, Vc * 2, 64, 64) ||
+        (!w3d && !encode_map_bf16(&mW_mn, Wj, d, w, d * 2, 64, 64)) ||
+        (!d3d && !encode_map_bf16(&mD_mn, ds, w, T, Vc * 2, 64, 64)) ||
         !encode_map_bf16(&mD_k, ds, w, T, Vc * 2, 64, 128))
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for slab %lld", (long long)j);
 
@@ -356,7 +381,9 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     trace_launch_end(st, 1, slab_flops);
 
     // dW[slab] = dS[:, slab]^T H  (complete for this slab: plain store).
-    const GemmShape g4 = make_shape(w, d, T, bnd, (int)cdiv(d, bnd), &hdr->status);
+    GemmShape g4 = make_shape(w, d, T, bnd, (int)cdiv(d, bnd), &hdr->status);
+    g4.a_box3d = d3d ? 1 : 0;
+    g4.b_box3d = h3d ? 1 : 0;
     F32Params p4;
     p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d; p4.accumulate = 0; p4.vec_ok = 1;
     trace_launch_begin(st);
@@ -365,7 +392,8 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     trace_launch_end(st, 2, slab_flops);
 
     // dH (+)= dS[:, slab] W[slab]  (slabs in order: deterministic accumulation).
-    const GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status);
+    GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status);
+    g5.b_box3d = w3d ? 1 : 0;
     F32Params p5;
     p5.out = dH; p5.ldo = d; p5.M = (int)T; p5.N = (int)d; p5.accumulate = j > 0 ? 1 : 0; p5.vec_ok = 1;
     trace_launch_begin(st);
@@ -413,14 +441,21 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   cudaError_t e = cudaMemsetAsync(workspace, 0, 256, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  // MN-major operands use one 3-D box per tile when their extent is a multiple of 64, unless
+  // bit 1 of `accumulate` asks for the 64-wide 2-D boxes.
+  const bool allow3d = (accumulate & 2) == 0;
   CUtensorMap mA, mB;
-  bool ok = a_mn_major ? encode_map_bf16(&mA, A, M, Kd, M * 2, 64, 64) : encode_map_bf16(&mA, A, Kd, M, Kd * 2, 64, 128);
-  ok = ok && (b_mn_major ? encode_map_bf16(&mB, B, N, Kd, N * 2, 64, 64)
-                         : encode_map_bf16(&mB, B, Kd, N, Kd * 2, 64, (uint32_t)bn));
+  const bool a3d = a_mn_major && allow3d && encode_map_mn3d(&mA, A, M, Kd, M * 2, 128);
+  const bool b3d = b_mn_major && allow3d && encode_map_mn3d(&mB, B, N, Kd, N * 2, (uint32_t)bn);
+  bool ok = a3d || (a_mn_major ? encode_map_bf16(&mA, A, M, Kd, M * 2, 64, 64) : encode_map_bf16(&mA, A, Kd, M, Kd * 2, 64, 128));
+  ok = ok && (b3d || (b_mn_major ? encode_map_bf16(&mB, B, N, Kd, N * 2, 64, 64)
+                                 : encode_map_bf16(&mB, B, Kd, N, Kd * 2, 64, (uint32_t)bn)));
   if (!ok) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for A or B");
-  const GemmShape g = make_shape(M, N, Kd, bn, (int)cdiv(N, bn), &hdr->status);
+  GemmShape g = make_shape(M, N, Kd, bn, (int)cdiv(N, bn), &hdr->status);
+  g.a_box3d = a3d ? 1 : 0;
+  g.b_box3d = b3d ? 1 : 0;
   F32Params p;
-  p.out = D; p.ldo = N; p.M = (int)M; p.N = (int)N; p.accumulate = accumulate ? 1 : 0;
+  p.out = D; p.ldo = N; p.M = (int)M; p.N = (int)N; p.accumulate = (accumulate & 1) ? 1 : 0;
   p.vec_ok = (N % 4 == 0 && aligned(D, 16)) ? 1 : 0;
   if ((e = launch_gemm_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p,
                            g.num_units < di.sms ? g.num_units : di.sms, st)) != cudaSuccess)

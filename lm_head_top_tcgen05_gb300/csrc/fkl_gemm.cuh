@@ -378,12 +378,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(fb, STAGE_BYTES);
             if (!A_MN) {
               tma_load_2d(sa, &tmA, fb, k0, m_blk * kBM);
+            } else if (g.a_box3d) {
+              tma_load_3d(sa, &tmA, fb, 0, k0, m_blk * (kBM / 64));
             } else {
               tma_load_2d(sa, &tmA, fb, m_blk * kBM, k0);
               tma_load_2d(sa + BOX_BYTES, &tmA, fb, m_blk * kBM + 64, k0);
             }
             if (!B_MN) {
               tma_load_2d(sb, &tmB, fb, k0, n * BN);
+            } else if (g.b_box3d) {
+              tma_load_3d(sb, &tmB, fb, 0, k0, n * (BN / 64));
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmB, fb, n * BN + j * 64, k0);

@@ -67,6 +67,8 @@ struct GemmShape {
   int m_tiles, n_tiles, k_blocks;
   int nsplit;     // units per 128-row block
   int num_units;  // m_tiles * nsplit
+  int a_box3d;    // MN-major A loaded by one 3-D box per tile (else 64-wide 2-D boxes)
+  int b_box3d;    // same for B
   uint32_t* status;
   uint64_t limit_ns;
 };
@@ -104,6 +106,11 @@ struct F32Params {
 
 bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// 3-D view of an MN-major operand stored [k][mn] (mn contiguous, mn_extent % 64 == 0 and
+// every element below mn_extent inside the buffer): dims (64, k, mn_extent / 64), box
+// (64, 64, tile_mn / 64).  Returns false if the map cannot be encoded.
+bool encode_map_mn3d(CUtensorMap* map, const void* base, uint64_t mn_extent, uint64_t k_extent,
+                     uint64_t row_stride_bytes, uint32_t tile_mn);
 
 cudaError_t launch_gemm_fwd(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
                             const FwdParams& ep, int grid, cudaStream_t st);

@@ -22,7 +22,7 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0):
+def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0, force2d=False):
     g = torch.Generator().manual_seed(seed)
     A = torch.randn(M, Kd, generator=g).to(torch.bfloat16)
     B = torch.randn(N, Kd, generator=g).to(torch.bfloat16)
@@ -31,8 +31,9 @@ def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0):
     Bd = (B.t().contiguous() if b_mn else B).cuda()
     D = D0.clone().cuda()
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    flags = int(accumulate) | (2 if force2d else 0)
     st = L.fkl_test_gemm(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, Kd, int(a_mn), int(b_mn), bn,
-                         int(accumulate), ws.data_ptr(), 256, _stream())
+                         flags, ws.data_ptr(), 256, _stream())
     assert st == 0, L.fkl_last_error()
     assert L.fkl_read_status(ws.data_ptr(), _stream()) == 0
     ref = A.double() @ B.double().T + D0.double()
@@ -54,6 +55,14 @@ def test_ragged_all_majors(L, a_mn, b_mn, bn):
 def test_many_waves(L, a_mn, b_mn, bn):
     # more tiles than SMs: wraps the shared-memory ring and both TMEM accumulators many times
     assert run_gemm(L, 2048, 3072, 1024, a_mn, b_mn, bn, seed=3) < 2e-5
+
+
+@pytest.mark.parametrize("force2d", [False, True])
+@pytest.mark.parametrize("bn", [256, 192, 128])
+def test_mn_major_box_paths(L, bn, force2d):
+    # extents that are multiples of 64 take one 3-D box per tile (M = 320: the last 128-row
+    # tile has one 64-wide block past the end, read as zeros); force2d takes 64-wide boxes
+    assert run_gemm(L, 320, 1344, 200, True, True, bn, force2d=force2d) < 1e-5
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(False, True), (True, True)])
