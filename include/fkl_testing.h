@@ -28,7 +28,9 @@ extern "C" {
  * extent of each operand must be a multiple of 8.  An MN-major operand whose extent is a
  * multiple of 64 is loaded with one 3-D TMA box per tile, unless bit 1 of `accumulate` is
  * set (then 64-wide 2-D boxes, the path used for other extents).  Bit 0 of `accumulate`
- * selects accumulation.  `workspace` needs 256 bytes (the status word).
+ * selects accumulation.  Bit 2 selects the two-SM kernel (CTA pairs, 256-row tiles, the one
+ * the loss uses; bn 256 or 128) instead of the one-SM kernel (128-row tiles).  `workspace`
+ * needs 256 bytes (the status word).
  */
 fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N,
                          int64_t Kd, int a_mn_major, int b_mn_major, int bn, int accumulate,

@@ -94,12 +94,13 @@ int plan_splits(int m_tiles, int n_tiles, int sms) {
   return best;
 }
 
-GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status) {
+GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status,
+                     int rows_per_unit) {
   GemmShape g;
   g.M = static_cast<int>(M);
   g.N = static_cast<int>(N);
   g.Kd = static_cast<int>(Kd);
-  g.m_tiles = static_cast<int>(cdiv(M, 128));
+  g.m_tiles = static_cast<int>(cdiv(M, rows_per_unit));
   g.n_tiles = static_cast<int>(cdiv(N, bn));
   g.k_blocks = static_cast<int>(cdiv(Kd, 64));
   g.nsplit = nsplit;
@@ -194,12 +195,13 @@ static fkl_status device_info(DevInfo* out) {
 // Tile width along d for the dW and dH products: the width with the least estimated time,
 // counting padded columns and the measured relative cost per column of each width on GB300
 // (narrower tiles need more operand bytes per FLOP).
-static int choose_bn_d(int64_t d) {
+static int choose_bn_d(int64_t d, bool pair) {
   const int cand[3] = {256, 192, 128};
   const double cost[3] = {1.0, 1.11, 1.4};
   int best = 256;
   double best_t = 1e300;
   for (int i = 0; i < 3; ++i) {
+    if (pair && cand[i] == 192) continue;  // the two-SM kernel splits B in 64-wide halves
     const double t = static_cast<double>(cdiv(d, cand[i]) * cand[i]) * cost[i];
     if (t < best_t) { best_t = t; best = cand[i]; }
   }
@@ -287,20 +289,20 @@ fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk
   if (T > 0) {
     if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st)) != cudaSuccess)
       return cuda_fail(e, "prep kernel");
+    // Two-SM tiles: each CTA of a pair loads 128 rows of H and 128 rows of the W tile.
     CUtensorMap mH, mW;
-    if (!encode_map_bf16(&mH, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, W, d, V, d * 2, 64, kVocabTile))
+    if (!encode_map_bf16(&mH, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, W, d, V, d * 2, 64, kVocabTile / 2))
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H or W");
-    const int m_tiles = (int)cdiv(T, 128), n_tiles = (int)cdiv(V, kVocabTile);
-    const int nsplit = plan_splits(m_tiles, n_tiles, di.sms);
-    const GemmShape g = make_shape(T, V, d, kVocabTile, nsplit, &hdr->status);
+    const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(V, kVocabTile);
+    const int nsplit = plan_splits(m_tiles, n_tiles, di.sms / 2);
+    const GemmShape g = make_shape(T, V, d, kVocabTile, nsplit, &hdr->status, 256);
     FwdParams fp;
     fp.pairs = pairs;
     fp.part = part;
     fp.T = (int)T; fp.K = (int)K; fp.V = (int)V; fp.nsplit = nsplit;
     fp.scale2 = 1.4426950408889634f / tau;
-    const int grid = g.num_units < di.sms ? g.num_units : di.sms;
     trace_launch_begin(st);
-    if ((e = launch_gemm_fwd(mH, mW, g, fp, grid, st)) != cudaSuccess) return cuda_fail(e, "forward GEMM");
+    if ((e = launch_gemm2_fwd(mH, mW, g, fp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "forward GEMM");
     trace_launch_end(st, 0, 2.0 * T * V * d);
     if ((e = launch_combine(part, nsplit, crow, mask, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st)) != cudaSuccess)
       return cuda_fail(e, "combine kernels");
@@ -345,10 +347,11 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     return cuda_fail(e, "prep kernel");
   if ((e = launch_bwd_scalars(mask, T, grad_loss, tau, hdr, st)) != cudaSuccess) return cuda_fail(e, "scalars kernel");
 
-  const int bnd = choose_bn_d(d);
+  // All three products use two-SM tiles (256 rows per CTA pair, B split between the CTAs).
+  const int bnd = choose_bn_d(d, true);
   CUtensorMap mH_k, mH_mn;
   if (!encode_map_bf16(&mH_k, H, d, T, d * 2, 64, 128)) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
-  const bool h3d = encode_map_mn3d(&mH_mn, H, d, T, d * 2, bnd);
+  const bool h3d = encode_map_mn3d(&mH_mn, H, d, T, d * 2, bnd / 2);
   if (!h3d && !encode_map_bf16(&mH_mn, H, d, T, d * 2, 64, 64))
     return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
   const int64_t Vc = pl.Vc;
@@ -359,45 +362,44 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
     // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
     // 3-D view may span round_up(w, 64) columns.
-    const bool w3d = encode_map_mn3d(&mW_mn, Wj, d, w, d * 2, bnd);
+    const bool w3d = encode_map_mn3d(&mW_mn, Wj, d, w, d * 2, bnd / 2);
     const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, T, Vc * 2, 128);
-    if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile) ||
+    if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) ||
         (!w3d && !encode_map_bf16(&mW_mn, Wj, d, w, d * 2, 64, 64)) ||
         (!d3d && !encode_map_bf16(&mD_mn, ds, w, T, Vc * 2, 64, 64)) ||
         !encode_map_bf16(&mD_k, ds, w, T, Vc * 2, 64, 128))
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for slab %lld", (long long)j);
 
     // dS[:, slab] = dscale * (q - ptilde), recomputing S = H W_slab^T.
-    const int m_tiles = (int)cdiv(T, 128), n_tiles = (int)cdiv(w, kVocabTile);
-    const GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms), &hdr->status);
+    const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(w, kVocabTile);
+    const GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
     DsParams dp;
     dp.pairs = pairs; dp.lse = lse; dp.mask = mask; dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
     dp.T = (int)T; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
     dp.scale2 = 1.4426950408889634f / tau;
     const double slab_flops = 2.0 * T * w * d;
     trace_launch_begin(st);
-    if ((e = launch_gemm_ds(mH_k, mW_k, g3, dp, g3.num_units < di.sms ? g3.num_units : di.sms, st)) != cudaSuccess)
-      return cuda_fail(e, "dS GEMM");
+    if ((e = launch_gemm2_ds(mH_k, mW_k, g3, dp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "dS GEMM");
     trace_launch_end(st, 1, slab_flops);
 
     // dW[slab] = dS[:, slab]^T H  (complete for this slab: plain store).
-    GemmShape g4 = make_shape(w, d, T, bnd, (int)cdiv(d, bnd), &hdr->status);
+    GemmShape g4 = make_shape(w, d, T, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
     g4.a_box3d = d3d ? 1 : 0;
     g4.b_box3d = h3d ? 1 : 0;
     F32Params p4;
     p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d; p4.accumulate = 0; p4.vec_ok = 1;
     trace_launch_begin(st);
-    if ((e = launch_gemm_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, g4.num_units < di.sms ? g4.num_units : di.sms, st)) != cudaSuccess)
+    if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
       return cuda_fail(e, "dW GEMM");
     trace_launch_end(st, 2, slab_flops);
 
     // dH (+)= dS[:, slab] W[slab]  (slabs in order: deterministic accumulation).
-    GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status);
+    GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
     g5.b_box3d = w3d ? 1 : 0;
     F32Params p5;
     p5.out = dH; p5.ldo = d; p5.M = (int)T; p5.N = (int)d; p5.accumulate = j > 0 ? 1 : 0; p5.vec_ok = 1;
     trace_launch_begin(st);
-    if ((e = launch_gemm_f32(bnd, false, true, mD_k, mW_mn, g5, p5, g5.num_units < di.sms ? g5.num_units : di.sms, st)) != cudaSuccess)
+    if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
       return cuda_fail(e, "dH GEMM");
     trace_launch_end(st, 3, slab_flops);
   }
@@ -428,6 +430,8 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
   if (M < 1 || N < 1 || Kd < 1 || M >= (1 << 30) || N >= (1 << 30) || Kd >= (1 << 30))
     return fail(FKL_ERR_INVALID_ARG, "M, N, Kd must be in [1, 2^30)");
   if (bn != 256 && bn != 192 && bn != 128) return fail(FKL_ERR_INVALID_ARG, "bn must be 256, 192 or 128");
+  const bool pair = (accumulate & 4) != 0;
+  if (pair && bn == 192) return fail(FKL_ERR_INVALID_ARG, "the two-SM kernel takes bn 256 or 128");
   const int64_t a_inner = a_mn_major ? M : Kd, b_inner = b_mn_major ? N : Kd;
   if (a_inner % 8 != 0 || b_inner % 8 != 0)
     return fail(FKL_ERR_ALIGNMENT, "the contiguous extent of A and B must be a multiple of 8");
@@ -445,21 +449,23 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
   // bit 1 of `accumulate` asks for the 64-wide 2-D boxes.
   const bool allow3d = (accumulate & 2) == 0;
   CUtensorMap mA, mB;
+  const uint32_t b_tile = pair ? (uint32_t)bn / 2 : (uint32_t)bn;  // B rows / columns per CTA
   const bool a3d = a_mn_major && allow3d && encode_map_mn3d(&mA, A, M, Kd, M * 2, 128);
-  const bool b3d = b_mn_major && allow3d && encode_map_mn3d(&mB, B, N, Kd, N * 2, (uint32_t)bn);
+  const bool b3d = b_mn_major && allow3d && encode_map_mn3d(&mB, B, N, Kd, N * 2, b_tile);
   bool ok = a3d || (a_mn_major ? encode_map_bf16(&mA, A, M, Kd, M * 2, 64, 64) : encode_map_bf16(&mA, A, Kd, M, Kd * 2, 64, 128));
   ok = ok && (b3d || (b_mn_major ? encode_map_bf16(&mB, B, N, Kd, N * 2, 64, 64)
-                                 : encode_map_bf16(&mB, B, Kd, N, Kd * 2, 64, (uint32_t)bn)));
+                                 : encode_map_bf16(&mB, B, Kd, N, Kd * 2, 64, b_tile)));
   if (!ok) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for A or B");
-  GemmShape g = make_shape(M, N, Kd, bn, (int)cdiv(N, bn), &hdr->status);
+  GemmShape g = make_shape(M, N, Kd, bn, (int)cdiv(N, bn), &hdr->status, pair ? 256 : 128);
   g.a_box3d = a3d ? 1 : 0;
   g.b_box3d = b3d ? 1 : 0;
   F32Params p;
   p.out = D; p.ldo = N; p.M = (int)M; p.N = (int)N; p.accumulate = (accumulate & 1) ? 1 : 0;
   p.vec_ok = (N % 4 == 0 && aligned(D, 16)) ? 1 : 0;
-  if ((e = launch_gemm_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p,
-                           g.num_units < di.sms ? g.num_units : di.sms, st)) != cudaSuccess)
-    return cuda_fail(e, "test GEMM");
+  e = pair ? launch_gemm2_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p, di.sms, st)
+           : launch_gemm_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p,
+                             g.num_units < di.sms ? g.num_units : di.sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "test GEMM");
   return FKL_OK;
 }
 

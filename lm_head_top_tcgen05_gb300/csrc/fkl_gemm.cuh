@@ -106,8 +106,9 @@ struct EpiFwd {
 
   __device__ explicit EpiFwd(const Params& prm) : p(prm) {}
 
-  __device__ __forceinline__ void begin_unit(int m_blk, int n_begin, int /*split*/, int row) {
-    t = m_blk * kBM + row;
+  // row0: first row of this CTA's 128 accumulator lanes.
+  __device__ __forceinline__ void begin_unit(int row0, int n_begin, int /*split*/, int row) {
+    t = row0 + row;
     row_ok = t < p.T;
     m2 = -INFINITY;
     l = 0.f;
@@ -185,8 +186,8 @@ struct EpiDs {
 
   __device__ explicit EpiDs(const Params& prm) : p(prm) {}
 
-  __device__ __forceinline__ void begin_unit(int m_blk, int n_begin, int /*split*/, int row) {
-    t = m_blk * kBM + row;
+  __device__ __forceinline__ void begin_unit(int row0, int n_begin, int /*split*/, int row) {
+    t = row0 + row;
     row_ok = t < p.T;
     if (row_ok) {
       lse2 = p.lse[t] * 1.4426950408889634f;
@@ -263,8 +264,8 @@ struct EpiF32 {
 
   __device__ explicit EpiF32(const Params& prm) : p(prm) {}
 
-  __device__ __forceinline__ void begin_unit(int m_blk, int, int, int row) {
-    const int r = m_blk * kBM + row;
+  __device__ __forceinline__ void begin_unit(int row0, int, int, int row) {
+    const int r = row0 + row;
     row_ok = r < p.M;
     rowp = p.out + static_cast<size_t>(row_ok ? r : 0) * p.ldo;
   }
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
       int m_blk, nb, ne, split;
       unit_range(g, u, m_blk, nb, ne, split);
-      epi.begin_unit(m_blk, nb, split, row);
+      epi.begin_unit(m_blk * kBM, nb, split, row);
       for (int n = nb; n < ne; ++n) {
         const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, ctl);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }

@@ -1,0 +1,268 @@
+// Two-SM variant of the persistent tcgen05 GEMM (cta_group::2): a cluster of two CTAs on
+// neighbouring SMs computes 256 x BN tiles.  Each CTA loads its own 128 rows of A and its
+// own half (BN/2 rows) of B into its shared memory; the even CTA issues 256 x BN x 16
+// tcgen05.mma instructions that read both CTAs' shared memory and write each CTA's 128
+// accumulator rows into that CTA's TMEM.  Per SM this halves the B-operand traffic of the
+// one-SM kernel (fkl_gemm.cuh): 32 KB per 64-deep k-block instead of 48 KB for BN = 256.
+//
+// Roles per CTA (192 threads), as in the one-SM kernel, with these hand-offs:
+//   warp 0      TMA producer (both CTAs): own stage slot -> own `full` barrier;
+//   warp 1      even CTA: MMA issuer; waits for its own `full` and the odd CTA's forwarded
+//               `pfull`, commits slot release to `empty` and tile completion to `tfull`
+//               of both CTAs (multicast commit);
+//               odd CTA: forwards each completed `full` phase to the even CTA's `pfull`;
+//   warps 2..5  epilogue (both CTAs) on its own 128 TMEM lanes; hands the accumulator
+//               back by arriving on the even CTA's `tempty` (8 arrivals: 4 warps x 2 CTAs).
+// Every wait is bounded as in the one-SM kernel; teardown drains copies and MMAs, meets
+// the other CTA at a cluster barrier and frees TMEM of both CTAs together.
+#pragma once
+
+#include "fkl_gemm.cuh"
+
+namespace fkl {
+
+constexpr int kBM2 = 256;  // rows per CTA pair
+
+__host__ __device__ constexpr int stages2_for(int bn) { return bn == 256 ? 6 : 8; }
+__host__ __device__ constexpr size_t smem2_bytes_for(int bn) {
+  return static_cast<size_t>(stages2_for(bn)) * (kBM * kBK * 2 + (bn / 2) * kBK * 2) + 1024 + 512;
+}
+
+template <int BN, bool A_MN, bool B_MN, class Epi>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmShape g, const __grid_constant__ typename Epi::Params ep) {
+  constexpr int STAGES = stages2_for(BN);
+  constexpr int BNH = BN / 2;                   // rows of B held by each CTA
+  constexpr uint32_t A_BYTES = kBM * kBK * 2;   // 16 KB
+  constexpr uint32_t B_BYTES = BNH * kBK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t BOX_BYTES = 64 * kBK * 2;
+  constexpr uint32_t IDESC = instr_desc_bf16(kBM2, BN, A_MN, B_MN);
+  static_assert(BN == 256 || BN == 128, "two-SM tiles are 256 x 256 or 256 x 128");
+  static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators must fit in TMEM");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);  // [0] TMEM base, [1] abort
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+  const uint32_t stage0 = smem_addr(smem);
+  const uint32_t full0 = smem_addr(bars);
+  const uint32_t pfull0 = full0 + 8 * STAGES;
+  const uint32_t empty0 = pfull0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(pfull0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 2 * 4);
+    }
+    mbar_init(drain, 1);
+    misc[1] = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA arrival
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const WaitCtl ctl{reinterpret_cast<volatile uint32_t*>(&misc[1]), g.status, g.limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = cluster; ok && u < g.num_units; u += nclusters) {
+        int m_blk, nb, ne, split;
+        unit_range(g, u, m_blk, nb, ne, split);
+        const int a_row = m_blk * kBM2 + static_cast<int>(rank) * kBM;
+        for (int n = nb; ok && n < ne; ++n) {
+          const int b_row = n * BN + static_cast<int>(rank) * BNH;
+          for (int kb = 0; kb < g.k_blocks; ++kb) {
+            // the slot is released by the even CTA's tensor core (multicast commit)
+            if (!mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, ctl)) { ok = false; break; }
+            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t sa = stage0 + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+            const int k0 = kb * kBK;
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            if (!A_MN) {
+              tma_load_2d(sa, &tmA, fb, k0, a_row);
+            } else if (g.a_box3d) {
+              tma_load_3d(sa, &tmA, fb, 0, k0, a_row / 64);
+            } else {
+              tma_load_2d(sa, &tmA, fb, a_row, k0);
+              tma_load_2d(sa + BOX_BYTES, &tmA, fb, a_row + 64, k0);
+            }
+            if (!B_MN) {
+              tma_load_2d(sb, &tmB, fb, k0, b_row);
+            } else if (g.b_box3d) {
+              tma_load_3d(sb, &tmB, fb, 0, k0, b_row / 64);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BNH / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmB, fb, b_row + j * 64, k0);
+            }
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) mbar_wait_drain(full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && even) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = cluster; ok && u < g.num_units; u += nclusters) {
+        int m_blk, nb, ne, split;
+        unit_range(g, u, m_blk, nb, ne, split);
+        for (int n = nb; ok && n < ne; ++n) {
+          if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kb = 0; kb < g.k_blocks; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, ctl) ||
+                !mbar_wait_cluster(pfull0 + 8 * stage, phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = stage0 + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, BOX_BYTES, 1024)
+                                       : smem_desc_sw128(sa + k * 32, 16, 1024);
+              const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, BOX_BYTES, 1024)
+                                       : smem_desc_sw128(sb + k * 32, 16, 1024);
+              tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          tc_commit_pair_mc(tfull0 + 8 * acc, 0x3);  // both halves of the tile are complete
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      tc_commit_pair(drain);
+      mbar_wait_drain(drain, 0u, g.limit_ns);
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- forwarder (odd CTA)
+      const uint32_t remote_pfull0 = map_to_rank(pfull0, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = cluster; ok && u < g.num_units; u += nclusters) {
+        int m_blk, nb, ne, split;
+        unit_range(g, u, m_blk, nb, ne, split);
+        for (int n = nb; ok && n < ne; ++n) {
+          for (int kb = 0; kb < g.k_blocks; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, ctl)) { ok = false; break; }
+            mbar_arrive_cluster(remote_pfull0 + 8 * stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t remote_tempty0 = map_to_rank(tempty0, 0);
+    Epi epi(ep);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = cluster; ok && u < g.num_units; u += nclusters) {
+      int m_blk, nb, ne, split;
+      unit_range(g, u, m_blk, nb, ne, split);
+      epi.begin_unit(m_blk * kBM2 + static_cast<int>(rank) * kBM, nb, split, row);
+      for (int n = nb; n < ne; ++n) {
+        const bool got = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, ctl);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after();
+        epi.template tile<BN>(tmem_base + lane_base + static_cast<uint32_t>(acc * BN), n, row);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(remote_tempty0 + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (ok) epi.end_unit(split, row);
+    }
+  }
+
+  __syncthreads();
+  tc_fence_before();
+  cluster_sync();  // no arrival or commit toward either CTA is still in flight
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// Clusters of this instantiation that fit on the device at once (cached per device).
+template <class Kern>
+int max_pair_clusters(Kern kern, size_t smem, int sms) {
+  static int cached[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  if (n > sms / 2) n = sms / 2;
+  cached[dev] = n;
+  return n;
+}
+
+template <int BN, bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm2_t(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
+                           const typename Epi::Params& ep, int sms, cudaStream_t st) {
+  constexpr size_t SMEM = smem2_bytes_for(BN);
+  auto kern = gemm2_kernel<BN, A_MN, B_MN, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM));
+  if (e != cudaSuccess) return e;
+  const int clusters = max_pair_clusters(kern, SMEM, sms);
+  const int n = g.num_units < clusters ? g.num_units : clusters;
+  kern<<<2 * n, kThreads, SMEM, st>>>(a, b, g, ep);
+  return cudaGetLastError();
+}
+
+}  // namespace fkl

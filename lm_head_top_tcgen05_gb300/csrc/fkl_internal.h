@@ -73,7 +73,9 @@ struct GemmShape {
   uint64_t limit_ns;
 };
 
-GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status);
+// rows_per_unit: 128 for the one-SM kernel, 256 for the two-SM (CTA pair) kernel.
+GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status,
+                     int rows_per_unit = 128);
 
 // Forward: online base-2 logsumexp and top-K gather per (row, vocabulary split).
 struct FwdParams {
@@ -116,6 +118,14 @@ cudaError_t launch_gemm_fwd(const CUtensorMap& a, const CUtensorMap& b, const Ge
                             const FwdParams& ep, int grid, cudaStream_t st);
 cudaError_t launch_gemm_ds(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
                            const DsParams& ep, int grid, cudaStream_t st);
+// Two-SM (CTA pair) versions: 256-row tiles; B maps load BN/2 rows (or columns) per CTA;
+// the grid is sized from the clusters that fit on the device (sms = SM count).
+cudaError_t launch_gemm2_fwd(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
+                             const FwdParams& ep, int sms, cudaStream_t st);
+cudaError_t launch_gemm2_ds(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
+                            const DsParams& ep, int sms, cudaStream_t st);
+cudaError_t launch_gemm2_f32(int bn, bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
+                             const GemmShape& g, const F32Params& ep, int sms, cudaStream_t st);
 // F32-output GEMM for bn in {256, 192, 128} and either major-ness of A and B.
 cudaError_t launch_gemm_f32(int bn, bool a_mn, bool b_mn, const CUtensorMap& a,
                             const CUtensorMap& b, const GemmShape& g, const F32Params& ep,

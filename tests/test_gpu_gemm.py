@@ -22,7 +22,7 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0, force2d=False):
+def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0, force2d=False, pair=False):
     g = torch.Generator().manual_seed(seed)
     A = torch.randn(M, Kd, generator=g).to(torch.bfloat16)
     B = torch.randn(N, Kd, generator=g).to(torch.bfloat16)
@@ -31,7 +31,7 @@ def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0, force2d=Fals
     Bd = (B.t().contiguous() if b_mn else B).cuda()
     D = D0.clone().cuda()
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    flags = int(accumulate) | (2 if force2d else 0)
+    flags = int(accumulate) | (2 if force2d else 0) | (4 if pair else 0)
     st = L.fkl_test_gemm(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, Kd, int(a_mn), int(b_mn), bn,
                          flags, ws.data_ptr(), 256, _stream())
     assert st == 0, L.fkl_last_error()
@@ -81,3 +81,31 @@ def test_timeout_probe_reports_status(L):
     assert L.fkl_read_status(ws.data_ptr(), _stream()) == 8  # FKL_ERR_TIMEOUT
     # the context is still usable afterwards
     assert run_gemm(L, 128, 256, 64, False, False, 256) < 1e-5
+
+
+# ---- the two-SM (CTA pair, cta_group::2) kernel that the loss uses: 256-row tiles, each CTA
+# ---- of a pair holding 128 rows of A and half of the B tile
+
+def test_pair_single_tile(L):
+    assert run_gemm(L, 256, 256, 64, False, False, 256, pair=True) < 1e-5
+
+
+@pytest.mark.parametrize("bn", [256, 128])
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
+def test_pair_ragged_all_majors(L, a_mn, b_mn, bn):
+    # M = 304: the second 256-row tile has 48 rows, so the odd CTA's half is all padding
+    assert run_gemm(L, 304, 520, 200, a_mn, b_mn, bn, pair=True) < 1e-5
+
+
+@pytest.mark.parametrize("force2d", [False, True])
+def test_pair_mn_major_box_paths(L, force2d):
+    assert run_gemm(L, 320, 1344, 200, True, True, 256, force2d=force2d, pair=True) < 1e-5
+
+
+@pytest.mark.parametrize("a_mn,b_mn,bn", [(False, False, 256), (True, True, 256), (False, True, 128)])
+def test_pair_many_waves(L, a_mn, b_mn, bn):
+    assert run_gemm(L, 2048, 3072, 1024, a_mn, b_mn, bn, seed=3, pair=True) < 2e-5
+
+
+def test_pair_accumulate_long_k(L):
+    assert run_gemm(L, 512, 384, 8192, True, True, 128, accumulate=True, seed=9, pair=True) < 5e-5
