@@ -6,11 +6,11 @@
 // one-SM kernel (fkl_gemm.cuh): 32 KB per 64-deep k-block instead of 48 KB for BN = 256.
 //
 // Roles per CTA (192 threads), as in the one-SM kernel, with these hand-offs:
-//   warp 0      TMA producer (both CTAs): own stage slot -> own `full` barrier;
-//   warp 1      even CTA: MMA issuer; waits for its own `full` and the odd CTA's forwarded
-//               `pfull`, commits slot release to `empty` and tile completion to `tfull`
-//               of both CTAs (multicast commit);
-//               odd CTA: forwards each completed `full` phase to the even CTA's `pfull`;
+//   warp 0      TMA producer (both CTAs): loads into its own stage slot; the completion of
+//               both CTAs' loads is counted on the even CTA's `full` barrier (the even
+//               producer posts the expected bytes of the pair, 2 x STAGE_BYTES);
+//   warp 1      even CTA: MMA issuer; commits slot release to `empty` and tile completion
+//               to `tfull` of both CTAs (multicast commit); idle in the odd CTA;
 //   warps 2..5  epilogue (both CTAs) on its own 128 TMEM lanes; hands the accumulator
 //               back by arriving on the even CTA's `tempty` (8 arrivals: 4 warps x 2 CTAs).
 // Every wait is bounded as in the one-SM kernel; teardown drains copies and MMAs, meets
@@ -46,7 +46,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);  // [0] TMEM base, [1] abort
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);  // [0] TMEM base, [1] abort
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -56,8 +56,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int nclusters = static_cast<int>(gridDim.x >> 1);
   const uint32_t stage0 = smem_addr(smem);
   const uint32_t full0 = smem_addr(bars);
-  const uint32_t pfull0 = full0 + 8 * STAGES;
-  const uint32_t empty0 = pfull0 + 8 * STAGES;
+  const uint32_t empty0 = full0 + 8 * STAGES;
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
@@ -65,7 +64,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(pfull0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -94,6 +92,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
+      const uint32_t full0_even = map_to_rank(full0, 0);  // the pair's `full` barriers
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
       bool ok = true;
@@ -106,26 +105,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < g.k_blocks; ++kb) {
             // the slot is released by the even CTA's tensor core (multicast commit)
             if (!mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, ctl)) { ok = false; break; }
-            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t fb = full0_even + 8 * stage;
             const uint32_t sa = stage0 + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
             const int k0 = kb * kBK;
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            if (even) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
             if (!A_MN) {
-              tma_load_2d(sa, &tmA, fb, k0, a_row);
+              tma_load_2d_pair(sa, &tmA, fb, k0, a_row);
             } else if (g.a_box3d) {
-              tma_load_3d(sa, &tmA, fb, 0, k0, a_row / 64);
+              tma_load_3d_pair(sa, &tmA, fb, 0, k0, a_row / 64);
             } else {
-              tma_load_2d(sa, &tmA, fb, a_row, k0);
-              tma_load_2d(sa + BOX_BYTES, &tmA, fb, a_row + 64, k0);
+              tma_load_2d_pair(sa, &tmA, fb, a_row, k0);
+              tma_load_2d_pair(sa + BOX_BYTES, &tmA, fb, a_row + 64, k0);
             }
             if (!B_MN) {
-              tma_load_2d(sb, &tmB, fb, k0, b_row);
+              tma_load_2d_pair(sb, &tmB, fb, k0, b_row);
             } else if (g.b_box3d) {
-              tma_load_3d(sb, &tmB, fb, 0, k0, b_row / 64);
+              tma_load_3d_pair(sb, &tmB, fb, 0, k0, b_row / 64);
             } else {
 #pragma unroll
-              for (int j = 0; j < BNH / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmB, fb, b_row + j * 64, k0);
+              for (int j = 0; j < BNH / 64; ++j) tma_load_2d_pair(sb + j * BOX_BYTES, &tmB, fb, b_row + j * 64, k0);
             }
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -133,8 +132,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1u) mbar_wait_drain(full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
+      // The even CTA drains the pair's copies (its `full` phases count both CTAs' bytes).
+      // The odd CTA's copies are covered by those phases; on the abort path its last copy
+      // was issued before a wait that ran for the full time limit.
+      if (even)
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1u) mbar_wait_drain(full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
     }
   } else if (warp == 1) {
     if (lane == 0 && even) {
@@ -150,8 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int kb = 0; kb < g.k_blocks; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, ctl) ||
-                !mbar_wait_cluster(pfull0 + 8 * stage, phase, ctl)) { ok = false; break; }
+            if (!mbar_wait_cluster(full0 + 8 * stage, phase, ctl)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = stage0 + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
@@ -174,23 +176,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_commit_pair(drain);
       mbar_wait_drain(drain, 0u, g.limit_ns);
-    } else if (lane == 0) {
-      // ---------------------------------------------------------- forwarder (odd CTA)
-      const uint32_t remote_pfull0 = map_to_rank(pfull0, 0);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int u = cluster; ok && u < g.num_units; u += nclusters) {
-        int m_blk, nb, ne, split;
-        unit_range(g, u, m_blk, nb, ne, split);
-        for (int n = nb; ok && n < ne; ++n) {
-          for (int kb = 0; kb < g.k_blocks; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, ctl)) { ok = false; break; }
-            mbar_arrive_cluster(remote_pfull0 + 8 * stage);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          }
-        }
-      }
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
