@@ -164,8 +164,35 @@ def max_over_ranks(value: float, device=None) -> float:
 
 
 KIND_NAMES = {0: "forward projection + logsumexp/top-K", 1: "dS recompute", 2: "dW", 3: "dH"}
-KERNEL_NAMES = {0: "gemm_kernel<256,0,0,EpiFwd>", 1: "gemm_kernel<256,0,0,EpiDs>",
-                2: "gemm_kernel<BN,1,1,EpiF32> (dW)", 3: "gemm_kernel<BN,0,1,EpiF32> (dH)"}
+KERNEL_NAMES = {0: "gemm2_kernel<256,0,0,EpiFwd> (two-SM)", 1: "gemm2_kernel<256,0,0,EpiDs> (two-SM)",
+                2: "gemm2_kernel<256,1,1,EpiF32> (two-SM, dW)", 3: "gemm2_kernel<256,0,1,EpiF32> (two-SM, dH)"}
+
+# DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
+# of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
+# bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
+TRAFFIC_SOURCES_SHA = "a00aa85a678b7959"
+TRAFFIC_BYTES = {1: 2.904e9, 2: 2.545e9, 3: 2.690e9}
+TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
+
+
+def csrc_sha() -> str:
+    import glob
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "lm_head_top_tcgen05_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(kind, flops_per_launch, d):
+    """Measured bytes per launch, scaled to the mean launch by the work it does (traffic of
+    these products grows in proportion to the slab width), or None when no capture applies."""
+    if kind not in TRAFFIC_BYTES or d != 2880 or csrc_sha() != TRAFFIC_SOURCES_SHA:
+        return None
+    return TRAFFIC_BYTES[kind] * flops_per_launch / TRAFFIC_FLOPS
 
 
 def trace_summary(L, cap):
@@ -339,7 +366,9 @@ def main():
                      "frac_of_burst": kernels[dom]["tflops"] / burst,
                      "peak_source": f"{peak_kind} bf16_tflops_sustained (timed inside a seconds-long loop)",
                      "flops_per_launch": kernels[dom]["flops_per_launch"],
-                     "ms_per_launch": kernels[dom]["ms_per_launch"], "traffic": None},
+                     "ms_per_launch": kernels[dom]["ms_per_launch"],
+                     "traffic": traffic_per_launch(dom, kernels[dom]["flops_per_launch"], d)
+                     if T == 32768 else None},
         "kernels": {KIND_NAMES[k]: {kk: round(vv, 4) if isinstance(vv, float) else vv for kk, vv in v.items()}
                     for k, v in kernels.items()},
         "clocks": clk,
