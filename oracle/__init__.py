@@ -11,4 +11,5 @@ from .dense_kl import (  # noqa: F401
     forward,
     teacher_probs,
     to_f64,
+    token_weights,
 )

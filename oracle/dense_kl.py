@@ -37,6 +37,16 @@ The post names this the "closed-form gradient behind the fused chunked loss" wit
 printing it; the expression above is the derivative of L and is checked against finite
 differences and torch.autograd in the tests.
 
+Normalisation (the pages mention sequence packing without fixing the loss's normaliser).
+``norm="tokens"`` is the formula above.  ``norm="sequences"`` averages per packed sequence
+first: with seq_ids[t] the sequence of token t, N_s the valid tokens of sequence s and S the
+number of sequences with N_s > 0,
+
+    L = tau^2 / S * sum_{s : N_s > 0} (1 / N_s) * sum_{t valid, seq t = s} KL_t,
+
+i.e. every token carries the weight w_t = 1 / (S N_{s(t)}) instead of 1 / N, and the gradient
+is the same expression with tau / N replaced by tau * w_t.
+
 Everything is float64.  H and W arrive as bfloat16 on the GPU path; ``to_f64`` widens
 them exactly.  Rows are processed in blocks of ``chunk`` rows (a dense [chunk, V] block
 of logits at a time); the result does not depend on ``chunk`` beyond float64 rounding.
@@ -89,6 +99,32 @@ def teacher_probs(topk_logits, tau: float):
     return p, logp
 
 
+def token_weights(mask, T: int, norm: str = "tokens", seq_ids=None) -> np.ndarray:
+    """w_t, the weight of token t's KL in the loss (before tau^2): 1/N for valid tokens under
+    the token mean; 1/(S N_s) under the sequence mean; 0 for masked tokens."""
+    msk = np.ones(T, dtype=bool) if mask is None else _np(mask).astype(bool)
+    w = np.zeros(T)
+    if norm == "tokens":
+        n = int(msk.sum())
+        if n:
+            w[msk] = 1.0 / n
+        return w
+    if norm != "sequences":
+        raise ValueError(norm)
+    if seq_ids is None:
+        raise ValueError("seq_ids are needed for the sequence mean")
+    sid = _np(seq_ids, np.int64)
+    if sid.shape != (T,) or (T and sid.min() < 0):
+        raise ValueError("seq_ids must be [T] non-negative")
+    counts = {}
+    for t in np.flatnonzero(msk):
+        counts[int(sid[t])] = counts.get(int(sid[t]), 0) + 1
+    S = len(counts)
+    for t in np.flatnonzero(msk):
+        w[t] = 1.0 / (S * counts[int(sid[t])])
+    return w
+
+
 def _check(H, W, idx, V):
     if H.ndim != 2 or W.ndim != 2 or H.shape[1] != W.shape[1]:
         raise ValueError("H must be [T, d] and W [V, d]")
@@ -108,7 +144,7 @@ def _row_terms(s_blk: np.ndarray, idx_blk: np.ndarray, p_blk: np.ndarray, logp_b
 
 
 def forward(H, W, topk_idx, topk_logits, mask, tau: float, chunk: int = 64,
-            rows: Optional[Sequence[int]] = None):
+            rows: Optional[Sequence[int]] = None, norm: str = "tokens", seq_ids=None):
     """Loss, per-token lse and per-token KL.
 
     H [T, d] and W [V, d] are float64 arrays (see ``to_f64``); topk_idx [T, K] ints;
@@ -117,6 +153,7 @@ def forward(H, W, topk_idx, topk_logits, mask, tau: float, chunk: int = 64,
     With ``rows`` given, lse and KL are computed only for those rows (returned in that
     order) and the loss is computed only if every valid row is among them; otherwise
     ``loss`` is None.  This keeps exact checks affordable at full vocabulary size.
+    ``norm`` / ``seq_ids`` select the normaliser (module docstring).
     """
     H = np.asarray(H, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
@@ -139,14 +176,18 @@ def forward(H, W, topk_idx, topk_logits, mask, tau: float, chunk: int = 64,
     if all(t in covered for t in np.flatnonzero(msk).tolist()):
         if n_valid == 0:
             loss = 0.0
-        else:
+        elif norm == "tokens":
             valid_sel = msk[sel]
             loss = float(tau) ** 2 / n_valid * float(np.sum(kl[valid_sel]))
+        else:
+            wts = token_weights(mask, T, norm, seq_ids)[sel]
+            loss = float(tau) ** 2 * float(np.sum(wts * kl))
     return {"loss": loss, "lse": lse, "kl": kl, "n_valid": n_valid, "rows": sel}
 
 
 def _ds_block(s_blk, idx_blk, p_blk, valid_blk, tau, scale):
-    """dS for one block of rows: scale * (q - ptilde), zero on masked rows."""
+    """dS for one block of rows: scale * (q - ptilde), zero on masked rows.  ``scale`` is a
+    number or one value per row."""
     a = s_blk / tau
     m = np.max(a, axis=1, keepdims=True)
     e = np.exp(a - m)
@@ -154,12 +195,14 @@ def _ds_block(s_blk, idx_blk, p_blk, valid_blk, tau, scale):
     ptilde = np.zeros_like(q)
     rr = np.repeat(np.arange(q.shape[0]), idx_blk.shape[1])
     np.add.at(ptilde, (rr, idx_blk.reshape(-1)), p_blk.reshape(-1))
-    ds = scale * (q - ptilde)
+    scale = np.asarray(scale, dtype=np.float64)
+    ds = (scale[:, None] if scale.ndim else scale) * (q - ptilde)
     ds[~valid_blk] = 0.0
     return ds
 
 
-def backward(H, W, topk_idx, topk_logits, mask, tau: float, grad: float = 1.0, chunk: int = 64):
+def backward(H, W, topk_idx, topk_logits, mask, tau: float, grad: float = 1.0, chunk: int = 64,
+             norm: str = "tokens", seq_ids=None):
     """dH [T, d] and dW [V, d] in float64, the exact gradient of ``forward``'s loss."""
     H = np.asarray(H, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
@@ -172,12 +215,12 @@ def backward(H, W, topk_idx, topk_logits, mask, tau: float, grad: float = 1.0, c
     dW = np.zeros_like(W)
     if n_valid == 0:
         return dH, dW
-    scale = float(grad) * float(tau) / n_valid
+    row_scale = float(grad) * float(tau) * token_weights(mask, T, norm, seq_ids)
     p, _ = teacher_probs(topk_logits, tau)
     for b0 in range(0, T, chunk):
         r = slice(b0, min(T, b0 + chunk))
         s_blk = H[r] @ W.T
-        ds = _ds_block(s_blk, idx[r], p[r], msk[r], tau, scale)
+        ds = _ds_block(s_blk, idx[r], p[r], msk[r], tau, row_scale[r])
         dH[r] = ds @ W
         dW += ds.T @ H[r]
     return dH, dW

@@ -23,6 +23,9 @@ PIN_CALLS = [
     pins.test_chunk_invariance,
     pins.test_masked_rows_change_nothing,
     pins.test_no_valid_token,
+    pins.test_sequence_mean_of_one_sequence_is_token_mean,
+    pins.test_sequence_mean_weights_unequal_sequences,
+    pins.test_sequence_mean_matches_autograd,
 ]
 
 
@@ -77,8 +80,18 @@ def ds_missing_tau(s, idx, p, valid, tau, scale):
     return orig_ds_block(s, idx, p, valid, tau, scale / tau)
 
 
-def ds_ignores_mask(s, idx, p, valid, tau, scale):
-    return orig_ds_block(s, idx, p, np.ones_like(valid), tau, scale)
+orig_token_weights = dk.token_weights
+
+
+def weights_ignore_mask(mask, T, norm="tokens", seq_ids=None):
+    return orig_token_weights(None, T, norm, seq_ids)
+
+
+def weights_sequence_by_total_count(mask, T, norm="tokens", seq_ids=None):
+    w = orig_token_weights(mask, T, norm, seq_ids)
+    if norm == "sequences":  # divides by the total valid count instead of each sequence's
+        w = orig_token_weights(mask, T, "tokens")
+    return w
 
 
 def probs_no_teacher_tau(z, tau):
@@ -92,7 +105,8 @@ def lse_log2(s, idx, p, logp, tau):
 
 MUTATIONS = {
     "_row_terms": [row_terms_no_student_tau, row_terms_drop_entropy, row_terms_wrong_index, lse_log2],
-    "_ds_block": [ds_sign_flip, ds_scatter_assign, ds_missing_tau, ds_ignores_mask],
+    "_ds_block": [ds_sign_flip, ds_scatter_assign, ds_missing_tau],
+    "token_weights": [weights_ignore_mask, weights_sequence_by_total_count],
     "teacher_probs": [probs_no_teacher_tau],
 }
 
@@ -107,8 +121,8 @@ def test_planted_mistake_is_caught(monkeypatch, target, mutant):
 def test_loss_normaliser_mistake_is_caught(monkeypatch):
     orig_forward = dk.forward
 
-    def forward_over_all_tokens(H, W, idx, z, mask, tau, chunk=64, rows=None):
-        out = orig_forward(H, W, idx, z, mask, tau, chunk, rows)
+    def forward_over_all_tokens(H, W, idx, z, mask, tau, chunk=64, rows=None, **kw):
+        out = orig_forward(H, W, idx, z, mask, tau, chunk, rows, **kw)
         if out["loss"] is not None and out["n_valid"]:
             out["loss"] *= out["n_valid"] / len(out["lse"])  # divides by T, not N_valid
         return out

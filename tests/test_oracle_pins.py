@@ -44,10 +44,11 @@ def rand_case(T=6, d=8, V=32, K=5, seed=0, tau=1.0, mask=None, distinct=True, w_
 def test_closed_form_cases(case):
     H, W = np.array(case["H"], float), np.array(case["W"], float)
     ids, z, mask, tau = np.array(case["ids"]), np.array(case["z"], float), np.array(case["mask"]), case["tau"]
-    f = oracle.forward(H, W, ids, z, mask, tau)
+    norm, seq = case.get("norm", "tokens"), case.get("seq_ids")
+    f = oracle.forward(H, W, ids, z, mask, tau, norm=norm, seq_ids=seq)
     assert f["loss"] == pytest.approx(case["loss"], rel=1e-13, abs=1e-14)
     np.testing.assert_allclose(f["lse"], case["lse"], rtol=1e-13)
-    dH, dW = oracle.backward(H, W, ids, z, mask, tau)
+    dH, dW = oracle.backward(H, W, ids, z, mask, tau, norm=norm, seq_ids=seq)
     np.testing.assert_allclose(dH, case["dH"], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(dW, case["dW"], rtol=1e-12, atol=1e-14)
 
@@ -253,3 +254,71 @@ def test_to_f64_is_exact_for_bf16():
     assert y.dtype == np.float64
     assert np.array_equal(y, x.float().numpy().astype(np.float64))
     assert math.isclose(float(oracle.to_f64(torch.tensor([1.5], dtype=torch.bfloat16))[0]), 1.5)
+
+
+# ---------------------------------------------------------------- sequence-mean normaliser
+
+def test_sequence_mean_of_one_sequence_is_token_mean():
+    H, W, idx, z, m, tau = rand_case(T=9, d=6, V=30, K=5, seed=21, tau=1.3, mask=[1, 1, 0, 1, 1, 1, 1, 0, 1])
+    seq = np.zeros(9, np.int64)
+    a = oracle.forward(H, W, idx, z, m, tau)["loss"]
+    b = oracle.forward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)["loss"]
+    assert a == pytest.approx(b, rel=1e-14)
+    ga = oracle.backward(H, W, idx, z, m, tau)
+    gb = oracle.backward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)
+    np.testing.assert_allclose(ga[1], gb[1], rtol=1e-13, atol=1e-16)
+
+
+def test_sequence_mean_with_equal_counts_is_token_mean():
+    H, W, idx, z, _, tau = rand_case(T=12, d=6, V=30, K=5, seed=22)
+    seq = np.repeat(np.arange(3), 4)
+    m = np.array([1, 1, 1, 0] * 3, np.uint8)  # three valid tokens in every sequence
+    a = oracle.forward(H, W, idx, z, m, tau)["loss"]
+    b = oracle.forward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)["loss"]
+    assert a == pytest.approx(b, rel=1e-14)
+
+
+def test_sequence_mean_weights_unequal_sequences():
+    seq = np.array([0, 0, 0, 1, 2, 2, 3, 3])
+    m = np.array([1, 1, 0, 1, 1, 1, 0, 0], np.uint8)  # sequence 3 has no valid token
+    w = oracle.token_weights(m, 8, "sequences", seq)
+    np.testing.assert_allclose(w, [1 / 6, 1 / 6, 0, 1 / 3, 1 / 6, 1 / 6, 0, 0])
+    assert w.sum() == pytest.approx(1.0)
+
+
+def test_sequence_mean_gradient_finite_differences():
+    seq = np.array([0, 0, 0, 1, 1, 2, 2, 2])
+    H, W, idx, z, m, tau = rand_case(T=8, d=10, V=40, K=6, seed=23, tau=1.4, mask=[1, 1, 0, 1, 1, 1, 1, 0])
+    dH, dW = oracle.backward(H, W, idx, z, m, tau, grad=0.8, norm="sequences", seq_ids=seq)
+    h = 1e-6
+    for X, G in ((H, dH), (W, dW)):
+        num = np.zeros_like(X)
+        for i in np.ndindex(X.shape):
+            old = X[i]
+            X[i] = old + h
+            lp = oracle.forward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)["loss"]
+            X[i] = old - h
+            lm = oracle.forward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)["loss"]
+            X[i] = old
+            num[i] = 0.8 * (lp - lm) / (2 * h)
+        assert np.linalg.norm(num - G) / np.linalg.norm(G) < 1e-6
+
+
+def test_sequence_mean_matches_autograd():
+    seq = np.array([0, 0, 1, 1, 1, 1, 2, 3, 3, 3])
+    H, W, idx, z, m, tau = rand_case(T=10, d=12, V=40, K=6, seed=24, tau=1.1,
+                                     mask=[1, 1, 0, 1, 1, 1, 1, 1, 0, 1])
+    Ht, Wt = torch.tensor(H, requires_grad=True), torch.tensor(W, requires_grad=True)
+    logq = torch.log_softmax(Ht @ Wt.T / tau, dim=1)
+    P = torch.zeros(10, 40, dtype=torch.float64).scatter_(1, torch.tensor(idx),
+                                                          torch.softmax(torch.tensor(z / tau), 1))
+    kl = torch.nn.functional.kl_div(logq, P, reduction="none").sum(1)
+    valid = torch.tensor(m.astype(bool))
+    per_seq = [kl[(torch.tensor(seq) == s) & valid].mean() for s in range(4)
+               if ((torch.tensor(seq) == s) & valid).any()]
+    L = tau ** 2 * torch.stack(per_seq).mean()
+    L.backward()
+    assert oracle.forward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)["loss"] == pytest.approx(L.item(), rel=1e-13)
+    dH, dW = oracle.backward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)
+    np.testing.assert_allclose(dH, Ht.grad.numpy(), rtol=1e-11, atol=1e-15)
+    np.testing.assert_allclose(dW, Wt.grad.numpy(), rtol=1e-11, atol=1e-15)
