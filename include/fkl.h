@@ -39,10 +39,10 @@
  *   - Errors found on the host (bad argument, alignment, workspace too small, a CUDA
  *     launch failure) are returned at once and nothing is enqueued after the failing
  *     step; fkl_last_error() gives a message.  Errors found on the device (a teacher id
- *     outside [0, V), a teacher row with no finite logit, a pipeline wait that exceeded
- *     its time limit) are recorded in a status word inside the workspace, make the loss
- *     NaN (forward) or fill dH and dW with NaN (backward), and are reported by
- *     fkl_read_status().  No device code traps.
+ *     outside [0, V), a teacher row with no finite logit, a sequence id out of range, a
+ *     pipeline wait that exceeded its time limit) are recorded in a status word inside the
+ *     workspace, make the loss NaN (forward) or fill dH and dW with NaN (backward), and are
+ *     reported by fkl_read_status().  No device code traps.
  *   - Results are deterministic: the same inputs give bitwise the same outputs.
  */
 #ifndef FKL_H_
@@ -64,8 +64,37 @@ typedef enum fkl_status {
   FKL_ERR_CUDA = 5,         /* a CUDA runtime or driver call failed */
   FKL_ERR_BAD_TOPK_ID = 6,  /* device: a teacher id is outside [0, V) */
   FKL_ERR_BAD_TOPK_ROW = 7, /* device: a teacher row has no finite logit */
-  FKL_ERR_TIMEOUT = 8       /* device: a pipeline wait exceeded its time limit */
+  FKL_ERR_TIMEOUT = 8,      /* device: a pipeline wait exceeded its time limit */
+  FKL_ERR_BAD_SEQ_ID = 9    /* device: a valid token's sequence id is outside [0, num_seqs) */
 } fkl_status;
+
+/*
+ * Options of fkl_forward_ex / fkl_backward_ex (fkl_forward / fkl_backward use the defaults:
+ * all fields zero).
+ *
+ * normalization  FKL_NORM_TOKENS (0): L = tau^2 / N * sum over valid tokens of KL_t, the
+ *                mean over the batch's valid tokens.
+ *                FKL_NORM_SEQUENCES (1): for packed batches, the mean over sequences of each
+ *                sequence's token mean, L = tau^2 / S * sum_s (1 / N_s) sum_{valid t in s} KL_t,
+ *                over the S sequences that have a valid token (N_s of them in sequence s).
+ *                The pages mention sequence packing without fixing the normaliser; both
+ *                readings are offered, the token mean is the default.
+ * seq_ids        FKL_NORM_SEQUENCES: device int32 [T], the packed sequence of each token, in
+ *                [0, num_seqs); any order.  Ignored otherwise (may be NULL).
+ * num_seqs       FKL_NORM_SEQUENCES: 1 <= num_seqs <= max(T, 1).
+ * accumulate     fkl_backward_ex: FKL_ACCUMULATE_DH and/or FKL_ACCUMULATE_DW add the gradient
+ *                into dH / dW (gradient accumulation over micro-batches) instead of
+ *                overwriting them.  Ignored by the forward.
+ */
+enum { FKL_NORM_TOKENS = 0, FKL_NORM_SEQUENCES = 1 };
+enum { FKL_ACCUMULATE_DH = 1, FKL_ACCUMULATE_DW = 2 };
+typedef struct fkl_options {
+  int32_t normalization;
+  int32_t num_seqs;
+  const int32_t* seq_ids;
+  int32_t accumulate;
+  int32_t reserved;  /* must be 0 */
+} fkl_options;
 
 /*
  * Bytes of workspace that fkl_forward and fkl_backward need for this shape (one buffer
@@ -98,6 +127,12 @@ fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk
                        int64_t V, int64_t K, float tau, int64_t chunk, float* loss, float* lse,
                        void* workspace, size_t ws_bytes, void* stream);
 
+/* fkl_forward with options (NULL = defaults). */
+fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                          const float* topk_logits, const uint8_t* mask, int64_t T, int64_t d,
+                          int64_t V, int64_t K, float tau, int64_t chunk, const fkl_options* opts,
+                          float* loss, float* lse, void* workspace, size_t ws_bytes, void* stream);
+
 /*
  * Backward pass: recomputes the projection chunk by chunk and writes dH (device float
  * [T, d]) and dW (device float [V, d]); both are overwritten, not accumulated into.
@@ -121,7 +156,7 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
  * Same results and arguments as fkl_forward, without `chunk` (the forward does not depend
  * on it) and without a workspace: the scratch lives in a 64 MiB device array inside the
  * library, which every GPU that loads the library keeps until the process exits.  Shapes
- * whose forward scratch exceeds it (about T * (8K + 392) bytes; T up to about 56K tokens at
+ * whose forward scratch exceeds it (about T * (8K + 400) bytes; T up to about 56K tokens at
  * K = 100) are rejected with FKL_ERR_WORKSPACE and a message in fkl_last_error().
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
@@ -136,6 +171,13 @@ fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, const int32
                                const float* topk_logits, const uint8_t* mask, int64_t T,
                                int64_t d, int64_t V, int64_t K, float tau, float* loss, float* lse,
                                void* stream);
+
+/* fkl_backward with options (NULL = defaults).  With the same options as the forward. */
+fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                           const float* topk_logits, const uint8_t* mask, const float* lse,
+                           const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K,
+                           float tau, int64_t chunk, const fkl_options* opts, float* dH, float* dW,
+                           void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Waits for `stream`, then returns the device-side status recorded in `workspace` by the

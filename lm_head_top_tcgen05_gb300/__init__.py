@@ -19,7 +19,8 @@ from typing import Optional, Tuple
 
 import torch
 
-from ._lib import FKL_OK, STATUS, FklError, check, lib  # noqa: F401
+from ._lib import (FKL_ACCUMULATE_DH, FKL_ACCUMULATE_DW, FKL_NORM_SEQUENCES, FKL_NORM_TOKENS,  # noqa: F401
+                   FKL_OK, STATUS, FklError, FklOptions, check, lib)
 
 __all__ = ["workspace_size", "Workspace", "forward", "backward", "read_status", "fused_kl",
            "FusedKL", "FklError", "STATUS"]
@@ -93,27 +94,50 @@ def _check_inputs(H, W, topk_idx, topk_logits, mask):
     return mask
 
 
+def _options(T: int, seq_ids: Optional[torch.Tensor], num_seqs: Optional[int], accumulate: int = 0):
+    """fkl_options for the sequence-mean normaliser (seq_ids given) and accumulation flags."""
+    o = FklOptions()
+    o.accumulate = accumulate
+    if seq_ids is not None:
+        if seq_ids.dtype != torch.int32 or tuple(seq_ids.shape) != (T,) or not seq_ids.is_cuda:
+            raise ValueError("seq_ids must be a CUDA int32 tensor of shape [T]")
+        seq_ids = seq_ids.contiguous()
+        o.normalization = FKL_NORM_SEQUENCES
+        o.num_seqs = int(num_seqs) if num_seqs is not None else max(1, int(seq_ids.max().item()) + 1 if T else 1)
+        o.seq_ids = seq_ids.data_ptr()
+    return o, seq_ids
+
+
 def forward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
             mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048,
-            workspace: Optional[Workspace] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Loss (0-dim float32) and lse [T] (float32) on H's device and current stream."""
+            workspace: Optional[Workspace] = None, seq_ids: Optional[torch.Tensor] = None,
+            num_seqs: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Loss (0-dim float32) and lse [T] (float32) on H's device and current stream.
+
+    With ``seq_ids`` (int32 [T], the packed sequence of each token) the loss is the mean
+    over sequences of each sequence's token mean; otherwise the mean over valid tokens."""
     mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
     T, d = H.shape
     V, K = W.shape[0], topk_idx.shape[1]
     ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk), H.device)
     loss = torch.empty((), dtype=torch.float32, device=H.device)
     lse = torch.empty(T, dtype=torch.float32, device=H.device)
-    st = lib().fkl_forward(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask), T, d, V, K,
-                           float(tau), chunk, _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _stream(H.device))
-    check(st, "fkl_forward")
+    opts, seq_ids = _options(T, seq_ids, num_seqs)
+    st = lib().fkl_forward_ex(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask), T, d, V, K,
+                              float(tau), chunk, ctypes.byref(opts), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
+                              _stream(H.device))
+    check(st, "fkl_forward_ex")
     return loss, lse
 
 
 def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
              mask: Optional[torch.Tensor], lse: torch.Tensor, grad_loss: Optional[torch.Tensor] = None,
              tau: float = 1.0, chunk: int = 2048, workspace: Optional[Workspace] = None,
-             out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """dH [T, d] and dW [V, d] (float32), the gradient of g * loss (g = grad_loss or 1)."""
+             out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None, seq_ids: Optional[torch.Tensor] = None,
+             num_seqs: Optional[int] = None, accumulate: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """dH [T, d] and dW [V, d] (float32), the gradient of g * loss (g = grad_loss or 1).
+
+    ``accumulate=True`` adds into the tensors given in ``out`` (gradient accumulation)."""
     mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
     T, d = H.shape
     V, K = W.shape[0], topk_idx.shape[1]
@@ -123,14 +147,21 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
         grad_loss = grad_loss.detach().to(device=H.device, dtype=torch.float32).reshape(()).contiguous()
     ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk), H.device)
     if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs the gradients to add into, in `out`")
         dH = torch.empty((T, d), dtype=torch.float32, device=H.device)
         dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
     else:
         dH, dW = out
-    st = lib().fkl_backward(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask),
-                            _ptr(lse.contiguous()), _ptr(grad_loss), T, d, V, K, float(tau), chunk,
-                            _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(H.device))
-    check(st, "fkl_backward")
+        for g, shape in ((dH, (T, d)), (dW, (V, d))):
+            if g.dtype != torch.float32 or tuple(g.shape) != shape or not g.is_contiguous() or g.device != H.device:
+                raise ValueError(f"out gradients must be contiguous float32 {shape} on {H.device}")
+    flags = (FKL_ACCUMULATE_DH | FKL_ACCUMULATE_DW) if accumulate else 0
+    opts, seq_ids = _options(T, seq_ids, num_seqs, flags)
+    st = lib().fkl_backward_ex(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask),
+                               _ptr(lse.contiguous()), _ptr(grad_loss), T, d, V, K, float(tau), chunk,
+                               ctypes.byref(opts), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(H.device))
+    check(st, "fkl_backward_ex")
     return dH, dW
 
 
@@ -145,21 +176,24 @@ class FusedKL(torch.autograd.Function):
     """Autograd wrapper: forward saves lse; backward recomputes the projection chunk by chunk."""
 
     @staticmethod
-    def forward(ctx, H, W, topk_idx, topk_logits, mask, tau, chunk):
-        loss, lse = forward(H, W, topk_idx, topk_logits, mask, tau, chunk)
+    def forward(ctx, H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=None, num_seqs=None):
+        loss, lse = forward(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=seq_ids, num_seqs=num_seqs)
         ctx.save_for_backward(H, W, topk_idx, topk_logits, lse)
-        ctx.mask = mask
+        ctx.mask, ctx.seq_ids, ctx.num_seqs = mask, seq_ids, num_seqs
         ctx.tau, ctx.chunk = tau, chunk
         return loss
 
     @staticmethod
     def backward(ctx, grad):
         H, W, topk_idx, topk_logits, lse = ctx.saved_tensors
-        dH, dW = backward(H, W, topk_idx, topk_logits, ctx.mask, lse, grad, ctx.tau, ctx.chunk)
-        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None, None
+        dH, dW = backward(H, W, topk_idx, topk_logits, ctx.mask, lse, grad, ctx.tau, ctx.chunk,
+                          seq_ids=ctx.seq_ids, num_seqs=ctx.num_seqs)
+        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None, None, None, None
 
 
 def fused_kl(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
-             mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048) -> torch.Tensor:
-    """tau^2 / N * sum over valid tokens of KL(teacher top-K || student), differentiable in H, W."""
-    return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk)
+             mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048,
+             seq_ids: Optional[torch.Tensor] = None, num_seqs: Optional[int] = None) -> torch.Tensor:
+    """tau^2 * KL(teacher top-K || student) averaged over valid tokens (or, with seq_ids, over
+    packed sequences of their token means); differentiable in H and W."""
+    return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids, num_seqs)

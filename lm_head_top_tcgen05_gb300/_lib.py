@@ -20,8 +20,19 @@ STATUS = {
     6: "FKL_ERR_BAD_TOPK_ID",
     7: "FKL_ERR_BAD_TOPK_ROW",
     8: "FKL_ERR_TIMEOUT",
+    9: "FKL_ERR_BAD_SEQ_ID",
 }
 FKL_OK = 0
+
+class FklOptions(ctypes.Structure):
+    """fkl_options of include/fkl.h."""
+
+    _fields_ = [("normalization", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+                ("seq_ids", ctypes.c_void_p), ("accumulate", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+FKL_NORM_TOKENS, FKL_NORM_SEQUENCES = 0, 1
+FKL_ACCUMULATE_DH, FKL_ACCUMULATE_DW = 1, 2
 
 # Every symbol declared in include/*.h, with (restype, argtypes).
 _P = ctypes.c_void_p
@@ -38,6 +49,10 @@ _SIGNATURES = {
     "fkl_trace_start": (ctypes.c_int, [ctypes.c_int32]),
     "fkl_trace_stop": (ctypes.c_int, []),
     "fkl_trace_read": (ctypes.c_int32, [_P, _P, _P, ctypes.c_int32]),
+    "fkl_forward_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float, _I64,
+                                      ctypes.POINTER(FklOptions), _P, _P, _P, ctypes.c_size_t, _P]),
+    "fkl_backward_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                       _I64, ctypes.POINTER(FklOptions), _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_read_status": (ctypes.c_int, [_P, _P]),
     "fkl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fkl_last_error": (ctypes.c_char_p, []),

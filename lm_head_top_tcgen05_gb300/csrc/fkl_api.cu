@@ -65,6 +65,8 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   size_t off = 256;  // header
   p->off_pairs = off; off = align_up(off + static_cast<size_t>(T) * K * 8, 256);
   p->off_crow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
+  p->off_wrow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
+  p->off_scnt = off;  off = align_up(off + static_cast<size_t>(T > 0 ? T : 1) * 4, 256);
   p->off_part = off;  off = align_up(off + static_cast<size_t>(T) * 3 * kMaxSplit * 4, 256);
   const size_t nbb = static_cast<size_t>(p->nb > 0 ? p->nb : 1);
   p->off_bsum = off;  off = align_up(off + nbb * 8, 256);
@@ -208,6 +210,28 @@ static int choose_bn_d(int64_t d, bool pair) {
   return best;
 }
 
+static fkl_status check_options(const fkl_options* o, int64_t T) {
+  if (o == nullptr) return FKL_OK;
+  if (o->reserved != 0) return fail(FKL_ERR_INVALID_ARG, "fkl_options.reserved must be 0");
+  if (o->accumulate < 0 || o->accumulate > 3) return fail(FKL_ERR_INVALID_ARG, "bad fkl_options.accumulate");
+  if (o->normalization == FKL_NORM_TOKENS) return FKL_OK;
+  if (o->normalization != FKL_NORM_SEQUENCES) return fail(FKL_ERR_INVALID_ARG, "bad fkl_options.normalization");
+  if (o->num_seqs < 1 || o->num_seqs > (T > 0 ? T : 1))
+    return fail(FKL_ERR_INVALID_ARG, "fkl_options.num_seqs must be in [1, max(T, 1)]");
+  if (T > 0 && o->seq_ids == nullptr) return fail(FKL_ERR_INVALID_ARG, "fkl_options.seq_ids is NULL");
+  if (!aligned(o->seq_ids, 4)) return fail(FKL_ERR_ALIGNMENT, "fkl_options.seq_ids must be 4-byte aligned");
+  return FKL_OK;
+}
+
+// Token weights of the loss (and N, S in the header) for the options' normaliser.
+static cudaError_t run_weights(const fkl_options* o, const uint8_t* mask, int64_t T, uint8_t* ws, const Plan& pl,
+                               WsHeader* hdr, cudaStream_t st) {
+  const bool per_seq = o != nullptr && o->normalization == FKL_NORM_SEQUENCES;
+  return launch_weights(mask, per_seq ? o->seq_ids : nullptr, per_seq ? o->num_seqs : 1, per_seq ? 1 : 0, T,
+                        reinterpret_cast<int*>(ws + pl.off_scnt), hdr, reinterpret_cast<float*>(ws + pl.off_wrow),
+                        st);
+}
+
 static fkl_status check_common(const uint16_t* H, const uint16_t* W, const int32_t* idx, const float* z,
                                int64_t T, int64_t d, int64_t V, int64_t K, float tau, int64_t chunk,
                                void* ws, size_t ws_bytes, Plan* plan) {
@@ -259,6 +283,7 @@ const char* fkl_status_string(int status) {
     case FKL_ERR_BAD_TOPK_ID: return "teacher id outside [0, V)";
     case FKL_ERR_BAD_TOPK_ROW: return "teacher row without a finite logit";
     case FKL_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case FKL_ERR_BAD_SEQ_ID: return "sequence id outside [0, num_seqs)";
     default: return "unknown status";
   }
 }
@@ -267,10 +292,19 @@ fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk
                        const float* topk_logits, const uint8_t* mask, int64_t T, int64_t d,
                        int64_t V, int64_t K, float tau, int64_t chunk, float* loss, float* lse,
                        void* workspace, size_t ws_bytes, void* stream) {
+  return fkl_forward_ex(H, W, topk_idx, topk_logits, mask, T, d, V, K, tau, chunk, nullptr, loss, lse, workspace,
+                        ws_bytes, stream);
+}
+
+fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                          const float* topk_logits, const uint8_t* mask, int64_t T, int64_t d,
+                          int64_t V, int64_t K, float tau, int64_t chunk, const fkl_options* opts,
+                          float* loss, float* lse, void* workspace, size_t ws_bytes, void* stream) {
   g_last_error.clear();
   Plan pl;
   fkl_status s = check_common(H, W, topk_idx, topk_logits, T, d, V, K, tau, chunk, workspace, ws_bytes, &pl);
   if (s != FKL_OK) return s;
+  if ((s = check_options(opts, T)) != FKL_OK) return s;
   if (loss == nullptr || (T > 0 && lse == nullptr)) return fail(FKL_ERR_INVALID_ARG, "loss and lse must not be NULL");
   if (!aligned(loss, 4) || (lse && !aligned(lse, 4))) return fail(FKL_ERR_ALIGNMENT, "loss and lse must be 4-byte aligned");
   DevInfo di;
@@ -285,10 +319,12 @@ fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk
   float* part = reinterpret_cast<float*>(ws + pl.off_part);
   double* bsum = reinterpret_cast<double*>(ws + pl.off_bsum);
   int* bcnt = reinterpret_cast<int*>(ws + pl.off_bcnt);
+  const float* wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
 
   if (T > 0) {
     if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st)) != cudaSuccess)
       return cuda_fail(e, "prep kernel");
+    if ((e = run_weights(opts, mask, T, ws, pl, hdr, st)) != cudaSuccess) return cuda_fail(e, "weights kernels");
     // Two-SM tiles: each CTA of a pair loads 128 rows of H and 128 rows of the W tile.
     CUtensorMap mH, mW;
     if (!encode_map_bf16(&mH, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, W, d, V, d * 2, 64, kVocabTile / 2))
@@ -304,10 +340,10 @@ fkl_status fkl_forward(const uint16_t* H, const uint16_t* W, const int32_t* topk
     trace_launch_begin(st);
     if ((e = launch_gemm2_fwd(mH, mW, g, fp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "forward GEMM");
     trace_launch_end(st, 0, 2.0 * T * V * d);
-    if ((e = launch_combine(part, nsplit, crow, mask, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st)) != cudaSuccess)
+    if ((e = launch_combine(part, nsplit, crow, wrow, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st)) != cudaSuccess)
       return cuda_fail(e, "combine kernels");
   } else {
-    if ((e = launch_combine(part, 1, crow, mask, 0, tau, lse, bsum, bcnt, 0, hdr, loss, st)) != cudaSuccess)
+    if ((e = launch_combine(part, 1, crow, wrow, 0, tau, lse, bsum, bcnt, 0, hdr, loss, st)) != cudaSuccess)
       return cuda_fail(e, "combine kernels");
   }
   return FKL_OK;
@@ -318,10 +354,21 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
                         const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K,
                         float tau, int64_t chunk, float* dH, float* dW, void* workspace,
                         size_t ws_bytes, void* stream) {
+  return fkl_backward_ex(H, W, topk_idx, topk_logits, mask, lse, grad_loss, T, d, V, K, tau, chunk, nullptr, dH, dW,
+                         workspace, ws_bytes, stream);
+}
+
+fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                           const float* topk_logits, const uint8_t* mask, const float* lse,
+                           const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K,
+                           float tau, int64_t chunk, const fkl_options* opts, float* dH, float* dW,
+                           void* workspace, size_t ws_bytes, void* stream) {
   g_last_error.clear();
   Plan pl;
   fkl_status s = check_common(H, W, topk_idx, topk_logits, T, d, V, K, tau, chunk, workspace, ws_bytes, &pl);
   if (s != FKL_OK) return s;
+  if ((s = check_options(opts, T)) != FKL_OK) return s;
+  const int accum = opts ? opts->accumulate : 0;
   if (dW == nullptr || (T > 0 && (dH == nullptr || lse == nullptr)))
     return fail(FKL_ERR_INVALID_ARG, "dH, dW and lse must not be NULL");
   if (!aligned(dW, 16) || (dH && !aligned(dH, 16))) return fail(FKL_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
@@ -335,7 +382,7 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
   if (T == 0) {
-    if ((e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * 4, st)) != cudaSuccess)
+    if (!(accum & FKL_ACCUMULATE_DW) && (e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * 4, st)) != cudaSuccess)
       return cuda_fail(e, "cudaMemsetAsync(dW)");
     return FKL_OK;
   }
@@ -345,7 +392,8 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
 
   if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st)) != cudaSuccess)
     return cuda_fail(e, "prep kernel");
-  if ((e = launch_bwd_scalars(mask, T, grad_loss, tau, hdr, st)) != cudaSuccess) return cuda_fail(e, "scalars kernel");
+  if ((e = run_weights(opts, mask, T, ws, pl, hdr, st)) != cudaSuccess) return cuda_fail(e, "weights kernels");
+  if ((e = launch_grad_scale(grad_loss, tau, hdr, st)) != cudaSuccess) return cuda_fail(e, "scale kernel");
 
   // All three products use two-SM tiles (256 rows per CTA pair, B split between the CTAs).
   const int bnd = choose_bn_d(d, true);
@@ -374,7 +422,8 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(w, kVocabTile);
     const GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
     DsParams dp;
-    dp.pairs = pairs; dp.lse = lse; dp.mask = mask; dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
+    dp.pairs = pairs; dp.lse = lse; dp.wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
+    dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
     dp.T = (int)T; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
     dp.scale2 = 1.4426950408889634f / tau;
     const double slab_flops = 2.0 * T * w * d;
@@ -387,7 +436,8 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     g4.a_box3d = d3d ? 1 : 0;
     g4.b_box3d = h3d ? 1 : 0;
     F32Params p4;
-    p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d; p4.accumulate = 0; p4.vec_ok = 1;
+    p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
+    p4.accumulate = (accum & FKL_ACCUMULATE_DW) ? 1 : 0; p4.vec_ok = 1;
     trace_launch_begin(st);
     if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
       return cuda_fail(e, "dW GEMM");
@@ -397,7 +447,8 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
     GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
     g5.b_box3d = w3d ? 1 : 0;
     F32Params p5;
-    p5.out = dH; p5.ldo = d; p5.M = (int)T; p5.N = (int)d; p5.accumulate = j > 0 ? 1 : 0; p5.vec_ok = 1;
+    p5.out = dH; p5.ldo = d; p5.M = (int)T; p5.N = (int)d;
+    p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = 1;
     trace_launch_begin(st);
     if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
       return cuda_fail(e, "dH GEMM");
@@ -418,6 +469,7 @@ fkl_status fkl_read_status(const void* workspace, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
   if (h & kStatusBadIdBit) return FKL_ERR_BAD_TOPK_ID;
   if (h & kStatusBadRowBit) return FKL_ERR_BAD_TOPK_ROW;
+  if (h & kStatusBadSeqBit) return FKL_ERR_BAD_SEQ_ID;
   if (h & kStatusTimeoutBit) return FKL_ERR_TIMEOUT;
   return FKL_OK;
 }

@@ -173,8 +173,8 @@ struct EpiFwd {
 };
 
 // ------------------------------------------------------------------ backward dS epilogue
-// dS[t, v] = dscale * (exp2(s * log2(e)/tau - lse_t * log2(e)) - ptilde[t, v]) for valid
-// rows, 0 for masked rows, rounded to bf16 and written to the slab buffer.
+// dS[t, v] = g tau w_t (exp2(s * log2(e)/tau - lse_t * log2(e)) - ptilde[t, v]) (w_t = 0 for
+// masked rows), rounded to bf16 and written to the slab buffer.
 struct EpiDs {
   using Params = DsParams;
   const Params& p;
@@ -191,8 +191,7 @@ struct EpiDs {
     row_ok = t < p.T;
     if (row_ok) {
       lse2 = p.lse[t] * 1.4426950408889634f;
-      const bool valid = (p.mask == nullptr) || (p.mask[t] != 0);
-      f = valid ? p.hdr->dscale : 0.f;
+      f = p.hdr->gtau * p.wrow[t];
       dst = p.ds + static_cast<size_t>(t) * p.ld_ds;
       cur.seek(p.pairs + static_cast<size_t>(t) * p.K, p.K, p.v0 + n_begin * kVocabTile);
     } else {

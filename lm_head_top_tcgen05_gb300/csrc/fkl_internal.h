@@ -12,13 +12,15 @@ namespace fkl {
 constexpr uint32_t kStatusBadIdBit = 1u;
 constexpr uint32_t kStatusBadRowBit = 2u;
 constexpr uint32_t kStatusTimeoutBit = 4u;
+constexpr uint32_t kStatusBadSeqBit = 8u;
 
-// Workspace header (first 256 bytes): status word, valid-token count, dS scale.
+// Workspace header (first 256 bytes): status word, valid tokens, sequences with a valid
+// token, and g * tau (the backward's dS scale is g * tau * w_t).
 struct WsHeader {
   uint32_t status;
   int32_t n_valid;
-  float dscale;  // g * tau / N (0 when N = 0)
-  float pad;
+  int32_t n_seqs;
+  float gtau;
 };
 
 constexpr int kVocabTile = 256;                   // tile width of the vocabulary axis
@@ -31,7 +33,7 @@ struct Plan {
   int64_t Vc;      // vocabulary columns per backward slab (multiple of kVocabTile)
   int64_t nslabs;  // number of backward slabs
   int64_t nb;      // row blocks of the combine step (256 rows each)
-  size_t off_pairs, off_crow, off_part, off_bsum, off_bcnt, off_ds, total;
+  size_t off_pairs, off_crow, off_wrow, off_scnt, off_part, off_bsum, off_bcnt, off_ds, total;
 };
 
 // Sets the message that fkl_last_error() returns on the calling thread.
@@ -50,11 +52,13 @@ int plan_splits(int m_tiles, int n_tiles, int sms);
 // ---------------------------------------------------------------- small kernels
 cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t T, int K, int V, float tau,
                         int2* pairs, float* crow, uint32_t* status, cudaStream_t st);
-cudaError_t launch_combine(const float* part, int nsplit, const float* crow, const uint8_t* mask,
+// Token weights w_t into wrow[T] (and N, S into the header); seq may be NULL (one sequence).
+cudaError_t launch_weights(const uint8_t* mask, const int32_t* seq, int num_seqs, int per_sequence,
+                           int64_t T, int* cnt, WsHeader* hdr, float* wrow, cudaStream_t st);
+cudaError_t launch_combine(const float* part, int nsplit, const float* crow, const float* wrow,
                            int64_t T, float tau, float* lse, double* bsum, int* bcnt, int64_t nb,
                            WsHeader* hdr, float* loss, cudaStream_t st);
-cudaError_t launch_bwd_scalars(const uint8_t* mask, int64_t T, const float* grad, float tau,
-                               WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_grad_scale(const float* grad, float tau, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_poison(float* a, int64_t na, float* b, int64_t nb, const uint32_t* status,
                           int sms, cudaStream_t st);
 cudaError_t launch_wait_timeout_test(uint32_t* status, uint64_t limit_ns, cudaStream_t st);
@@ -85,11 +89,11 @@ struct FwdParams {
   float scale2;       // log2(e) / tau
 };
 
-// Backward recompute: dS = dscale * (q - ptilde) for one vocabulary slab, bf16.
+// Backward recompute: dS = g tau w_t (q - ptilde) for one vocabulary slab, bf16.
 struct DsParams {
   const int2* pairs;
   const float* lse;
-  const uint8_t* mask;
+  const float* wrow;  // w_t (0 for masked tokens)
   const WsHeader* hdr;
   uint16_t* ds;       // [T][ld_ds]
   int64_t ld_ds;

@@ -20,8 +20,8 @@
 namespace fkl {
 
 // Largest forward scratch the static array holds: 64 MiB.  The forward needs about
-// T * (8K + 392) bytes (sorted teacher pairs, entropy terms, per-split partials, block sums),
-// so T up to about 56K tokens at K = 100.
+// T * (8K + 400) bytes (sorted teacher pairs, entropy terms, token weights and counts,
+// per-split partials, block sums), so T up to about 56K tokens at K = 100.
 constexpr size_t kNoAllocScratchBytes = size_t{64} << 20;
 
 static __device__ __align__(256) unsigned char fkl_static_scratch[kNoAllocScratchBytes];
@@ -83,7 +83,7 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
     char msg[256];
     snprintf(msg, sizeof(msg),
              "this shape needs %zu bytes of forward scratch; the static scratch holds %zu bytes "
-             "(about T * (8K + 392) bytes are needed)", need, kNoAllocScratchBytes);
+             "(about T * (8K + 400) bytes are needed)", need, kNoAllocScratchBytes);
     return noalloc_fail(FKL_ERR_WORKSPACE, msg);
   }
   uint8_t* ws = nullptr;
@@ -100,13 +100,16 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
   float* part = reinterpret_cast<float*>(ws + pl.off_part);
   double* bsum = reinterpret_cast<double*>(ws + pl.off_bsum);
   int* bcnt = reinterpret_cast<int*>(ws + pl.off_bcnt);
+  float* wrow = reinterpret_cast<float*>(ws + pl.off_wrow);
   if (T == 0) {
-    if (launch_combine(part, 1, crow, mask, 0, tau, lse, bsum, bcnt, 0, hdr, loss, st) != cudaSuccess)
+    if (launch_combine(part, 1, crow, wrow, 0, tau, lse, bsum, bcnt, 0, hdr, loss, st) != cudaSuccess)
       return noalloc_fail(FKL_ERR_CUDA, "combine launch failed");
     return FKL_OK;
   }
   if (launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st) != cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "prep launch failed");
+  if (launch_weights(mask, nullptr, 1, 0, T, reinterpret_cast<int*>(ws + pl.off_scnt), hdr, wrow, st) != cudaSuccess)
+    return noalloc_fail(FKL_ERR_CUDA, "weights launch failed");
   CUtensorMap mH, mW;
   if (!encode_map_bf16(&mH, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, W, d, V, d * 2, 64, kVocabTile))
     return noalloc_fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
@@ -121,7 +124,7 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
   fp.scale2 = 1.4426950408889634f / tau;
   if (launch_gemm_fwd(mH, mW, g, fp, g.num_units < sms ? g.num_units : sms, st) != cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "forward GEMM launch failed");
-  if (launch_combine(part, nsplit, crow, mask, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st) != cudaSuccess)
+  if (launch_combine(part, nsplit, crow, wrow, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st) != cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "combine launch failed");
   return FKL_OK;
 }

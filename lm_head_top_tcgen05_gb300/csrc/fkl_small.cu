@@ -2,9 +2,12 @@
 //   prep      teacher side of the loss: p = softmax(z / tau) over the K cached slots,
 //             c_t = sum_k p log p, and the (id, p) pairs of each row sorted by id so that
 //             the GEMM epilogues can walk them in step with the vocabulary tiles;
-//   combine   merges the forward's per-split partials into lse_t and KL_t and reduces the
-//             loss over valid tokens in a fixed order (no float atomics: deterministic);
-//   scalars   valid-token count and the dS scale g * tau / N for the backward;
+//   weights   the weight w_t of each token's KL in the loss: 1/N (token mean) or
+//             1/(S N_s) (mean over the S packed sequences of each sequence's token mean),
+//             0 for masked tokens; from integer counts, so deterministic;
+//   combine   merges the forward's per-split partials into lse_t and KL_t and reduces
+//             sum_t w_t KL_t in a fixed order (no float atomics: deterministic);
+//   scalars   g * tau for the backward's dS scale (g may live on the device);
 //   poison    fills the gradients with NaN when the device recorded an error;
 //   timeout   one bounded wait that nothing completes (checks the timeout path).
 #include <climits>
@@ -105,10 +108,10 @@ cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t T, int 
 constexpr int kCombineThreads = 256;
 
 // Per token: lse_t from the splits' (max, sum) in base 2, KL_t = c_t - g_t / tau + lse_t,
-// then a fixed-order tree sum of KL over the valid tokens of the block.
+// then a fixed-order tree sum of w_t KL_t over the tokens of the block.
 __global__ void __launch_bounds__(kCombineThreads)
     combine_rows_kernel(const float* __restrict__ part, int nsplit, const float* __restrict__ crow,
-                        const uint8_t* __restrict__ mask, int64_t T, float inv_tau,
+                        const float* __restrict__ wrow, int64_t T, float inv_tau,
                         float* __restrict__ lse, double* __restrict__ bsum, int* __restrict__ bcnt) {
   __shared__ double ssum[kCombineThreads];
   __shared__ int scnt[kCombineThreads];
@@ -127,8 +130,10 @@ __global__ void __launch_bounds__(kCombineThreads)
     }
     const float lse_t = (M + log2f(L)) * 0.69314718055994531f;
     lse[t] = lse_t;
-    if (mask == nullptr || mask[t] != 0) {
-      kl = static_cast<double>(crow[t]) - static_cast<double>(G) * inv_tau + static_cast<double>(lse_t);
+    const float w = wrow[t];
+    if (w != 0.f) {
+      kl = static_cast<double>(w) *
+           (static_cast<double>(crow[t]) - static_cast<double>(G) * inv_tau + static_cast<double>(lse_t));
       cnt = 1;
     }
   }
@@ -172,20 +177,18 @@ __global__ void __launch_bounds__(kFinalThreads)
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    const long long n = scnt[0];
-    double L = n > 0 ? static_cast<double>(tau) * tau * ssum[0] / static_cast<double>(n) : 0.0;
+    double L = scnt[0] > 0 ? static_cast<double>(tau) * tau * ssum[0] : 0.0;
     if (hdr->status != 0u) L = NAN;
-    hdr->n_valid = static_cast<int32_t>(n);
     *loss = static_cast<float>(L);
   }
 }
 
-cudaError_t launch_combine(const float* part, int nsplit, const float* crow, const uint8_t* mask,
+cudaError_t launch_combine(const float* part, int nsplit, const float* crow, const float* wrow,
                            int64_t T, float tau, float* lse, double* bsum, int* bcnt, int64_t nb,
                            WsHeader* hdr, float* loss, cudaStream_t st) {
   if (T > 0) {
     combine_rows_kernel<<<static_cast<unsigned>(nb), kCombineThreads, 0, st>>>(
-        part, nsplit, crow, mask, T, 1.0f / tau, lse, bsum, bcnt);
+        part, nsplit, crow, wrow, T, 1.0f / tau, lse, bsum, bcnt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -193,34 +196,90 @@ cudaError_t launch_combine(const float* part, int nsplit, const float* crow, con
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- backward scalars
-__global__ void __launch_bounds__(kFinalThreads)
-    bwd_scalars_kernel(const uint8_t* __restrict__ mask, int64_t T, const float* grad, float tau,
-                       WsHeader* hdr) {
-  __shared__ long long scnt[kFinalThreads];
-  long long c = 0;
-  if (mask == nullptr) {
-    c = threadIdx.x == 0 ? T : 0;
-  } else {
-    for (int64_t i = threadIdx.x; i < T; i += kFinalThreads) c += mask[i] != 0;
+// ---------------------------------------------------------------- token weights
+constexpr int kWeightThreads = 256;
+
+// Valid tokens per sequence (token mean: everything in sequence 0).  Integer atomics: the
+// counts do not depend on the order of the additions.
+__global__ void __launch_bounds__(kWeightThreads)
+    seq_count_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ seq, int64_t T,
+                     int num_seqs, int* __restrict__ cnt, uint32_t* __restrict__ status) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWeightThreads + threadIdx.x;
+  if (t >= T) return;
+  if (mask != nullptr && mask[t] == 0) return;
+  const int sid = seq ? seq[t] : 0;
+  if (sid < 0 || sid >= num_seqs) {
+    atomicOr(status, kStatusBadSeqBit);
+    return;
   }
-  scnt[threadIdx.x] = c;
+  atomicAdd(&cnt[sid], 1);
+}
+
+// N = sum of the counts, S = number of sequences with a valid token (fixed-order tree sums).
+__global__ void __launch_bounds__(kFinalThreads)
+    seq_total_kernel(const int* __restrict__ cnt, int num_seqs, WsHeader* hdr) {
+  __shared__ long long sn[kFinalThreads];
+  __shared__ int ss[kFinalThreads];
+  long long n = 0;
+  int nz = 0;
+  for (int i = threadIdx.x; i < num_seqs; i += kFinalThreads) {
+    n += cnt[i];
+    nz += cnt[i] > 0;
+  }
+  sn[threadIdx.x] = n;
+  ss[threadIdx.x] = nz;
   __syncthreads();
   for (int o = kFinalThreads / 2; o > 0; o >>= 1) {
-    if (threadIdx.x < o) scnt[threadIdx.x] += scnt[threadIdx.x + o];
+    if (threadIdx.x < o) {
+      sn[threadIdx.x] += sn[threadIdx.x + o];
+      ss[threadIdx.x] += ss[threadIdx.x + o];
+    }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    const long long n = scnt[0];
-    const float g = grad ? *grad : 1.0f;
-    hdr->n_valid = static_cast<int32_t>(n);
-    hdr->dscale = n > 0 ? static_cast<float>(static_cast<double>(g) * tau / static_cast<double>(n)) : 0.f;
+    hdr->n_valid = static_cast<int32_t>(sn[0]);
+    hdr->n_seqs = ss[0];
   }
 }
 
-cudaError_t launch_bwd_scalars(const uint8_t* mask, int64_t T, const float* grad, float tau,
-                               WsHeader* hdr, cudaStream_t st) {
-  bwd_scalars_kernel<<<1, kFinalThreads, 0, st>>>(mask, T, grad, tau, hdr);
+__global__ void __launch_bounds__(kWeightThreads)
+    row_weight_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ seq, int64_t T,
+                      int num_seqs, int per_sequence, const int* __restrict__ cnt, const WsHeader* hdr,
+                      float* __restrict__ wrow) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWeightThreads + threadIdx.x;
+  if (t >= T) return;
+  float w = 0.f;
+  const bool valid = mask == nullptr || mask[t] != 0;
+  const int sid = seq ? seq[t] : 0;
+  if (valid && sid >= 0 && sid < num_seqs) {
+    if (per_sequence) {
+      w = static_cast<float>(1.0 / (static_cast<double>(hdr->n_seqs) * static_cast<double>(cnt[sid])));
+    } else {
+      w = static_cast<float>(1.0 / static_cast<double>(hdr->n_valid));
+    }
+  }
+  wrow[t] = w;
+}
+
+cudaError_t launch_weights(const uint8_t* mask, const int32_t* seq, int num_seqs, int per_sequence,
+                           int64_t T, int* cnt, WsHeader* hdr, float* wrow, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(num_seqs) * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = static_cast<unsigned>((T + kWeightThreads - 1) / kWeightThreads);
+  seq_count_kernel<<<blocks, kWeightThreads, 0, st>>>(mask, seq, T, num_seqs, cnt, &hdr->status);
+  seq_total_kernel<<<1, kFinalThreads, 0, st>>>(cnt, num_seqs, hdr);
+  row_weight_kernel<<<blocks, kWeightThreads, 0, st>>>(mask, seq, T, num_seqs, per_sequence, cnt, hdr, wrow);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- backward scale
+__global__ void grad_scale_kernel(const float* grad, float tau, WsHeader* hdr) {
+  hdr->gtau = (grad ? *grad : 1.0f) * tau;
+}
+
+cudaError_t launch_grad_scale(const float* grad, float tau, WsHeader* hdr, cudaStream_t st) {
+  grad_scale_kernel<<<1, 1, 0, st>>>(grad, tau, hdr);
   return cudaGetLastError();
 }
 

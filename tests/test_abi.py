@@ -128,3 +128,35 @@ def test_python_binding_needs_cuda_tensors():
     H = torch.zeros(4, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fkl.forward(H, H, torch.zeros(4, 1, dtype=torch.int32), torch.zeros(4, 1))
+
+
+def test_options_are_checked_on_host(L):
+    from lm_head_top_tcgen05_gb300._lib import FklOptions
+
+    ws_bytes = L.fkl_workspace_size(256, 256, 4096, 16, 64)
+
+    def fwd(o):
+        return L.fkl_forward_ex(16, 16, 16, 16, None, 256, 256, 4096, 16, 1.0, 64, ctypes.byref(o), 16, 16, 256,
+                                ws_bytes, None)
+
+    o = FklOptions()
+    o.reserved = 1
+    assert fwd(o) == INVALID
+    o = FklOptions()
+    o.normalization = 5
+    assert fwd(o) == INVALID
+    o = FklOptions()
+    o.normalization = 1
+    o.num_seqs = 3
+    assert fwd(o) == INVALID          # seq_ids missing
+    o.seq_ids = 16
+    o.num_seqs = 0
+    assert fwd(o) == INVALID          # no sequence
+    o.num_seqs = 257
+    assert fwd(o) == INVALID          # more sequences than tokens
+    o.num_seqs = 3
+    o.seq_ids = 18
+    assert fwd(o) == ALIGN
+    o = FklOptions()
+    o.accumulate = 4
+    assert fwd(o) == INVALID

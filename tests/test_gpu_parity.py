@@ -188,3 +188,73 @@ def test_autograd_wrapper(fkl):
     assert H.grad.dtype == torch.bfloat16 and W.grad.dtype == torch.bfloat16
     assert_grad_close(H.grad.double().cpu().numpy(), ref["dH"], "H.grad")
     assert_grad_close(W.grad.double().cpu().numpy(), ref["dW"], "W.grad")
+
+
+# ---------------------------------------------------------------- variants: packed sequences, accumulation
+
+def run_oracle_seq(x, seq, grad=1.0):
+    H64, W64 = oracle.to_f64(x.H), oracle.to_f64(x.W)
+    f = oracle.forward(H64, W64, x.topk_idx, x.topk_logits, x.mask, x.tau, norm="sequences", seq_ids=seq)
+    dH, dW = oracle.backward(H64, W64, x.topk_idx, x.topk_logits, x.mask, x.tau, grad=grad,
+                             norm="sequences", seq_ids=seq)
+    return dict(loss=f["loss"], lse=f["lse"], dH=dH, dW=dW)
+
+
+def packed_case(seed=40):
+    x = workloads.make_random(300, 200, 5000, 16, tau=2.0, chunk=128, seed=seed, mask_frac=0.1)
+    lengths = [40, 130, 7, 90, 33]  # the third sequence is entirely masked below
+    seq = np.concatenate([np.full(n, i) for i, n in enumerate(lengths)]).astype(np.int32)
+    x.mask[170:177] = 0
+    return x, seq
+
+
+def test_sequence_mean_parity(fkl):
+    x, seq = packed_case()
+    H, W, idx, z, m = to_dev(x)
+    sid = torch.from_numpy(seq).cuda()
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk, seq_ids=sid, num_seqs=5)
+    dH, dW = fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, seq_ids=sid, num_seqs=5)
+    torch.cuda.synchronize()
+    gpu = dict(loss=loss.item(), lse=lse.cpu().numpy().astype(np.float64), dH=dH.cpu().numpy().astype(np.float64),
+               dW=dW.cpu().numpy().astype(np.float64), status=fkl.read_status(device="cuda"))
+    ref = run_oracle_seq(x, seq)
+    tok = run_oracle(x)
+    assert abs(ref["loss"] - tok["loss"]) > 1e-3 * abs(tok["loss"])  # the two normalisers differ here
+    assert_parity(gpu, ref)
+
+
+def test_sequence_mean_autograd(fkl):
+    x, seq = packed_case(41)
+    H, W, idx, z, m = to_dev(x)
+    H.requires_grad_(True)
+    W.requires_grad_(True)
+    loss = fkl.fused_kl(H, W, idx, z, m, tau=x.tau, chunk=64, seq_ids=torch.from_numpy(seq).cuda(), num_seqs=5)
+    loss.backward()
+    ref = run_oracle_seq(x, seq)
+    assert abs(loss.item() - ref["loss"]) <= LOSS_RTOL * abs(ref["loss"])
+    assert_grad_close(H.grad.double().cpu().numpy(), ref["dH"], "H.grad")
+
+
+def test_bad_sequence_id_is_reported(fkl):
+    x, seq = packed_case(42)
+    seq[5] = 7  # outside [0, 5) on a valid token
+    H, W, idx, z, m = to_dev(x)
+    loss, _ = fkl.forward(H, W, idx, z, m, x.tau, x.chunk, seq_ids=torch.from_numpy(seq).cuda(), num_seqs=5)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 9 and np.isnan(loss.item())
+
+
+def test_gradient_accumulation(fkl):
+    x = workloads.make_random(300, 200, 5000, 16, tau=1.5, chunk=128, seed=43, mask_frac=0.1)
+    H, W, idx, z, m = to_dev(x)
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    dH0 = torch.randn(H.shape, device="cuda", generator=g)
+    dW0 = torch.randn(W.shape, device="cuda", generator=g)
+    dH, dW = dH0.clone(), dW0.clone()
+    fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, out=(dH, dW), accumulate=True)
+    fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, out=(dH, dW), accumulate=True)
+    torch.cuda.synchronize()
+    ref = run_oracle(x, grad=2.0)  # two micro-batches of the same gradient
+    assert_grad_close((dH - dH0).double().cpu().numpy(), ref["dH"], "accumulated dH")
+    assert_grad_close((dW - dW0).double().cpu().numpy(), ref["dW"], "accumulated dW")
