@@ -65,7 +65,8 @@ typedef enum fkl_status {
   FKL_ERR_BAD_TOPK_ID = 6,  /* device: a teacher id is outside [0, V) */
   FKL_ERR_BAD_TOPK_ROW = 7, /* device: a teacher row has no finite logit */
   FKL_ERR_TIMEOUT = 8,      /* device: a pipeline wait exceeded its time limit */
-  FKL_ERR_BAD_SEQ_ID = 9    /* device: a valid token's sequence id is outside [0, num_seqs) */
+  FKL_ERR_BAD_SEQ_ID = 9,   /* device: a valid token's sequence id is outside [0, num_seqs) */
+  FKL_ERR_TOPK_OVERFLOW = 10 /* device: fkl_teacher_topk found more tied candidates than it holds */
 } fkl_status;
 
 /*
@@ -199,10 +200,27 @@ fkl_status fkl_trace_stop(void);
 /*
  * Waits for the recorded events and writes, for up to `capacity` recorded launches in launch
  * order, the duration in milliseconds (ms), the kind (0 forward projection + logsumexp,
- * 1 dS recompute, 2 dW, 3 dH) and the launch's algorithmic FLOPs (2 * M * N * K of its
- * product).  Any output pointer may be NULL.  Returns the number written, -1 on a CUDA error.
+ * 1 dS recompute, 2 dW, 3 dH, 5 teacher top-K bound pass, 6 teacher top-K candidate pass)
+ * and the launch's algorithmic FLOPs (2 * M * N * K of its product).  Any output pointer may be NULL.  Returns the number written, -1 on a CUDA error.
  */
 int32_t fkl_trace_read(float* ms, int32_t* kind, double* flops, int32_t capacity);
+
+/*
+ * Offline teacher cache ("Two systems changes", paragraph "Offline distillation": the teacher
+ * runs once and the top-100 tokens per position are stored): for the teacher's final hidden
+ * states Ht (bf16 [T, d]) and LM head Wt (bf16 [V, d]), writes the K largest logits of each
+ * row of s = Ht Wt^T (fp32 accumulation) and their ids, ordered by logit descending, ties by
+ * the lower id: topk_idx int32 [T, K] and topk_logits fp32 [T, K] - the cache that
+ * fkl_forward reads.  The T x V logits are never written: the projection runs twice, once to
+ * find a per-row lower bound of the K-th largest logit, once to collect the logits at or
+ * above it (at most max(512, 4K) per row; more, which needs massive ties, is reported as
+ * FKL_ERR_TOPK_OVERFLOW with id -1 and logit NaN in that row).  Limits: 1 <= K <= V,
+ * d % 8 == 0; when V > 4096 also K <= 256 and K <= 8 * ceil(V / 256).
+ */
+size_t fkl_teacher_topk_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K);
+fkl_status fkl_teacher_topk(const uint16_t* Ht, const uint16_t* Wt, int64_t T, int64_t d, int64_t V,
+                            int64_t K, int32_t* topk_idx, float* topk_logits, void* workspace,
+                            size_t ws_bytes, void* stream);
 
 /* Static text for a status code. */
 const char* fkl_status_string(int status);

@@ -23,7 +23,7 @@ from ._lib import (FKL_ACCUMULATE_DH, FKL_ACCUMULATE_DW, FKL_NORM_SEQUENCES, FKL
                    FKL_OK, STATUS, FklError, FklOptions, check, lib)
 
 __all__ = ["workspace_size", "Workspace", "forward", "backward", "read_status", "fused_kl",
-           "FusedKL", "FklError", "STATUS"]
+           "FusedKL", "FklError", "STATUS", "teacher_topk"]
 
 
 def workspace_size(T: int, d: int, V: int, K: int, chunk: int) -> int:
@@ -197,3 +197,25 @@ def fused_kl(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
     """tau^2 * KL(teacher top-K || student) averaged over valid tokens (or, with seq_ids, over
     packed sequences of their token means); differentiable in H and W."""
     return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids, num_seqs)
+
+
+def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int = 100,
+                 workspace: Optional[Workspace] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Offline teacher cache: (topk_idx int32 [T, K], topk_logits float32 [T, K]) of the K
+    largest teacher logits Ht Wt^T per row, by logit descending (ties: lower id first)."""
+    if not (Ht.is_cuda and Wt.is_cuda) or Ht.dtype != torch.bfloat16 or Wt.dtype != torch.bfloat16:
+        raise TypeError("Ht and Wt must be bfloat16 CUDA tensors")
+    if Ht.dim() != 2 or Wt.dim() != 2 or Ht.shape[1] != Wt.shape[1] or not (Ht.is_contiguous() and Wt.is_contiguous()):
+        raise ValueError("Ht must be [T, d] and Wt [V, d], contiguous")
+    T, d = Ht.shape
+    V = Wt.shape[0]
+    n = lib().fkl_teacher_topk_workspace_size(T, d, V, K)
+    if n == 0:
+        raise FklError(1, "fkl_teacher_topk_workspace_size", f"unsupported shape T={T} d={d} V={V} K={K}")
+    ws = _ws_for(workspace, int(n), Ht.device)
+    idx = torch.empty((T, K), dtype=torch.int32, device=Ht.device)
+    val = torch.empty((T, K), dtype=torch.float32, device=Ht.device)
+    st = lib().fkl_teacher_topk(_ptr(Ht), _ptr(Wt), T, d, V, K, _ptr(idx), _ptr(val), _ptr(ws), ws.numel(),
+                                _stream(Ht.device))
+    check(st, "fkl_teacher_topk")
+    return idx, val

@@ -21,6 +21,7 @@ STATUS = {
     7: "FKL_ERR_BAD_TOPK_ROW",
     8: "FKL_ERR_TIMEOUT",
     9: "FKL_ERR_BAD_SEQ_ID",
+    10: "FKL_ERR_TOPK_OVERFLOW",
 }
 FKL_OK = 0
 
@@ -53,6 +54,8 @@ _SIGNATURES = {
                                       ctypes.POINTER(FklOptions), _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_backward_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                        _I64, ctypes.POINTER(FklOptions), _P, _P, _P, ctypes.c_size_t, _P]),
+    "fkl_teacher_topk_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
+    "fkl_teacher_topk": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_read_status": (ctypes.c_int, [_P, _P]),
     "fkl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fkl_last_error": (ctypes.c_char_p, []),

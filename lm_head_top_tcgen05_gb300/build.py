@@ -19,7 +19,8 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 INCLUDE = PKG.parent / "include"
 LIB = PKG / "libfkl.so"
-SOURCES = ["fkl_api.cu", "fkl_small.cu", "fkl_gemm_loss.cu", "fkl_gemm_f32.cu", "fkl_noalloc.cu", "fkl_trace.cu", "fkl_gemm2.cu"]
+SOURCES = ["fkl_api.cu", "fkl_small.cu", "fkl_gemm_loss.cu", "fkl_gemm_f32.cu", "fkl_noalloc.cu", "fkl_trace.cu", "fkl_gemm2.cu",
+           "fkl_topk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", str(INCLUDE)]

@@ -1,4 +1,5 @@
-// Host side of the C ABI (include/fkl.h, include/fkl_testing.h): argument checks, the
+// Host side of the C ABI (include/fkl.h, include/fkl_testing.h; the teacher cache producer is
+// in fkl_topk.cu, the allocation-free forward in fkl_noalloc.cu): argument checks, the
 // workspace plan, tensor-map encoding, the tile schedule and the launch sequences of the
 // forward and backward passes.  All work is enqueued on the caller's stream; nothing here
 // allocates device memory or synchronises, except fkl_read_status.
@@ -284,6 +285,7 @@ const char* fkl_status_string(int status) {
     case FKL_ERR_BAD_TOPK_ROW: return "teacher row without a finite logit";
     case FKL_ERR_TIMEOUT: return "device pipeline wait timed out";
     case FKL_ERR_BAD_SEQ_ID: return "sequence id outside [0, num_seqs)";
+    case FKL_ERR_TOPK_OVERFLOW: return "too many tied top-K candidates in a row";
     default: return "unknown status";
   }
 }
@@ -470,6 +472,7 @@ fkl_status fkl_read_status(const void* workspace, void* stream) {
   if (h & kStatusBadIdBit) return FKL_ERR_BAD_TOPK_ID;
   if (h & kStatusBadRowBit) return FKL_ERR_BAD_TOPK_ROW;
   if (h & kStatusBadSeqBit) return FKL_ERR_BAD_SEQ_ID;
+  if (h & kStatusTopkOverflowBit) return FKL_ERR_TOPK_OVERFLOW;
   if (h & kStatusTimeoutBit) return FKL_ERR_TIMEOUT;
   return FKL_OK;
 }

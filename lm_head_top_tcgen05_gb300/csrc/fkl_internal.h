@@ -13,6 +13,7 @@ constexpr uint32_t kStatusBadIdBit = 1u;
 constexpr uint32_t kStatusBadRowBit = 2u;
 constexpr uint32_t kStatusTimeoutBit = 4u;
 constexpr uint32_t kStatusBadSeqBit = 8u;
+constexpr uint32_t kStatusTopkOverflowBit = 16u;
 
 // Workspace header (first 256 bytes): status word, valid tokens, sequences with a valid
 // token, and g * tau (the backward's dS scale is g * tau * w_t).

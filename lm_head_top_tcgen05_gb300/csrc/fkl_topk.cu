@@ -1,0 +1,345 @@
+// Offline teacher cache: the K largest teacher logits per position (fkl_teacher_topk).
+//
+// "Efficient Knowledge Distillation for LLMs: Offline Top-K Logits and a Fused Chunked KL
+// Loss", section "Two systems changes", paragraph "Offline distillation": the teacher runs
+// once and its top-100 tokens and logits per position are stored and reused.  Here the
+// teacher's LM-head projection s = Ht Wt^T is fused with the selection, so the T x V logits
+// are never written; two passes over the projection run on the two-SM GEMM:
+//
+//   1. bound pass   each row keeps, per vocabulary split, its kTopR largest logits in
+//                   registers (EpiTopR).  bound_kernel takes the K-th largest of those
+//                   S * kTopR values: theta_t, a lower bound of the row's K-th largest logit
+//                   (it is the K-th largest of a subset of the row), usually a tight one.
+//   2. candidate    recompute; every logit >= theta_t is appended to the row's candidate
+//      pass         buffer (EpiCand; an integer atomic counter per row).  All of the row's
+//                   top K are among them.
+//   3. select       per row, rank the candidates by (logit descending, id ascending) and
+//                   write the first K.  The ranks do not depend on the order of the appends,
+//                   so the output is deterministic.
+//
+// A row with more candidates than the buffer holds (massive ties) is reported as
+// FKL_ERR_TOPK_OVERFLOW and its outputs are set to id -1 and logit NaN.  For small
+// vocabularies (V <= kAllCandidatesV) the bound pass is skipped and every logit of a row
+// is a candidate.
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/fkl.h"
+#include "fkl_gemm2.cuh"
+
+namespace fkl {
+
+constexpr int kTopR = 8;                // logits kept per (row, split) in the bound pass
+constexpr int kMaxBoundSplits = 32;     // splits of the bound pass
+constexpr int64_t kAllCandidatesV = 4096;
+
+struct TopRParams {
+  float* topr;  // [split][T][kTopR]
+  int T, V;
+};
+
+struct CandParams {
+  const float* theta;  // [T]
+  int* cnt;            // [T]
+  int2* cand;          // [T][cap]: (logit bits, id)
+  int cap, T, V;
+};
+
+// ---------------------------------------------------------------- bound pass epilogue
+struct EpiTopR {
+  using Params = TopRParams;
+  const Params& p;
+  int t;
+  bool row_ok;
+  float r[kTopR];  // descending
+
+  __device__ explicit EpiTopR(const Params& prm) : p(prm) {}
+
+  __device__ __forceinline__ void begin_unit(int row0, int, int, int row) {
+    t = row0 + row;
+    row_ok = t < p.T;
+#pragma unroll
+    for (int i = 0; i < kTopR; ++i) r[i] = -INFINITY;
+  }
+
+  __device__ __forceinline__ void insert(float x) {
+#pragma unroll
+    for (int i = kTopR - 1; i > 0; --i) r[i] = (x > r[i - 1]) ? r[i - 1] : fmaxf(r[i], x);
+    r[0] = fmaxf(r[0], x);
+  }
+
+  __device__ __forceinline__ void chunk(float (&v)[32], int col0) {
+    if (col0 + 32 > p.V) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j >= p.V) v[j] = -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (v[j] > r[kTopR - 1]) insert(v[j]);
+  }
+
+  template <int BN>
+  __device__ __forceinline__ void tile(uint32_t taddr, int n, int) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; c += 2) {
+      float v0[32], v1[32];
+      tmem_ld32(taddr + c * 32, v0);
+      tmem_ld32(taddr + c * 32 + 32, v1);
+      tmem_wait_ld();
+      pin(v0);
+      pin(v1);
+      chunk(v0, n * BN + c * 32);
+      chunk(v1, n * BN + c * 32 + 32);
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(int split, int) {
+    if (!row_ok) return;
+    float4* o = reinterpret_cast<float4*>(p.topr + (static_cast<size_t>(split) * p.T + t) * kTopR);
+    o[0] = make_float4(r[0], r[1], r[2], r[3]);
+    o[1] = make_float4(r[4], r[5], r[6], r[7]);
+  }
+};
+
+// ---------------------------------------------------------------- candidate pass epilogue
+struct EpiCand {
+  using Params = CandParams;
+  const Params& p;
+  int t;
+  float th;
+
+  __device__ explicit EpiCand(const Params& prm) : p(prm) {}
+
+  __device__ __forceinline__ void begin_unit(int row0, int, int, int row) {
+    t = row0 + row;
+    th = t < p.T ? p.theta[t] : INFINITY;
+  }
+
+  __device__ __forceinline__ void chunk(const float (&v)[32], int col0) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (v[j] >= th && col0 + j < p.V) {
+        const int pos = atomicAdd(&p.cnt[t], 1);
+        if (pos < p.cap) p.cand[static_cast<size_t>(t) * p.cap + pos] = make_int2(__float_as_int(v[j]), col0 + j);
+      }
+    }
+  }
+
+  template <int BN>
+  __device__ __forceinline__ void tile(uint32_t taddr, int n, int) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; c += 2) {
+      float v0[32], v1[32];
+      tmem_ld32(taddr + c * 32, v0);
+      tmem_ld32(taddr + c * 32 + 32, v1);
+      tmem_wait_ld();
+      pin(v0);
+      pin(v1);
+      chunk(v0, n * BN + c * 32);
+      chunk(v1, n * BN + c * 32 + 32);
+    }
+  }
+
+  __device__ __forceinline__ void end_unit(int, int) {}
+};
+
+// ---------------------------------------------------------------- bound and select kernels
+// Orderable key: ascending key = logit descending, then id ascending.
+__device__ __forceinline__ unsigned long long rank_key(float v, int id) {
+  uint32_t b = __float_as_uint(v);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);  // ascending float order as unsigned
+  return (static_cast<unsigned long long>(~b) << 32) | static_cast<uint32_t>(id);
+}
+
+constexpr int kBoundWarps = 8;
+
+// theta_t = the K-th largest of the row's S * kTopR kept logits (-inf when fewer than K).
+__global__ void __launch_bounds__(kBoundWarps * 32)
+    bound_kernel(const float* __restrict__ topr, int nsplit, int64_t T, int K, float* __restrict__ theta) {
+  __shared__ float sv[kBoundWarps][kMaxBoundSplits * kTopR];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kBoundWarps + w;
+  if (t >= T) return;  // uniform per warp
+  const int n = nsplit * kTopR;
+  for (int i = lane; i < n; i += 32) {
+    const int s = i / kTopR, k = i - s * kTopR;
+    sv[w][i] = topr[(static_cast<size_t>(s) * T + t) * kTopR + k];
+  }
+  __syncwarp();
+  float th = -INFINITY;
+  if (n >= K) {
+    for (int i = lane; i < n; i += 32) {
+      const float x = sv[w][i];
+      int rank = 0;  // position of (x, i) in the order by value descending, then index
+      for (int j = 0; j < n; ++j) {
+        const float y = sv[w][j];
+        rank += (y > x) || (y == x && j < i);
+      }
+      if (rank == K - 1) th = x;
+    }
+    th = fmaxf(th, __shfl_xor_sync(0xffffffffu, th, 16));
+    th = fmaxf(th, __shfl_xor_sync(0xffffffffu, th, 8));
+    th = fmaxf(th, __shfl_xor_sync(0xffffffffu, th, 4));
+    th = fmaxf(th, __shfl_xor_sync(0xffffffffu, th, 2));
+    th = fmaxf(th, __shfl_xor_sync(0xffffffffu, th, 1));
+  }
+  if (lane == 0) theta[t] = th;
+}
+
+constexpr int kSelectThreads = 128;
+
+// One block per row: ranks the row's candidates, writes the first K in order.
+__global__ void __launch_bounds__(kSelectThreads)
+    select_kernel(const int2* __restrict__ cand, const int* __restrict__ cnt, int cap, int K, int64_t T,
+                  int32_t* __restrict__ out_idx, float* __restrict__ out_val, uint32_t* __restrict__ status) {
+  extern __shared__ unsigned long long keys[];
+  const int64_t t = blockIdx.x;
+  if (t >= T) return;
+  const int total = cnt[t];
+  int32_t* oi = out_idx + t * K;
+  float* ov = out_val + t * K;
+  if (total > cap || total < K) {
+    for (int k = threadIdx.x; k < K; k += kSelectThreads) {
+      oi[k] = -1;
+      ov[k] = NAN;
+    }
+    if (threadIdx.x == 0) atomicOr(status, kStatusTopkOverflowBit);
+    return;
+  }
+  const int2* c = cand + t * cap;
+  for (int i = threadIdx.x; i < total; i += kSelectThreads) keys[i] = rank_key(__int_as_float(c[i].x), c[i].y);
+  __syncthreads();
+  for (int i = threadIdx.x; i < total; i += kSelectThreads) {
+    const unsigned long long ki = keys[i];
+    int rank = 0;
+    for (int j = 0; j < total; ++j) rank += keys[j] < ki;
+    if (rank < K) {
+      const int2 e = c[i];
+      oi[rank] = e.y;
+      ov[rank] = __int_as_float(e.x);
+    }
+  }
+}
+
+__global__ void fill_kernel(float* __restrict__ a, int64_t n, float v) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) a[i] = v;
+}
+
+// ---------------------------------------------------------------- planning
+struct TopkPlan {
+  bool bound_pass;
+  int cap;
+  size_t off_topr, off_theta, off_cnt, off_cand, total;
+};
+
+static bool make_topk_plan(int64_t T, int64_t d, int64_t V, int64_t K, TopkPlan* p) {
+  if (T < 0 || T >= (int64_t{1} << 31) || d < 8 || d % 8 != 0 || d >= (int64_t{1} << 20)) return false;
+  if (V < 1 || V > (int64_t{1} << 30) || K < 1 || K > V) return false;
+  p->bound_pass = V > kAllCandidatesV;
+  if (p->bound_pass && K > kMaxBoundSplits * kTopR) return false;
+  if (p->bound_pass && (V + 255) / 256 * kTopR < K) return false;
+  p->cap = p->bound_pass ? static_cast<int>(K * 4 > 512 ? K * 4 : 512) : static_cast<int>(V);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  size_t off = 256;  // status header
+  p->off_topr = off;  off = up(off + static_cast<size_t>(T) * (p->bound_pass ? kMaxBoundSplits * kTopR * 4 : 0));
+  p->off_theta = off; off = up(off + static_cast<size_t>(T) * 4);
+  p->off_cnt = off;   off = up(off + static_cast<size_t>(T) * 4);
+  p->off_cand = off;  off = up(off + static_cast<size_t>(T) * p->cap * 8);
+  p->total = off;
+  return true;
+}
+
+static fkl_status topk_fail(fkl_status s, const char* msg) {
+  set_last_error_message(msg);
+  return s;
+}
+
+}  // namespace fkl
+
+using namespace fkl;
+
+extern "C" size_t fkl_teacher_topk_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K) {
+  TopkPlan p;
+  return make_topk_plan(T, d, V, K, &p) ? p.total : 0;
+}
+
+extern "C" fkl_status fkl_teacher_topk(const uint16_t* Ht, const uint16_t* Wt, int64_t T, int64_t d, int64_t V,
+                                       int64_t K, int32_t* topk_idx, float* topk_logits, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+  set_last_error_message("");
+  TopkPlan pl;
+  if (!make_topk_plan(T, d, V, K, &pl))
+    return topk_fail(FKL_ERR_INVALID_ARG,
+                     "unsupported shape (need d % 8 == 0, 1 <= K <= V, and K <= 256 with K <= 8 * ceil(V / 256) "
+                     "when V > 4096)");
+  if (Wt == nullptr || (T > 0 && (Ht == nullptr || topk_idx == nullptr || topk_logits == nullptr)))
+    return topk_fail(FKL_ERR_INVALID_ARG, "a required pointer is NULL");
+  if ((reinterpret_cast<uintptr_t>(Ht) | reinterpret_cast<uintptr_t>(Wt)) % 16 != 0 ||
+      (reinterpret_cast<uintptr_t>(topk_idx) | reinterpret_cast<uintptr_t>(topk_logits)) % 4 != 0)
+    return topk_fail(FKL_ERR_ALIGNMENT, "Ht and Wt need 16-byte alignment, the outputs 4-byte");
+  if (workspace == nullptr || ws_bytes < pl.total) return topk_fail(FKL_ERR_WORKSPACE, "workspace missing or too small");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return topk_fail(FKL_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return topk_fail(FKL_ERR_CUDA, "device query failed");
+  if (major != 10 || minor != 3) return topk_fail(FKL_ERR_UNSUPPORTED, "device is not sm_103");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "cudaMemsetAsync failed");
+  if (T == 0) return FKL_OK;
+  float* topr = reinterpret_cast<float*>(ws + pl.off_topr);
+  float* theta = reinterpret_cast<float*>(ws + pl.off_theta);
+  int* cnt = reinterpret_cast<int*>(ws + pl.off_cnt);
+  int2* cand = reinterpret_cast<int2*>(ws + pl.off_cand);
+  if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(T) * 4, st) != cudaSuccess)
+    return topk_fail(FKL_ERR_CUDA, "cudaMemsetAsync failed");
+
+  CUtensorMap mH, mW;
+  if (!encode_map_bf16(&mH, Ht, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, Wt, d, V, d * 2, 64, kVocabTile / 2))
+    return topk_fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  const int pairs = sms / 2;
+  const int m_tiles = static_cast<int>((T + 255) / 256), n_tiles = static_cast<int>((V + kVocabTile - 1) / kVocabTile);
+  if (pl.bound_pass) {
+    const int ns = n_tiles < kMaxBoundSplits ? n_tiles : kMaxBoundSplits;
+    const GemmShape g = make_shape(T, V, d, kVocabTile, ns, status, 256);
+    TopRParams tp;
+    tp.topr = topr;
+    tp.T = static_cast<int>(T);
+    tp.V = static_cast<int>(V);
+    trace_launch_begin(st);
+    if (launch_gemm2_t<kVocabTile, false, false, EpiTopR>(mH, mW, g, tp, sms, st) != cudaSuccess)
+      return topk_fail(FKL_ERR_CUDA, "bound-pass GEMM launch failed");
+    trace_launch_end(st, 5, 2.0 * T * V * d);
+    bound_kernel<<<static_cast<unsigned>((T + kBoundWarps - 1) / kBoundWarps), kBoundWarps * 32, 0, st>>>(
+        topr, ns, T, static_cast<int>(K), theta);
+  } else {
+    fill_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(theta, T, -INFINITY);
+  }
+  if (cudaGetLastError() != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "bound kernel launch failed");
+  const GemmShape g2 = make_shape(T, V, d, kVocabTile, plan_splits(m_tiles, n_tiles, pairs), status, 256);
+  CandParams cp;
+  cp.theta = theta;
+  cp.cnt = cnt;
+  cp.cand = cand;
+  cp.cap = pl.cap;
+  cp.T = static_cast<int>(T);
+  cp.V = static_cast<int>(V);
+  trace_launch_begin(st);
+  if (launch_gemm2_t<kVocabTile, false, false, EpiCand>(mH, mW, g2, cp, sms, st) != cudaSuccess)
+    return topk_fail(FKL_ERR_CUDA, "candidate-pass GEMM launch failed");
+  trace_launch_end(st, 6, 2.0 * T * V * d);
+  const size_t smem = static_cast<size_t>(pl.cap) * 8;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return topk_fail(FKL_ERR_CUDA, "cudaFuncSetAttribute failed");
+  select_kernel<<<static_cast<unsigned>(T), kSelectThreads, smem, st>>>(cand, cnt, pl.cap, static_cast<int>(K), T,
+                                                                       topk_idx, topk_logits, status);
+  if (cudaGetLastError() != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "select kernel launch failed");
+  return FKL_OK;
+}
