@@ -214,6 +214,70 @@ def trace_summary(L, cap):
                 "tflops": f / (t / 1e3) / 1e12} for k, (c, t, f) in sorted(per.items())}
 
 
+def run_teacher_topk(args, world, rank, local_rank):
+    """Times the offline teacher cache producer: the workload's H and W stand in for the
+    teacher's final hidden states and LM head; K as in the workload."""
+    import torch
+
+    import lm_head_top_tcgen05_gb300 as fkl
+    import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w)
+    T, d, V, K = w.T, w.d, w.V, w.K
+    Ht, Wt = x.H.to(dev), x.W.to(dev)
+    ws = fkl.Workspace(dev)
+    for _ in range(args.warmup):
+        fkl.teacher_topk(Ht, Wt, K, workspace=ws)
+    torch.cuda.synchronize()
+    assert fkl.read_status(ws) == 0
+    L = fkl.lib()
+    cap = 2 * args.steps
+    fkl.check(L.fkl_trace_start(cap), "fkl_trace_start")
+    stream = torch.cuda.current_stream(dev)
+    with ClockSampler(local_rank) as clocks:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fkl.teacher_topk(Ht, Wt, K, workspace=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    L.fkl_trace_stop()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    kernels = trace_summary(L, cap)
+    status = fkl.read_status(ws)
+    peaks, peak_kind = load_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    dom = max(kernels, key=lambda k: kernels[k]["ms_total"])
+    names = {5: "gemm2_kernel<256,0,0,EpiTopR> (bound pass)", 6: "gemm2_kernel<256,0,0,EpiCand> (candidate pass)"}
+    out = {
+        "metric": "teacher top-K cache tokens/s (two projection passes, 4TVd)", "value": T * args.steps / elapsed,
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "d": d, "V": V, "K": K},
+        "tflops": 4.0 * T * V * d * args.steps / elapsed / 1e12, "status": status,
+        "roofline": {"bound": "tensor", "kernel": names.get(dom, str(dom)), "achieved": kernels[dom]["tflops"],
+                     "peak": sustained, "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / sustained,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained", "traffic": None},
+        "kernels": {names.get(k, str(k)): v for k, v in kernels.items()},
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+
+        rows = min(args.cpu_rows, T)
+        W64, H64 = oracle.to_f64(x.W), oracle.to_f64(x.H[:rows])
+        t0 = time.perf_counter()
+        oracle.teacher_topk(H64, W64, K)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                               "kind": "oracle", "sample": f"first {rows} tokens, full vocabulary, float64, {dt:.1f} s"}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -227,6 +291,9 @@ def main():
     ap.add_argument("--vocab", type=int, default=None,
                     help="override V (profiling case with the full workload's per-launch GEMM shapes)")
     ap.add_argument("--chunk", type=int, default=None, help="override chunk")
+    ap.add_argument("--mode", default="loss", choices=["loss", "teacher_topk"],
+                    help="loss: the fused KL fwd+bwd step (the headline); teacher_topk: the offline "
+                         "teacher cache producer on the same shapes")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -249,6 +316,9 @@ def main():
     dev = torch.device("cuda", local_rank)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
+    if args.mode == "teacher_topk":
+        run_teacher_topk(args, world, rank, local_rank)
+        return
     w = workloads.WORKLOADS[args.workload]
     if args.vocab is not None or args.chunk is not None:
         w = dataclasses.replace(w, name=f"{w.name}_V{args.vocab or w.V}_chunk{args.chunk or w.chunk}",
