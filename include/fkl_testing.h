@@ -29,7 +29,7 @@ extern "C" {
  * multiple of 64 is loaded with one 3-D TMA box per tile, unless bit 1 of `accumulate` is
  * set (then 64-wide 2-D boxes, the path used for other extents).  Bit 0 of `accumulate`
  * selects accumulation.  Bit 2 selects the two-SM kernel (CTA pairs, 256-row tiles, the one
- * the loss uses; bn 256 or 128) instead of the one-SM kernel (128-row tiles).  `workspace`
+ * the loss uses; a 192-wide tile with MN-major B uses the 64-byte swizzle) instead of the one-SM kernel (128-row tiles).  `workspace`
  * needs 256 bytes (the status word).
  */
 fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N,

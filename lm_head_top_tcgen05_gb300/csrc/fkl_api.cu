@@ -162,6 +162,44 @@ bool encode_map_mn3d(CUtensorMap* map, const void* base, uint64_t mn_extent, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_map_mn3d_sw64(CUtensorMap* map, const void* base, uint64_t mn_extent, uint64_t k_extent,
+                          uint64_t row_stride_bytes, uint32_t tile_mn) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || mn_extent % 32 != 0 || tile_mn % 32 != 0) return false;
+  const cuuint64_t dims[3] = {32, k_extent, mn_extent / 32};
+  const cuuint64_t strides[2] = {row_stride_bytes, 64};
+  const cuuint32_t box[3] = {32, 64, tile_mn / 32};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_map_bf16_sw64(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_stride_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {32, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MN-major B map of the two-SM kernel for tile width bn: the 3-D one-box-per-half view when
+// the extent allows, else per-atom 2-D boxes; 64-byte swizzle when a half is 96 wide.
+static bool encode_b_mn_pair(CUtensorMap* map, const void* base, uint64_t mn_extent, uint64_t k_extent,
+                             uint64_t row_stride_bytes, int bn, bool allow3d, bool* box3d) {
+  const bool sw64 = (bn / 2) % 64 != 0;
+  *box3d = allow3d && (sw64 ? encode_map_mn3d_sw64(map, base, mn_extent, k_extent, row_stride_bytes, bn / 2)
+                            : encode_map_mn3d(map, base, mn_extent, k_extent, row_stride_bytes, bn / 2));
+  if (*box3d) return true;
+  return sw64 ? encode_map_bf16_sw64(map, base, mn_extent, k_extent, row_stride_bytes)
+              : encode_map_bf16(map, base, mn_extent, k_extent, row_stride_bytes, 64, 64);
+}
+
 // ---------------------------------------------------------------- device info
 struct DevInfo {
   int sms = 0;
@@ -200,11 +238,14 @@ static fkl_status device_info(DevInfo* out) {
 // (narrower tiles need more operand bytes per FLOP).
 static int choose_bn_d(int64_t d, bool pair) {
   const int cand[3] = {256, 192, 128};
-  const double cost[3] = {1.0, 1.11, 1.4};
+  const double cost1[3] = {1.0, 1.11, 1.4};   // one-SM kernel
+  // Two-SM kernel: 192-wide tiles (96-wide MN-major B halves, 64-byte swizzle) measured ~23 %
+  // slower per FLOP than 256-wide ones on GB300, so they win only when 256 pads far more.
+  const double cost2[3] = {1.0, 1.23, 1.3};
+  const double* cost = pair ? cost2 : cost1;
   int best = 256;
   double best_t = 1e300;
   for (int i = 0; i < 3; ++i) {
-    if (pair && cand[i] == 192) continue;  // the two-SM kernel splits B in 64-wide halves
     const double t = static_cast<double>(cdiv(d, cand[i]) * cand[i]) * cost[i];
     if (t < best_t) { best_t = t; best = cand[i]; }
   }
@@ -401,8 +442,8 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
   const int bnd = choose_bn_d(d, true);
   CUtensorMap mH_k, mH_mn;
   if (!encode_map_bf16(&mH_k, H, d, T, d * 2, 64, 128)) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
-  const bool h3d = encode_map_mn3d(&mH_mn, H, d, T, d * 2, bnd / 2);
-  if (!h3d && !encode_map_bf16(&mH_mn, H, d, T, d * 2, 64, 64))
+  bool h3d = false;
+  if (!encode_b_mn_pair(&mH_mn, H, d, T, d * 2, bnd, true, &h3d))
     return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
   const int64_t Vc = pl.Vc;
   for (int64_t j = 0; j < pl.nslabs; ++j) {
@@ -412,10 +453,10 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
     CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
     // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
     // 3-D view may span round_up(w, 64) columns.
-    const bool w3d = encode_map_mn3d(&mW_mn, Wj, d, w, d * 2, bnd / 2);
+    bool w3d = false;
+    const bool wmap = encode_b_mn_pair(&mW_mn, Wj, d, w, d * 2, bnd, true, &w3d);
     const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, T, Vc * 2, 128);
-    if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) ||
-        (!w3d && !encode_map_bf16(&mW_mn, Wj, d, w, d * 2, 64, 64)) ||
+    if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) || !wmap ||
         (!d3d && !encode_map_bf16(&mD_mn, ds, w, T, Vc * 2, 64, 64)) ||
         !encode_map_bf16(&mD_k, ds, w, T, Vc * 2, 64, 128))
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for slab %lld", (long long)j);
@@ -486,7 +527,7 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
     return fail(FKL_ERR_INVALID_ARG, "M, N, Kd must be in [1, 2^30)");
   if (bn != 256 && bn != 192 && bn != 128) return fail(FKL_ERR_INVALID_ARG, "bn must be 256, 192 or 128");
   const bool pair = (accumulate & 4) != 0;
-  if (pair && bn == 192) return fail(FKL_ERR_INVALID_ARG, "the two-SM kernel takes bn 256 or 128");
+
   const int64_t a_inner = a_mn_major ? M : Kd, b_inner = b_mn_major ? N : Kd;
   if (a_inner % 8 != 0 || b_inner % 8 != 0)
     return fail(FKL_ERR_ALIGNMENT, "the contiguous extent of A and B must be a multiple of 8");
@@ -506,10 +547,15 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
   CUtensorMap mA, mB;
   const uint32_t b_tile = pair ? (uint32_t)bn / 2 : (uint32_t)bn;  // B rows / columns per CTA
   const bool a3d = a_mn_major && allow3d && encode_map_mn3d(&mA, A, M, Kd, M * 2, 128);
-  const bool b3d = b_mn_major && allow3d && encode_map_mn3d(&mB, B, N, Kd, N * 2, b_tile);
+  bool b3d = false;
   bool ok = a3d || (a_mn_major ? encode_map_bf16(&mA, A, M, Kd, M * 2, 64, 64) : encode_map_bf16(&mA, A, Kd, M, Kd * 2, 64, 128));
-  ok = ok && (b3d || (b_mn_major ? encode_map_bf16(&mB, B, N, Kd, N * 2, 64, 64)
-                                 : encode_map_bf16(&mB, B, Kd, N, Kd * 2, 64, b_tile)));
+  if (b_mn_major && pair) {
+    ok = ok && encode_b_mn_pair(&mB, B, N, Kd, N * 2, bn, allow3d, &b3d);
+  } else {
+    b3d = b_mn_major && allow3d && encode_map_mn3d(&mB, B, N, Kd, N * 2, b_tile);
+    ok = ok && (b3d || (b_mn_major ? encode_map_bf16(&mB, B, N, Kd, N * 2, 64, 64)
+                                   : encode_map_bf16(&mB, B, Kd, N, Kd * 2, 64, b_tile)));
+  }
   if (!ok) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for A or B");
   GemmShape g = make_shape(M, N, Kd, bn, (int)cdiv(N, bn), &hdr->status, pair ? 256 : 128);
   g.a_box3d = a3d ? 1 : 0;

@@ -27,6 +27,7 @@ cudaError_t launch_gemm2_f32(int bn, bool a_mn, bool b_mn, const CUtensorMap& a,
                              const GemmShape& g, const F32Params& ep, int sms, cudaStream_t st) {
   switch (bn) {
     case 256: return dispatch2<256>(a_mn, b_mn, a, b, g, ep, sms, st);
+    case 192: return dispatch2<192>(a_mn, b_mn, a, b, g, ep, sms, st);
     case 128: return dispatch2<128>(a_mn, b_mn, a, b, g, ep, sms, st);
     default: return cudaErrorInvalidValue;
   }

@@ -23,7 +23,10 @@ namespace fkl {
 
 constexpr int kBM2 = 256;  // rows per CTA pair
 
-__host__ __device__ constexpr int stages2_for(int bn) { return bn == 256 ? 6 : 8; }
+__host__ __device__ constexpr int stages2_for(int bn) { return bn == 256 ? 7 : 8; }
+// An MN-major B half that is not a whole number of 64-element (128-byte) rows uses the
+// 64-byte swizzle: 32-element atoms (a 192-wide tile: 96-wide halves, three atoms).
+__host__ __device__ constexpr bool b_sw64_for(int bn, bool b_mn) { return b_mn && (bn / 2) % 64 != 0; }
 __host__ __device__ constexpr size_t smem2_bytes_for(int bn) {
   return static_cast<size_t>(stages2_for(bn)) * (kBM * kBK * 2 + (bn / 2) * kBK * 2) + 1024 + 512;
 }
@@ -39,7 +42,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t BOX_BYTES = 64 * kBK * 2;
   constexpr uint32_t IDESC = instr_desc_bf16(kBM2, BN, A_MN, B_MN);
-  static_assert(BN == 256 || BN == 128, "two-SM tiles are 256 x 256 or 256 x 128");
+  constexpr bool B_SW64 = b_sw64_for(BN, B_MN);
+  constexpr uint32_t BOX64_BYTES = 32 * kBK * 2;  // one 32 x 64 MN-major box (64-byte swizzle), 4 KB
+  static_assert(BN == 256 || BN == 192 || BN == 128, "two-SM tiles are 256 x {256, 192, 128}");
+  static_assert(!B_SW64 || (BN / 2) % 32 == 0, "64-byte swizzle halves are whole 32-wide atoms");
   static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators must fit in TMEM");
 
   extern __shared__ uint8_t smem_raw[];
@@ -120,6 +126,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (!B_MN) {
               tma_load_2d_pair(sb, &tmB, fb, k0, b_row);
+            } else if (B_SW64) {
+              if (g.b_box3d) {
+                tma_load_3d_pair(sb, &tmB, fb, 0, k0, b_row / 32);
+              } else {
+#pragma unroll
+                for (int j = 0; j < BNH / 32; ++j) tma_load_2d_pair(sb + j * BOX64_BYTES, &tmB, fb, b_row + j * 32, k0);
+              }
             } else if (g.b_box3d) {
               tma_load_3d_pair(sb, &tmB, fb, 0, k0, b_row / 64);
             } else {
@@ -161,8 +174,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kBK / 16; ++k) {
               const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, BOX_BYTES, 1024)
                                        : smem_desc_sw128(sa + k * 32, 16, 1024);
-              const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, BOX_BYTES, 1024)
-                                       : smem_desc_sw128(sb + k * 32, 16, 1024);
+              // MN-major B, 64-byte swizzle: 64-byte rows, 8-row groups 512 B apart, atoms 4 KB
+              // apart, 16 rows = 1 KB per step.
+              const uint64_t bd = !B_MN ? smem_desc_sw128(sb + k * 32, 16, 1024)
+                                  : B_SW64 ? smem_desc(sb + k * 1024, BOX64_BYTES, 512, 4u)
+                                           : smem_desc_sw128(sb + k * 2048, BOX_BYTES, 1024);
               tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
             }
             tc_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs

@@ -118,6 +118,12 @@ bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
 // (64, 64, tile_mn / 64).  Returns false if the map cannot be encoded.
 bool encode_map_mn3d(CUtensorMap* map, const void* base, uint64_t mn_extent, uint64_t k_extent,
                      uint64_t row_stride_bytes, uint32_t tile_mn);
+// The same with 32-element atoms and the 64-byte swizzle (two-SM B halves 96 wide); the
+// 2-D form loads one 32 x 64 box.  mn_extent % 32 == 0 for the 3-D form.
+bool encode_map_mn3d_sw64(CUtensorMap* map, const void* base, uint64_t mn_extent, uint64_t k_extent,
+                          uint64_t row_stride_bytes, uint32_t tile_mn);
+bool encode_map_bf16_sw64(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                          uint64_t row_stride_bytes);
 
 cudaError_t launch_gemm_fwd(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
                             const FwdParams& ep, int grid, cudaStream_t st);

@@ -90,19 +90,22 @@ def test_pair_single_tile(L):
     assert run_gemm(L, 256, 256, 64, False, False, 256, pair=True) < 1e-5
 
 
-@pytest.mark.parametrize("bn", [256, 128])
+@pytest.mark.parametrize("bn", [256, 192, 128])
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
 def test_pair_ragged_all_majors(L, a_mn, b_mn, bn):
     # M = 304: the second 256-row tile has 48 rows, so the odd CTA's half is all padding
     assert run_gemm(L, 304, 520, 200, a_mn, b_mn, bn, pair=True) < 1e-5
 
 
+@pytest.mark.parametrize("bn", [256, 192])
 @pytest.mark.parametrize("force2d", [False, True])
-def test_pair_mn_major_box_paths(L, force2d):
-    assert run_gemm(L, 320, 1344, 200, True, True, 256, force2d=force2d, pair=True) < 1e-5
+def test_pair_mn_major_box_paths(L, force2d, bn):
+    # bn = 192: the 96-wide B halves use the 64-byte swizzle (three 32-wide atoms)
+    assert run_gemm(L, 320, 1344, 200, True, True, bn, force2d=force2d, pair=True) < 1e-5
 
 
-@pytest.mark.parametrize("a_mn,b_mn,bn", [(False, False, 256), (True, True, 256), (False, True, 128)])
+@pytest.mark.parametrize("a_mn,b_mn,bn", [(False, False, 256), (True, True, 256), (False, True, 128),
+                                           (True, True, 192), (False, True, 192)])
 def test_pair_many_waves(L, a_mn, b_mn, bn):
     assert run_gemm(L, 2048, 3072, 1024, a_mn, b_mn, bn, seed=3, pair=True) < 2e-5
 
