@@ -461,7 +461,7 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
         !encode_map_bf16(&mD_k, ds, w, T, Vc * 2, 64, 128))
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for slab %lld", (long long)j);
 
-    // dS[:, slab] = dscale * (q - ptilde), recomputing S = H W_slab^T.
+    // dS[:, slab] = g tau w_t (q - ptilde), recomputing S = H W_slab^T.
     const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(w, kVocabTile);
     const GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
     DsParams dp;

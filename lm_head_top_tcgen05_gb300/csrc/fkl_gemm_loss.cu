@@ -1,5 +1,5 @@
-// Instantiations of the persistent tcgen05 GEMM with the loss epilogues: the forward
-// projection + online logsumexp + top-K gather, and the backward recompute + dS.
+// One-SM instantiation of the forward projection + online logsumexp + top-K gather, used by
+// the allocation-free forward (the loss itself runs on the two-SM kernel, fkl_gemm2.cu).
 #include "fkl_gemm.cuh"
 
 namespace fkl {
@@ -7,11 +7,6 @@ namespace fkl {
 cudaError_t launch_gemm_fwd(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
                             const FwdParams& ep, int grid, cudaStream_t st) {
   return launch_gemm_t<kVocabTile, false, false, EpiFwd>(a, b, g, ep, grid, st);
-}
-
-cudaError_t launch_gemm_ds(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
-                           const DsParams& ep, int grid, cudaStream_t st) {
-  return launch_gemm_t<kVocabTile, false, false, EpiDs>(a, b, g, ep, grid, st);
 }
 
 }  // namespace fkl

@@ -127,8 +127,6 @@ bool encode_map_bf16_sw64(CUtensorMap* map, const void* base, uint64_t inner, ui
 
 cudaError_t launch_gemm_fwd(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
                             const FwdParams& ep, int grid, cudaStream_t st);
-cudaError_t launch_gemm_ds(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
-                           const DsParams& ep, int grid, cudaStream_t st);
 // Two-SM (CTA pair) versions: 256-row tiles; B maps load BN/2 rows (or columns) per CTA;
 // the grid is sized from the clusters that fit on the device (sms = SM count).
 cudaError_t launch_gemm2_fwd(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
