@@ -170,8 +170,8 @@ KERNEL_NAMES = {0: "gemm2_kernel<256,0,0,EpiFwd> (two-SM)", 1: "gemm2_kernel<256
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "a00aa85a678b7959"
-TRAFFIC_BYTES = {1: 2.904e9, 2: 2.545e9, 3: 2.690e9}
+TRAFFIC_SOURCES_SHA = "c2b1d065ffc67ae9"
+TRAFFIC_BYTES = {1: 3.068e9, 2: 3.097e9, 3: 3.126e9}
 TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
 
 
