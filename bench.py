@@ -166,6 +166,9 @@ def max_over_ranks(value: float, device=None) -> float:
 KIND_NAMES = {0: "forward projection + logsumexp/top-K", 1: "dS recompute", 2: "dW", 3: "dH"}
 KERNEL_NAMES = {0: "gemm2_kernel<256,0,0,EpiFwd> (two-SM)", 1: "gemm2_kernel<256,0,0,EpiDs> (two-SM)",
                 2: "gemm2_kernel<256,1,1,EpiF32> (two-SM, dW)", 3: "gemm2_kernel<256,0,1,EpiF32> (two-SM, dH)"}
+# Launches per step outside the GEMM trace: forward prep, 3 token-weight kernels, 2 combine;
+# backward prep, 3 token-weight kernels, gradient scale, poison check.
+UNTRACED_LAUNCHES_PER_STEP = 12
 
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
@@ -416,7 +419,8 @@ def main():
     tflops = world * w.flops_fwd_bwd * args.steps / elapsed / 1e12
     sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     burst = float(peaks["bf16_tflops"])
-    launches_per_step = 4 + 3 + 3 * nslabs  # forward: prep, GEMM, 2 combine; backward: prep, scalars, poison, 3 per slab
+    traced = sum(v["launches"] for v in kernels.values())
+    launches_per_step = UNTRACED_LAUNCHES_PER_STEP + traced / args.steps
     clk = clocks.summary()
     dom = max(kernels, key=lambda k: kernels[k]["ms_total"])  # largest share of the step
     out = {
@@ -442,7 +446,7 @@ def main():
         "kernels": {KIND_NAMES[k]: {kk: round(vv, 4) if isinstance(vv, float) else vv for kk, vv in v.items()}
                     for k, v in kernels.items()},
         "clocks": clk,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
     }
     if e2e is not None:
         out["e2e"] = e2e
