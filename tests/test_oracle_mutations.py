@@ -131,3 +131,85 @@ def test_loss_normaliser_mistake_is_caught(monkeypatch):
     import oracle
     monkeypatch.setattr(oracle, "forward", forward_over_all_tokens)
     assert failing_pins() >= 1
+
+
+# ---- the other divergences (oracle/divergences.py) against their own pins
+
+import oracle.divergences as dvm  # noqa: E402
+from tests import test_oracle_divergences as dpins  # noqa: E402
+
+DIV_PIN_CALLS = [
+    lambda: dpins.test_jsd_half_is_scipy_jensen_shannon(1.0),
+    lambda: dpins.test_generalised_jsd_against_relative_entropy(0.35),
+    lambda: dpins.test_skew_kl_against_relative_entropy(0.1),
+    lambda: dpins.test_skew_reverse_kl_against_relative_entropy(0.1),
+    dpins.test_total_variation_brute_force_over_events,
+    dpins.test_skew_kl_zero_is_the_default_kl_loss,
+] + [(lambda k=k, a=a: dpins.test_gradients_finite_differences(k, a)) for k, a in dpins.PARAMS] + [
+    (lambda k=k, a=a: dpins.test_repeated_ids_add_their_probabilities(k, a)) for k, a in dpins.PARAMS]
+
+
+def failing_div_pins():
+    failed = 0
+    for call in DIV_PIN_CALLS:
+        try:
+            with np.errstate(all="ignore"):
+                call()
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            failed += 1
+    return failed
+
+
+orig_div_rows = dvm.divergence_rows
+orig_gamma = dvm.gamma
+orig_dense_block = dvm._dense_block
+
+
+def div_jsd_mixture_swapped(p, q, kind, param):
+    return orig_div_rows(p, q, kind, 1.0 - param if kind == "jsd" else param)
+
+
+def div_tv_no_half(p, q, kind, param):
+    return orig_div_rows(p, q, kind, param) * (2.0 if kind == "tv" else 1.0)
+
+
+def div_skew_rkl_as_skew_kl(p, q, kind, param):
+    return orig_div_rows(p, q, "skew_kl" if kind == "skew_rkl" else kind, min(param, 0.99))
+
+
+def gamma_skew_rkl_drops_terms(p, q, kind, param):
+    g = orig_gamma(p, q, kind, param)
+    if kind == "skew_rkl":
+        m = param * q + (1 - param) * p
+        g = g - 1.0 + param * q / m
+    return g
+
+
+def gamma_jsd_drops_weight(p, q, kind, param):
+    g = orig_gamma(p, q, kind, param)
+    return g / (1.0 - param) if kind == "jsd" else g
+
+
+def dense_block_assigns_repeats(s_blk, idx_blk, p_blk, tau):
+    q, pt, lse = orig_dense_block(s_blk, idx_blk, p_blk, tau)
+    pt = np.zeros_like(q)
+    pt[np.arange(q.shape[0])[:, None], idx_blk] = p_blk
+    return q, pt, lse
+
+
+DIV_MUTATIONS = {
+    "divergence_rows": [div_jsd_mixture_swapped, div_tv_no_half, div_skew_rkl_as_skew_kl],
+    "gamma": [gamma_skew_rkl_drops_terms, gamma_jsd_drops_weight],
+    "_dense_block": [dense_block_assigns_repeats],
+}
+
+
+def test_unmutated_divergence_oracle_passes_every_pin():
+    assert failing_div_pins() == 0
+
+
+@pytest.mark.parametrize("target,mutant", [(t, m) for t, ms in DIV_MUTATIONS.items() for m in ms],
+                         ids=lambda x: getattr(x, "__name__", x))
+def test_planted_divergence_mistake_is_caught(monkeypatch, target, mutant):
+    monkeypatch.setattr(dvm, target, mutant)
+    assert failing_div_pins() > 0
