@@ -86,15 +86,43 @@ typedef enum fkl_status {
  * accumulate     fkl_backward_ex: FKL_ACCUMULATE_DH and/or FKL_ACCUMULATE_DW add the gradient
  *                into dH / dW (gradient accumulation over micro-batches) instead of
  *                overwriting them.  Ignored by the forward.
+ * divergence     The divergence D_t in place of KL_t (the post's closing section says the
+ *                paper also compares loss functions without naming them).  With p the
+ *                teacher's K-slot softmax added onto the vocabulary at its ids (zero at
+ *                every other id; a repeated id carries the sum of its slots) and q_t the
+ *                student's full softmax of s_t / tau:
+ *                  FKL_DIV_KL (0)        KL(p || q), the loss above (default; a repeated id
+ *                                        counts once per slot, as in KL_t's slot sum)
+ *                  FKL_DIV_JSD (1)       b KL(p || m) + (1 - b) KL(q || m), m = b p + (1 - b) q,
+ *                                        0 < b < 1 (b = 1/2: Jensen-Shannon)
+ *                  FKL_DIV_SKEW_KL (2)   KL(p || a p + (1 - a) q), 0 <= a < 1
+ *                  FKL_DIV_SKEW_RKL (3)  KL(q || a q + (1 - a) p), 0 < a <= 1
+ *                  FKL_DIV_TV (4)        1/2 sum_v |p - q| (sign(0) = 0 in its gradient)
+ *                all summed over the whole vocabulary, and L = tau^2 sum_t w_t D_t with the
+ *                token weights w_t of `normalization`.  Each is finite where p is zero, so
+ *                the K cached slots suffice: D_t = sum over the row's ids of a term in
+ *                (p, q) plus a constant times the student mass outside them.
+ * div_param      b for FKL_DIV_JSD, a for FKL_DIV_SKEW_KL / FKL_DIV_SKEW_RKL; ignored
+ *                otherwise.
+ * student_topk_logits
+ *                device float [T, K] or NULL.  fkl_forward_ex writes s_{t, id_tk}, the
+ *                student's logit (fp32, before 1/tau) at each cached slot, when it is not
+ *                NULL.  fkl_backward_ex reads it for every divergence but FKL_DIV_KL (the
+ *                gradient needs q at the ids before the vocabulary sweep), so it must then
+ *                hold the forward's values for the same inputs; it is ignored for KL.
  */
 enum { FKL_NORM_TOKENS = 0, FKL_NORM_SEQUENCES = 1 };
 enum { FKL_ACCUMULATE_DH = 1, FKL_ACCUMULATE_DW = 2 };
+enum { FKL_DIV_KL = 0, FKL_DIV_JSD = 1, FKL_DIV_SKEW_KL = 2, FKL_DIV_SKEW_RKL = 3, FKL_DIV_TV = 4 };
 typedef struct fkl_options {
   int32_t normalization;
   int32_t num_seqs;
   const int32_t* seq_ids;
   int32_t accumulate;
+  int32_t divergence;
+  float div_param;
   int32_t reserved;  /* must be 0 */
+  float* student_topk_logits;
 } fkl_options;
 
 /*

@@ -10,7 +10,11 @@ memory and streams) into that ABI.
     loss = fused_kl(H, W, topk_idx, topk_logits, mask=None, tau=1.0, chunk=2048)
     loss.backward()          # gradients for H and W
 
-or the explicit calls ``forward`` / ``backward`` with a reusable ``Workspace``.
+or the explicit calls ``forward`` / ``backward`` with a reusable ``Workspace``.  Other
+divergences than KL(teacher || student) over the same top-K support: ``divergence="jsd"``
+(``div_param`` = b, default 0.5), ``"skew_kl"`` / ``"skew_rkl"`` (``div_param`` = a, default
+0.1) and ``"tv"``; their backward needs the student logits at the cached ids that the
+forward returns in ``student_topk_logits`` (``fused_kl`` keeps them itself).
 """
 from __future__ import annotations
 
@@ -19,8 +23,10 @@ from typing import Optional, Tuple
 
 import torch
 
-from ._lib import (FKL_ACCUMULATE_DH, FKL_ACCUMULATE_DW, FKL_NORM_SEQUENCES, FKL_NORM_TOKENS,  # noqa: F401
-                   FKL_OK, STATUS, FklError, FklOptions, check, lib)
+from ._lib import (DIVERGENCES, FKL_ACCUMULATE_DH, FKL_ACCUMULATE_DW, FKL_NORM_SEQUENCES,  # noqa: F401
+                   FKL_NORM_TOKENS, FKL_OK, STATUS, FklError, FklOptions, check, lib)
+
+_DEFAULT_PARAM = {"kl": 0.0, "jsd": 0.5, "skew_kl": 0.1, "skew_rkl": 0.1, "tv": 0.0}
 
 __all__ = ["workspace_size", "Workspace", "forward", "backward", "read_status", "fused_kl",
            "FusedKL", "FklError", "STATUS", "teacher_topk"]
@@ -94,10 +100,28 @@ def _check_inputs(H, W, topk_idx, topk_logits, mask):
     return mask
 
 
-def _options(T: int, seq_ids: Optional[torch.Tensor], num_seqs: Optional[int], accumulate: int = 0):
-    """fkl_options for the sequence-mean normaliser (seq_ids given) and accumulation flags."""
+def _divergence(divergence: str, div_param: Optional[float]):
+    if divergence not in DIVERGENCES:
+        raise ValueError(f"divergence must be one of {sorted(DIVERGENCES)}")
+    return DIVERGENCES[divergence], float(_DEFAULT_PARAM[divergence] if div_param is None else div_param)
+
+
+def _student_buf(t: Optional[torch.Tensor], T: int, K: int, device) -> Optional[torch.Tensor]:
+    if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (T, K) or not t.is_contiguous()
+                          or t.device != device):
+        raise ValueError(f"student_topk_logits must be a contiguous float32 [{T}, {K}] tensor on {device}")
+    return t
+
+
+def _options(T: int, seq_ids: Optional[torch.Tensor], num_seqs: Optional[int], accumulate: int = 0,
+             divergence: str = "kl", div_param: Optional[float] = None,
+             student_topk_logits: Optional[torch.Tensor] = None):
+    """fkl_options: sequence-mean normaliser (seq_ids given), accumulation flags, divergence."""
     o = FklOptions()
     o.accumulate = accumulate
+    o.divergence, o.div_param = _divergence(divergence, div_param)
+    if student_topk_logits is not None:
+        o.student_topk_logits = student_topk_logits.data_ptr()
     if seq_ids is not None:
         if seq_ids.dtype != torch.int32 or tuple(seq_ids.shape) != (T,) or not seq_ids.is_cuda:
             raise ValueError("seq_ids must be a CUDA int32 tensor of shape [T]")
@@ -111,18 +135,22 @@ def _options(T: int, seq_ids: Optional[torch.Tensor], num_seqs: Optional[int], a
 def forward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
             mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048,
             workspace: Optional[Workspace] = None, seq_ids: Optional[torch.Tensor] = None,
-            num_seqs: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+            num_seqs: Optional[int] = None, divergence: str = "kl", div_param: Optional[float] = None,
+            student_topk_logits: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Loss (0-dim float32) and lse [T] (float32) on H's device and current stream.
 
     With ``seq_ids`` (int32 [T], the packed sequence of each token) the loss is the mean
-    over sequences of each sequence's token mean; otherwise the mean over valid tokens."""
+    over sequences of each sequence's token mean; otherwise the mean over valid tokens.
+    ``student_topk_logits`` (float32 [T, K], optional) receives the student's logit at each
+    cached slot; the backward of every divergence but "kl" needs it."""
     mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
     T, d = H.shape
     V, K = W.shape[0], topk_idx.shape[1]
+    student_topk_logits = _student_buf(student_topk_logits, T, K, H.device)
     ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk), H.device)
     loss = torch.empty((), dtype=torch.float32, device=H.device)
     lse = torch.empty(T, dtype=torch.float32, device=H.device)
-    opts, seq_ids = _options(T, seq_ids, num_seqs)
+    opts, seq_ids = _options(T, seq_ids, num_seqs, 0, divergence, div_param, student_topk_logits)
     st = lib().fkl_forward_ex(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask), T, d, V, K,
                               float(tau), chunk, ctypes.byref(opts), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
                               _stream(H.device))
@@ -134,13 +162,17 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
              mask: Optional[torch.Tensor], lse: torch.Tensor, grad_loss: Optional[torch.Tensor] = None,
              tau: float = 1.0, chunk: int = 2048, workspace: Optional[Workspace] = None,
              out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None, seq_ids: Optional[torch.Tensor] = None,
-             num_seqs: Optional[int] = None, accumulate: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+             num_seqs: Optional[int] = None, accumulate: bool = False, divergence: str = "kl",
+             div_param: Optional[float] = None,
+             student_topk_logits: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """dH [T, d] and dW [V, d] (float32), the gradient of g * loss (g = grad_loss or 1).
 
-    ``accumulate=True`` adds into the tensors given in ``out`` (gradient accumulation)."""
+    ``accumulate=True`` adds into the tensors given in ``out`` (gradient accumulation).  For
+    every divergence but "kl", ``student_topk_logits`` is the forward's output of that name."""
     mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
     T, d = H.shape
     V, K = W.shape[0], topk_idx.shape[1]
+    student_topk_logits = _student_buf(student_topk_logits, T, K, H.device)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (T,) or not lse.is_cuda:
         raise ValueError("lse must be a CUDA float32 tensor of shape [T]")
     if grad_loss is not None:
@@ -157,7 +189,7 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
             if g.dtype != torch.float32 or tuple(g.shape) != shape or not g.is_contiguous() or g.device != H.device:
                 raise ValueError(f"out gradients must be contiguous float32 {shape} on {H.device}")
     flags = (FKL_ACCUMULATE_DH | FKL_ACCUMULATE_DW) if accumulate else 0
-    opts, seq_ids = _options(T, seq_ids, num_seqs, flags)
+    opts, seq_ids = _options(T, seq_ids, num_seqs, flags, divergence, div_param, student_topk_logits)
     st = lib().fkl_backward_ex(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask),
                                _ptr(lse.contiguous()), _ptr(grad_loss), T, d, V, K, float(tau), chunk,
                                ctypes.byref(opts), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(H.device))
@@ -173,30 +205,39 @@ def read_status(workspace: Optional[Workspace] = None, device=None) -> int:
 
 
 class FusedKL(torch.autograd.Function):
-    """Autograd wrapper: forward saves lse; backward recomputes the projection chunk by chunk."""
+    """Autograd wrapper: forward saves lse (and, for divergences other than KL, the student
+    logits at the cached ids); backward recomputes the projection chunk by chunk."""
 
     @staticmethod
-    def forward(ctx, H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=None, num_seqs=None):
-        loss, lse = forward(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=seq_ids, num_seqs=num_seqs)
+    def forward(ctx, H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=None, num_seqs=None,
+                divergence="kl", div_param=None):
+        s_ids = None
+        if divergence != "kl":
+            s_ids = torch.empty(topk_idx.shape, dtype=torch.float32, device=H.device)
+        loss, lse = forward(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=seq_ids, num_seqs=num_seqs,
+                            divergence=divergence, div_param=div_param, student_topk_logits=s_ids)
         ctx.save_for_backward(H, W, topk_idx, topk_logits, lse)
         ctx.mask, ctx.seq_ids, ctx.num_seqs = mask, seq_ids, num_seqs
-        ctx.tau, ctx.chunk = tau, chunk
+        ctx.tau, ctx.chunk, ctx.divergence, ctx.div_param, ctx.s_ids = tau, chunk, divergence, div_param, s_ids
         return loss
 
     @staticmethod
     def backward(ctx, grad):
         H, W, topk_idx, topk_logits, lse = ctx.saved_tensors
         dH, dW = backward(H, W, topk_idx, topk_logits, ctx.mask, lse, grad, ctx.tau, ctx.chunk,
-                          seq_ids=ctx.seq_ids, num_seqs=ctx.num_seqs)
-        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None, None, None, None
+                          seq_ids=ctx.seq_ids, num_seqs=ctx.num_seqs, divergence=ctx.divergence,
+                          div_param=ctx.div_param, student_topk_logits=ctx.s_ids)
+        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None, None, None, None, None, None
 
 
 def fused_kl(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
              mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048,
-             seq_ids: Optional[torch.Tensor] = None, num_seqs: Optional[int] = None) -> torch.Tensor:
+             seq_ids: Optional[torch.Tensor] = None, num_seqs: Optional[int] = None,
+             divergence: str = "kl", div_param: Optional[float] = None) -> torch.Tensor:
     """tau^2 * KL(teacher top-K || student) averaged over valid tokens (or, with seq_ids, over
-    packed sequences of their token means); differentiable in H and W."""
-    return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids, num_seqs)
+    packed sequences of their token means); differentiable in H and W.  ``divergence`` picks
+    another divergence over the same support ("jsd", "skew_kl", "skew_rkl", "tv")."""
+    return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids, num_seqs, divergence, div_param)
 
 
 def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int = 100,

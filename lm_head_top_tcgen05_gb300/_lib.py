@@ -29,11 +29,15 @@ class FklOptions(ctypes.Structure):
     """fkl_options of include/fkl.h."""
 
     _fields_ = [("normalization", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
-                ("seq_ids", ctypes.c_void_p), ("accumulate", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("seq_ids", ctypes.c_void_p), ("accumulate", ctypes.c_int32), ("divergence", ctypes.c_int32),
+                ("div_param", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("student_topk_logits", ctypes.c_void_p)]
 
 
 FKL_NORM_TOKENS, FKL_NORM_SEQUENCES = 0, 1
 FKL_ACCUMULATE_DH, FKL_ACCUMULATE_DW = 1, 2
+# fkl_options.divergence, by the names the binding accepts
+DIVERGENCES = {"kl": 0, "jsd": 1, "skew_kl": 2, "skew_rkl": 3, "tv": 4}
 
 # Every symbol declared in include/*.h, with (restype, argtypes).
 _P = ctypes.c_void_p

@@ -73,6 +73,9 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   p->off_bsum = off;  off = align_up(off + nbb * 8, 256);
   p->off_bcnt = off;  off = align_up(off + nbb * 4, 256);
   p->off_ds = off;    off = align_up(off + static_cast<size_t>(T) * p->Vc * 2, 256);
+  p->off_slot = off;  off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
+  p->off_sg = off;    off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
+  p->off_arow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
   p->total = off;
   return true;
 }
@@ -256,6 +259,22 @@ static fkl_status check_options(const fkl_options* o, int64_t T) {
   if (o == nullptr) return FKL_OK;
   if (o->reserved != 0) return fail(FKL_ERR_INVALID_ARG, "fkl_options.reserved must be 0");
   if (o->accumulate < 0 || o->accumulate > 3) return fail(FKL_ERR_INVALID_ARG, "bad fkl_options.accumulate");
+  const float c = o->div_param;
+  switch (o->divergence) {
+    case FKL_DIV_KL: case FKL_DIV_TV: break;
+    case FKL_DIV_JSD:
+      if (!(c > 0.f && c < 1.f)) return fail(FKL_ERR_INVALID_ARG, "FKL_DIV_JSD needs 0 < div_param < 1");
+      break;
+    case FKL_DIV_SKEW_KL:
+      if (!(c >= 0.f && c < 1.f)) return fail(FKL_ERR_INVALID_ARG, "FKL_DIV_SKEW_KL needs 0 <= div_param < 1");
+      break;
+    case FKL_DIV_SKEW_RKL:
+      if (!(c > 0.f && c <= 1.f)) return fail(FKL_ERR_INVALID_ARG, "FKL_DIV_SKEW_RKL needs 0 < div_param <= 1");
+      break;
+    default: return fail(FKL_ERR_INVALID_ARG, "bad fkl_options.divergence");
+  }
+  if (!aligned(o->student_topk_logits, 4))
+    return fail(FKL_ERR_ALIGNMENT, "fkl_options.student_topk_logits must be 4-byte aligned");
   if (o->normalization == FKL_NORM_TOKENS) return FKL_OK;
   if (o->normalization != FKL_NORM_SEQUENCES) return fail(FKL_ERR_INVALID_ARG, "bad fkl_options.normalization");
   if (o->num_seqs < 1 || o->num_seqs > (T > 0 ? T : 1))
@@ -364,8 +383,15 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
   int* bcnt = reinterpret_cast<int*>(ws + pl.off_bcnt);
   const float* wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
 
+  const DivSpec dv{opts ? opts->divergence : FKL_DIV_KL, opts ? opts->div_param : 0.f};
+  float* user_s = opts ? opts->student_topk_logits : nullptr;
+  const bool record_s = dv.kind != FKL_DIV_KL || user_s != nullptr;
+  int* slot = reinterpret_cast<int*>(ws + pl.off_slot);
+  float* sg = reinterpret_cast<float*>(ws + pl.off_sg);
+
   if (T > 0) {
-    if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st)) != cudaSuccess)
+    if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, slot, crow, &hdr->status, st)) !=
+        cudaSuccess)
       return cuda_fail(e, "prep kernel");
     if ((e = run_weights(opts, mask, T, ws, pl, hdr, st)) != cudaSuccess) return cuda_fail(e, "weights kernels");
     // Two-SM tiles: each CTA of a pair loads 128 rows of H and 128 rows of the W tile.
@@ -378,13 +404,20 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
     FwdParams fp;
     fp.pairs = pairs;
     fp.part = part;
+    fp.sg = record_s ? sg : nullptr;
     fp.T = (int)T; fp.K = (int)K; fp.V = (int)V; fp.nsplit = nsplit;
     fp.scale2 = 1.4426950408889634f / tau;
     trace_launch_begin(st);
     if ((e = launch_gemm2_fwd(mH, mW, g, fp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "forward GEMM");
     trace_launch_end(st, 0, 2.0 * T * V * d);
-    if ((e = launch_combine(part, nsplit, crow, wrow, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st)) != cudaSuccess)
-      return cuda_fail(e, "combine kernels");
+    if ((e = launch_combine_rows(part, nsplit, crow, wrow, T, tau, lse, bsum, bcnt, pl.nb, st)) != cudaSuccess)
+      return cuda_fail(e, "combine kernel");
+    if (record_s &&
+        (e = launch_div_rows(dv, pairs, slot, sg, lse, wrow, T, (int)K, tau, user_s, bsum, bcnt, pl.nb, st)) !=
+            cudaSuccess)
+      return cuda_fail(e, "divergence kernel");
+    if ((e = launch_combine_final(bsum, bcnt, T, pl.nb, tau, hdr, loss, st)) != cudaSuccess)
+      return cuda_fail(e, "combine kernel");
   } else {
     if ((e = launch_combine(part, 1, crow, wrow, 0, tau, lse, bsum, bcnt, 0, hdr, loss, st)) != cudaSuccess)
       return cuda_fail(e, "combine kernels");
@@ -414,6 +447,9 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
   const int accum = opts ? opts->accumulate : 0;
   if (dW == nullptr || (T > 0 && (dH == nullptr || lse == nullptr)))
     return fail(FKL_ERR_INVALID_ARG, "dH, dW and lse must not be NULL");
+  const DivSpec dv{opts ? opts->divergence : FKL_DIV_KL, opts ? opts->div_param : 0.f};
+  if (dv.kind != FKL_DIV_KL && T > 0 && opts->student_topk_logits == nullptr)
+    return fail(FKL_ERR_INVALID_ARG, "this divergence's backward needs fkl_options.student_topk_logits");
   if (!aligned(dW, 16) || (dH && !aligned(dH, 16))) return fail(FKL_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
   if ((lse && !aligned(lse, 4)) || (grad_loss && !aligned(grad_loss, 4)))
     return fail(FKL_ERR_ALIGNMENT, "lse and grad_loss must be 4-byte aligned");
@@ -433,10 +469,16 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
   float* crow = reinterpret_cast<float*>(ws + pl.off_crow);
   uint16_t* ds = reinterpret_cast<uint16_t*>(ws + pl.off_ds);
 
-  if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st)) != cudaSuccess)
+  int* slot = reinterpret_cast<int*>(ws + pl.off_slot);
+  float* arow = reinterpret_cast<float*>(ws + pl.off_arow);
+  if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, slot, crow, &hdr->status, st)) !=
+      cudaSuccess)
     return cuda_fail(e, "prep kernel");
   if ((e = run_weights(opts, mask, T, ws, pl, hdr, st)) != cudaSuccess) return cuda_fail(e, "weights kernels");
   if ((e = launch_grad_scale(grad_loss, tau, hdr, st)) != cudaSuccess) return cuda_fail(e, "scale kernel");
+  if (dv.kind != FKL_DIV_KL &&
+      (e = launch_div_coef(dv, pairs, slot, opts->student_topk_logits, lse, T, (int)K, tau, arow, st)) != cudaSuccess)
+    return cuda_fail(e, "divergence kernel");
 
   // All three products use two-SM tiles (256 rows per CTA pair, B split between the CTAs).
   const int bnd = choose_bn_d(d, true);
@@ -466,6 +508,7 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
     const GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
     DsParams dp;
     dp.pairs = pairs; dp.lse = lse; dp.wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
+    dp.arow = dv.kind != FKL_DIV_KL ? arow : nullptr;
     dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
     dp.T = (int)T; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
     dp.scale2 = 1.4426950408889634f / tau;

@@ -124,7 +124,9 @@ struct EpiFwd {
         if (col0 + j >= p.V) v[j] = -INFINITY;
     }
     while (cur.nid < col0 + 32) {  // teacher ids inside this 32-column chunk (rare)
-      g = fmaf(cur.pn, pick(v, cur.nid - col0), g);
+      const float sv = pick(v, cur.nid - col0);
+      g = fmaf(cur.pn, sv, g);
+      if (p.sg != nullptr) p.sg[static_cast<size_t>(t) * p.K + cur.kp] = sv;
       cur.next();
     }
     float c0 = fmaxf(v[0], v[1]), c1 = fmaxf(v[2], v[3]);
@@ -173,14 +175,15 @@ struct EpiFwd {
 };
 
 // ------------------------------------------------------------------ backward dS epilogue
-// dS[t, v] = g tau w_t (exp2(s * log2(e)/tau - lse_t * log2(e)) - ptilde[t, v]) (w_t = 0 for
-// masked rows), rounded to bf16 and written to the slab buffer.
+// dS[t, v] = g tau w_t (a_t exp2(s * log2(e)/tau - lse_t * log2(e)) - r[t, v]) (w_t = 0 for
+// masked rows), rounded to bf16 and written to the slab buffer.  r is the pairs' second
+// field added at their ids: for KL, a_t = 1 and r = ptilde.
 struct EpiDs {
   using Params = DsParams;
   const Params& p;
   int t;
   bool row_ok;
-  float lse2, f;
+  float lse2, f, a;
   uint16_t* dst;
   TopkCursor cur;
 
@@ -192,11 +195,13 @@ struct EpiDs {
     if (row_ok) {
       lse2 = p.lse[t] * 1.4426950408889634f;
       f = p.hdr->gtau * p.wrow[t];
+      a = p.arow != nullptr ? p.arow[t] : 1.f;
       dst = p.ds + static_cast<size_t>(t) * p.ld_ds;
       cur.seek(p.pairs + static_cast<size_t>(t) * p.K, p.K, p.v0 + n_begin * kVocabTile);
     } else {
       lse2 = 0.f;
       f = 0.f;
+      a = 1.f;
       dst = nullptr;
       cur.none();
     }
@@ -205,8 +210,8 @@ struct EpiDs {
   __device__ __forceinline__ void chunk(float (&v)[32], int cl0) {
     const int cg0 = p.v0 + cl0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = ex2_approx(fmaf(v[j], p.scale2, -lse2));
-    while (cur.nid < cg0 + 32) {  // subtract p at the teacher ids in this chunk (rare)
+    for (int j = 0; j < 32; ++j) v[j] = a * ex2_approx(fmaf(v[j], p.scale2, -lse2));
+    while (cur.nid < cg0 + 32) {  // subtract r at the teacher ids in this chunk (rare)
       const int jt = cur.nid - cg0;
 #pragma unroll
       for (int j = 0; j < 32; ++j)

@@ -34,7 +34,17 @@ struct Plan {
   int64_t Vc;      // vocabulary columns per backward slab (multiple of kVocabTile)
   int64_t nslabs;  // number of backward slabs
   int64_t nb;      // row blocks of the combine step (256 rows each)
-  size_t off_pairs, off_crow, off_wrow, off_scnt, off_part, off_bsum, off_bcnt, off_ds, total;
+  size_t off_pairs, off_crow, off_wrow, off_scnt, off_part, off_bsum, off_bcnt, off_ds;
+  size_t off_slot;  // int32 [T][K]: original slot of each sorted pair
+  size_t off_sg;    // fp32 [T][K]: student logit at each sorted pair (other divergences)
+  size_t off_arow;  // fp32 [T]: per-row factor a_t of dS (other divergences)
+  size_t total;
+};
+
+// Divergence of the loss (the FKL_DIV_* values of fkl.h) and its parameter.
+struct DivSpec {
+  int kind;
+  float param;
 };
 
 // Sets the message that fkl_last_error() returns on the calling thread.
@@ -52,10 +62,28 @@ int plan_splits(int m_tiles, int n_tiles, int sms);
 
 // ---------------------------------------------------------------- small kernels
 cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t T, int K, int V, float tau,
-                        int2* pairs, float* crow, uint32_t* status, cudaStream_t st);
+                        int2* pairs, int* slot, float* crow, uint32_t* status, cudaStream_t st);
+// Forward, after the combine has written lse: for a divergence other than KL, D_t of every
+// row from the sorted pairs and the student logits sg at them, and the per-block sums of
+// w_t D_t (overwriting the combine's KL sums); then, if user_s is not NULL, the student
+// logits scattered to the caller's slot order.  Call launch_combine_final afterwards.
+cudaError_t launch_div_rows(DivSpec dv, const int2* pairs, const int* slot, const float* sg,
+                            const float* lse, const float* wrow, int64_t T, int K, float tau,
+                            float* user_s, double* bsum, int* bcnt, int64_t nb, cudaStream_t st);
+// Backward, after prep: a_t into arow and, in place of p in the pairs, the per-id term r so
+// that dS = g tau w_t (a_t q - r) reproduces the divergence's gradient.
+cudaError_t launch_div_coef(DivSpec dv, int2* pairs, const int* slot, const float* user_s,
+                            const float* lse, int64_t T, int K, float tau, float* arow, cudaStream_t st);
 // Token weights w_t into wrow[T] (and N, S into the header); seq may be NULL (one sequence).
 cudaError_t launch_weights(const uint8_t* mask, const int32_t* seq, int num_seqs, int per_sequence,
                            int64_t T, int* cnt, WsHeader* hdr, float* wrow, cudaStream_t st);
+// lse_t and the per-block sums of w_t KL_t (launch_combine_rows), then the loss from the
+// block sums (launch_combine_final); launch_combine runs both.
+cudaError_t launch_combine_rows(const float* part, int nsplit, const float* crow, const float* wrow,
+                                int64_t T, float tau, float* lse, double* bsum, int* bcnt, int64_t nb,
+                                cudaStream_t st);
+cudaError_t launch_combine_final(const double* bsum, const int* bcnt, int64_t T, int64_t nb, float tau,
+                                 WsHeader* hdr, float* loss, cudaStream_t st);
 cudaError_t launch_combine(const float* part, int nsplit, const float* crow, const float* wrow,
                            int64_t T, float tau, float* lse, double* bsum, int* bcnt, int64_t nb,
                            WsHeader* hdr, float* loss, cudaStream_t st);
@@ -86,15 +114,18 @@ GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint3
 struct FwdParams {
   const int2* pairs;  // [T][K] (id, p) sorted by id
   float* part;        // [3][nsplit][T]: running max (base 2), sum, gather
+  float* sg;          // [T][K] student logit at each sorted pair, or NULL (not recorded)
   int T, K, V, nsplit;
   float scale2;       // log2(e) / tau
 };
 
-// Backward recompute: dS = g tau w_t (q - ptilde) for one vocabulary slab, bf16.
+// Backward recompute: dS = g tau w_t (a_t q - r) for one vocabulary slab, bf16, with r the
+// pairs' second field added at their ids (KL: a_t = 1, r = p, i.e. q - ptilde).
 struct DsParams {
   const int2* pairs;
   const float* lse;
   const float* wrow;  // w_t (0 for masked tokens)
+  const float* arow;  // a_t, or NULL for a_t = 1
   const WsHeader* hdr;
   uint16_t* ds;       // [T][ld_ds]
   int64_t ld_ds;

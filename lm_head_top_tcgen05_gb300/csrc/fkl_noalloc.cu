@@ -106,7 +106,7 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
       return noalloc_fail(FKL_ERR_CUDA, "combine launch failed");
     return FKL_OK;
   }
-  if (launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, crow, &hdr->status, st) != cudaSuccess)
+  if (launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, nullptr, crow, &hdr->status, st) != cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "prep launch failed");
   if (launch_weights(mask, nullptr, 1, 0, T, reinterpret_cast<int*>(ws + pl.off_scnt), hdr, wrow, st) != cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "weights launch failed");
@@ -120,6 +120,7 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
   FwdParams fp;
   fp.pairs = pairs;
   fp.part = part;
+  fp.sg = nullptr;
   fp.T = (int)T; fp.K = (int)K; fp.V = (int)V; fp.nsplit = nsplit;
   fp.scale2 = 1.4426950408889634f / tau;
   if (launch_gemm_fwd(mH, mW, g, fp, g.num_units < sms ? g.num_units : sms, st) != cudaSuccess)

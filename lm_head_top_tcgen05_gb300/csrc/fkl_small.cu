@@ -7,6 +7,8 @@
 //             0 for masked tokens; from integer counts, so deterministic;
 //   combine   merges the forward's per-split partials into lse_t and KL_t and reduces
 //             sum_t w_t KL_t in a fixed order (no float atomics: deterministic);
+//   div       the other divergences: D_t from the student logits at the cached ids
+//             (forward) and the per-row / per-id terms of their dS (backward);
 //   scalars   g * tau for the backward's dS scale (g may live on the device);
 //   poison    fills the gradients with NaN when the device recorded an error;
 //   timeout   one bounded wait that nothing completes (checks the timeout path).
@@ -34,7 +36,7 @@ constexpr int kPrepWarps = 8;
 // (consecutive lanes, consecutive slots); ids are staged in shared memory to rank them.
 __global__ void __launch_bounds__(kPrepWarps * 32)
     prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ z, int64_t T, int K, int V,
-                float inv_tau, int2* __restrict__ pairs, float* __restrict__ crow,
+                float inv_tau, int2* __restrict__ pairs, int* __restrict__ slot, float* __restrict__ crow,
                 uint32_t* __restrict__ status) {
   extern __shared__ int sid[];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
       rank += (o < id) || (o == id && j < k);
     }
     pairs[t * K + rank] = make_int2(id, __float_as_int(pk));
+    if (slot) slot[t * K + rank] = k;
   }
   c = warp_sum(c);
   if (!row_ok) bad |= kStatusBadRowBit;
@@ -95,12 +98,12 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
 }
 
 cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t T, int K, int V, float tau,
-                        int2* pairs, float* crow, uint32_t* status, cudaStream_t st) {
+                        int2* pairs, int* slot, float* crow, uint32_t* status, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(kPrepWarps) * K * sizeof(int);
   const int64_t blocks = (T + kPrepWarps - 1) / kPrepWarps;
   prep_kernel<<<static_cast<unsigned>(blocks), kPrepWarps * 32, smem, st>>>(
-      idx, logits, T, K, V, 1.0f / tau, pairs, crow, status);
+      idx, logits, T, K, V, 1.0f / tau, pairs, slot, crow, status);
   return cudaGetLastError();
 }
 
@@ -183,16 +186,226 @@ __global__ void __launch_bounds__(kFinalThreads)
   }
 }
 
+cudaError_t launch_combine_rows(const float* part, int nsplit, const float* crow, const float* wrow,
+                                int64_t T, float tau, float* lse, double* bsum, int* bcnt, int64_t nb,
+                                cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  combine_rows_kernel<<<static_cast<unsigned>(nb), kCombineThreads, 0, st>>>(
+      part, nsplit, crow, wrow, T, 1.0f / tau, lse, bsum, bcnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_final(const double* bsum, const int* bcnt, int64_t T, int64_t nb, float tau,
+                                 WsHeader* hdr, float* loss, cudaStream_t st) {
+  combine_final_kernel<<<1, kFinalThreads, 0, st>>>(bsum, bcnt, T > 0 ? nb : 0, tau, hdr, loss);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const float* part, int nsplit, const float* crow, const float* wrow,
                            int64_t T, float tau, float* lse, double* bsum, int* bcnt, int64_t nb,
                            WsHeader* hdr, float* loss, cudaStream_t st) {
-  if (T > 0) {
-    combine_rows_kernel<<<static_cast<unsigned>(nb), kCombineThreads, 0, st>>>(
-        part, nsplit, crow, wrow, T, 1.0f / tau, lse, bsum, bcnt);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  cudaError_t e = launch_combine_rows(part, nsplit, crow, wrow, T, tau, lse, bsum, bcnt, nb, st);
+  if (e != cudaSuccess) return e;
+  return launch_combine_final(bsum, bcnt, T, nb, tau, hdr, loss, st);
+}
+
+// ---------------------------------------------------------------- other divergences
+// With p the teacher's probability at one id (its slots added), q = exp(s / tau - lse) the
+// student's and D = sum over the row's ids of phi(p, q) + psi * (student mass outside
+// them), the per-id terms are phi and q * gamma, gamma = dD/dq at that id (psi outside).
+// Written out per divergence from its definition (JSD: m = b p + (1 - b) q; skew KL:
+// m = a p + (1 - a) q; skew reverse KL: m = a q + (1 - a) p):
+//   JSD        phi = b p log(p / m) + (1 - b) q log(q / m)   q gamma = (1 - b) q log(q / m)
+//              psi = -(1 - b) log(1 - b)
+//   skew KL    phi = p log(p / m)                            q gamma = -(1 - a) p q / m
+//              psi = 0
+//   skew RKL   phi = q log(q / m)                            q gamma = q (log(q / m) + 1 - a q / m)
+//              psi = -log a
+//   TV         phi = |p - q| / 2                             q gamma = -q sign(p - q) / 2
+//              psi = 1 / 2
+// log q is taken as s / tau - lse, so the terms stay finite where q underflows.
+__device__ __forceinline__ float div_psi(const DivSpec& dv) {
+  switch (dv.kind) {
+    case 1: return -(1.f - dv.param) * log1pf(-dv.param);
+    case 3: return -logf(dv.param);
+    case 4: return 0.5f;
+    default: return 0.f;
   }
-  combine_final_kernel<<<1, kFinalThreads, 0, st>>>(bsum, bcnt, T > 0 ? nb : 0, tau, hdr, loss);
+}
+
+__device__ __forceinline__ void div_terms(const DivSpec& dv, float p, float logq, float& phi, float& qg) {
+  const float q = expf(logq);
+  const float c = dv.param;
+  switch (dv.kind) {
+    case 1: {
+      const float lm = logf(fmaf(c, p, (1.f - c) * q));
+      const float ql = q * (logq - lm);
+      phi = c * p * (logf(p) - lm) + (1.f - c) * ql;
+      qg = (1.f - c) * ql;
+      break;
+    }
+    case 2: {
+      const float m = fmaf(c, p, (1.f - c) * q);
+      const float lm = c == 0.f ? logq : logf(m);
+      phi = p * (logf(p) - lm);
+      qg = -(1.f - c) * p * (c == 0.f ? 1.f : q / m);
+      break;
+    }
+    case 3: {
+      if (c == 1.f) { phi = 0.f; qg = 0.f; break; }
+      const float m = fmaf(c, q, (1.f - c) * p);
+      const float l = logq - logf(m);
+      phi = q * l;
+      qg = q * (l + 1.f - c * q / m);
+      break;
+    }
+    case 4: {
+      const float dlt = p - q;
+      phi = 0.5f * fabsf(dlt);
+      qg = dlt > 0.f ? -0.5f * q : (dlt < 0.f ? 0.5f * q : 0.f);
+      break;
+    }
+    default: {  // KL
+      phi = p * (logf(p) - logq);
+      qg = -p;
+    }
+  }
+}
+
+// Per-row sums over the merged ids of one row (warp per row; lanes over sorted positions):
+// phi, q and q * gamma.  The pair at position j starts a run of equal ids unless position
+// j - 1 holds the same id; the run's first position carries the run's total p, the others
+// contribute nothing.  Ids outside [0, V) (sorted last as INT_MAX) and p = 0 are skipped.
+// s_at(j) gives the student logit at position j.  If r_out is not NULL, the per-position
+// term r = q psi - q gamma (0 off a run start) is stored there, after the whole warp has
+// read the row.
+template <class SAt>
+__device__ __forceinline__ void div_row(const DivSpec& dv, const int2* row, int K, float lse, float inv_tau,
+                                        float psi, SAt s_at, int lane, float& sphi, float& sq, float& sqg,
+                                        int2* r_out) {
+  sphi = 0.f;
+  sq = 0.f;
+  sqg = 0.f;
+  for (int j0 = 0; j0 < K; j0 += 32) {
+    const int j = j0 + lane;
+    float r = 0.f;
+    if (j < K) {
+      const int id = row[j].x;
+      const bool start = id != INT_MAX && (j == 0 || row[j - 1].x != id);
+      if (start) {
+        float p = __int_as_float(row[j].y);
+        for (int jj = j + 1; jj < K && row[jj].x == id; ++jj) p += __int_as_float(row[jj].y);
+        if (p > 0.f) {
+          const float logq = s_at(j) * inv_tau - lse;
+          float phi, qg;
+          div_terms(dv, p, logq, phi, qg);
+          const float q = expf(logq);
+          sphi += phi;
+          sq += q;
+          sqg += qg;
+          r = q * psi - qg;
+        }
+      }
+    }
+    if (r_out) {
+      __syncwarp();
+      if (j < K) r_out[j].y = __float_as_int(r);
+      __syncwarp();
+    }
+  }
+  sphi = warp_sum(sphi);
+  sq = warp_sum(sq);
+  sqg = warp_sum(sqg);
+}
+
+constexpr int kDivRowsThreads = 256;  // 8 warps; a block covers the combine's 256-row block
+
+__global__ void __launch_bounds__(kDivRowsThreads)
+    div_rows_kernel(DivSpec dv, int compute, const int2* __restrict__ pairs, const int* __restrict__ slot,
+                    const float* __restrict__ sg, const float* __restrict__ lse, const float* __restrict__ wrow,
+                    int64_t T, int K, float inv_tau, float* __restrict__ user_s, double* __restrict__ bsum,
+                    int* __restrict__ bcnt) {
+  __shared__ double ssum[kDivRowsThreads];
+  __shared__ int scnt[kDivRowsThreads];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float psi = div_psi(dv);
+  for (int i = w; i < kDivRowsThreads; i += kDivRowsThreads / 32) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kDivRowsThreads + i;
+    double v = 0.0;
+    int c = 0;
+    if (t < T) {
+      const int2* row = pairs + t * K;
+      const float* srow = sg + t * K;
+      if (user_s) {
+        for (int j = lane; j < K; j += 32)
+          user_s[t * K + slot[t * K + j]] = row[j].x == INT_MAX ? NAN : srow[j];
+      }
+      const float wt = wrow[t];
+      if (compute && wt != 0.f) {
+        float sphi, sq, sqg;
+        div_row(dv, row, K, lse[t], inv_tau, psi, [&](int j) { return srow[j]; }, lane, sphi, sq, sqg, nullptr);
+        v = static_cast<double>(wt) * (static_cast<double>(sphi) + static_cast<double>(psi) * (1.0 - sq));
+        c = 1;
+      }
+    }
+    if (lane == 0) {
+      ssum[i] = v;
+      scnt[i] = c;
+    }
+  }
+  if (!compute) return;
+  __syncthreads();
+  for (int o = kDivRowsThreads / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      ssum[threadIdx.x] += ssum[threadIdx.x + o];
+      scnt[threadIdx.x] += scnt[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    bsum[blockIdx.x] = ssum[0];
+    bcnt[blockIdx.x] = scnt[0];
+  }
+}
+
+cudaError_t launch_div_rows(DivSpec dv, const int2* pairs, const int* slot, const float* sg,
+                            const float* lse, const float* wrow, int64_t T, int K, float tau,
+                            float* user_s, double* bsum, int* bcnt, int64_t nb, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int compute = dv.kind != 0;
+  if (!compute && user_s == nullptr) return cudaSuccess;
+  div_rows_kernel<<<static_cast<unsigned>(nb), kDivRowsThreads, 0, st>>>(
+      dv, compute, pairs, slot, sg, lse, wrow, T, K, 1.0f / tau, user_s, bsum, bcnt);
+  return cudaGetLastError();
+}
+
+constexpr int kDivCoefWarps = 8;
+
+// a_t = psi - gbar, gbar = sum over ids of q gamma + psi (1 - sum over ids of q): then
+// dD/ds_v = q_v (gamma_v - gbar) / tau = (a_t q_v - r_v) / tau with r = q psi - q gamma at
+// the ids and 0 elsewhere (gamma = psi there).
+__global__ void __launch_bounds__(kDivCoefWarps * 32)
+    div_coef_kernel(DivSpec dv, int2* __restrict__ pairs, const int* __restrict__ slot,
+                    const float* __restrict__ user_s, const float* __restrict__ lse, int64_t T, int K,
+                    float inv_tau, float* __restrict__ arow) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kDivCoefWarps + w;
+  if (t >= T) return;  // uniform per warp
+  const float psi = div_psi(dv);
+  int2* row = pairs + t * K;
+  const int* srow = slot + t * K;
+  const float* us = user_s + t * K;
+  float sphi, sq, sqg;
+  div_row(dv, row, K, lse[t], inv_tau, psi, [&](int j) { return us[srow[j]]; }, lane, sphi, sq, sqg, row);
+  if (lane == 0) arow[t] = psi - (sqg + psi * (1.f - sq));
+}
+
+cudaError_t launch_div_coef(DivSpec dv, int2* pairs, const int* slot, const float* user_s,
+                            const float* lse, int64_t T, int K, float tau, float* arow, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int64_t blocks = (T + kDivCoefWarps - 1) / kDivCoefWarps;
+  div_coef_kernel<<<static_cast<unsigned>(blocks), kDivCoefWarps * 32, 0, st>>>(
+      dv, pairs, slot, user_s, lse, T, K, 1.0f / tau, arow);
   return cudaGetLastError();
 }
 

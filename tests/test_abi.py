@@ -1,6 +1,7 @@
 """The C ABI library builds, loads without a GPU, exports every declared symbol, sizes its
 workspace as documented and rejects bad arguments on the host before touching CUDA."""
 import ctypes
+import os
 import re
 from pathlib import Path
 
@@ -160,3 +161,49 @@ def test_options_are_checked_on_host(L):
     o = FklOptions()
     o.accumulate = 4
     assert fwd(o) == INVALID
+
+
+def test_divergence_options_are_checked_on_host(L):
+    from lm_head_top_tcgen05_gb300._lib import FklOptions
+
+    ws_bytes = L.fkl_workspace_size(256, 256, 4096, 16, 64)
+
+    def fwd(o):
+        return L.fkl_forward_ex(16, 16, 16, 16, None, 256, 256, 4096, 16, 1.0, 64, ctypes.byref(o), 16, 16, 256,
+                                ws_bytes, None)
+
+    def bwd(o):
+        return L.fkl_backward_ex(16, 16, 16, 16, None, 16, None, 256, 256, 4096, 16, 1.0, 64, ctypes.byref(o),
+                                 16, 16, 256, ws_bytes, None)
+
+    for kind, param in ((5, 0.0), (-1, 0.0), (1, 0.0), (1, 1.0), (2, 1.0), (2, -0.1), (3, 0.0), (3, 1.5),
+                        (1, float("nan"))):
+        o = FklOptions()
+        o.divergence, o.div_param = kind, param
+        assert fwd(o) == INVALID, (kind, param)
+    o = FklOptions()
+    o.divergence, o.div_param = 1, 0.5
+    o.student_topk_logits = 18
+    assert fwd(o) == ALIGN
+    o.student_topk_logits = None
+    assert bwd(o) == INVALID  # the backward of a divergence other than KL needs the student logits
+
+
+def test_options_struct_layout_matches_header(tmp_path):
+    # Compile a probe against include/fkl.h and compare fkl_options' layout with the binding's.
+    import subprocess
+
+    from lm_head_top_tcgen05_gb300._lib import FklOptions
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "layout.c"
+    fields = [f for f, _ in FklOptions._fields_]
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "fkl.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(fkl_options));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(fkl_options, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)], check=True)
+    out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(FklOptions)
+    assert out[1:] == [getattr(FklOptions, f).offset for f in fields]
