@@ -102,7 +102,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_oracle_rate(x, rows: int):
+def cpu_oracle_rate(x, rows: int, divergence: str = "kl", div_param=None):
     """Tokens/s of the float64 oracle (forward + backward) on the first `rows` tokens."""
     import numpy as np
 
@@ -112,8 +112,13 @@ def cpu_oracle_rate(x, rows: int):
     H64 = oracle.to_f64(x.H[:rows])
     idx, z, m = x.topk_idx[:rows], x.topk_logits[:rows], x.mask[:rows]
     t0 = time.perf_counter()
-    oracle.forward(H64, W64, idx, z, m, x.tau)
-    oracle.backward(H64, W64, idx, z, m, x.tau)
+    if divergence == "kl":
+        oracle.forward(H64, W64, idx, z, m, x.tau)
+        oracle.backward(H64, W64, idx, z, m, x.tau)
+    else:
+        prm = {"jsd": 0.5, "skew_kl": 0.1, "skew_rkl": 0.1}.get(divergence, 0.0) if div_param is None else div_param
+        oracle.divergences.forward(H64, W64, idx, z, m, x.tau, divergence, prm)
+        oracle.divergences.backward(H64, W64, idx, z, m, x.tau, divergence, prm)
     dt = time.perf_counter() - t0
     del W64, H64
     cores = len(os.sched_getaffinity(0))
@@ -142,7 +147,8 @@ def run_reference(args, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "V": w.V, "K": w.K, "tau": w.tau,
                    "chunk": w.chunk},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "blas_threads": blas_threads(),
+                         "kind": "oracle",
                          "sample": f"first {args.cpu_rows} tokens of the batch per step, full "
                                    f"vocabulary, float64 forward+backward; ms_per_step extrapolates "
                                    f"to T={w.T}"},
@@ -167,14 +173,48 @@ KIND_NAMES = {0: "forward projection + logsumexp/top-K", 1: "dS recompute", 2: "
 KERNEL_NAMES = {0: "gemm2_kernel<256,0,0,EpiFwd> (two-SM)", 1: "gemm2_kernel<256,0,0,EpiDs> (two-SM)",
                 2: "gemm2_kernel<256,1,1,EpiF32> (two-SM, dW)", 3: "gemm2_kernel<256,0,1,EpiF32> (two-SM, dH)"}
 # Launches per step outside the GEMM trace: forward prep, 3 token-weight kernels, 2 combine;
-# backward prep, 3 token-weight kernels, gradient scale, poison check.
+# backward prep, 3 token-weight kernels, gradient scale, poison check.  A divergence other
+# than KL adds one per-row kernel to each pass.
 UNTRACED_LAUNCHES_PER_STEP = 12
+
+# Dense bf16 tensor-core rate of one Blackwell SM: 4096 FMA = 8192 FLOP per clock (NVIDIA's
+# nominal 2.25 PFLOP/s for GB300 is 152 SMs x 8192 x 1.807 GHz).  The nominal roofline of a
+# run is this rate x the device's SM count x the SM clock sampled during the timed region.
+BF16_FLOP_PER_CLK_PER_SM = 8192
+
+
+def blas_threads():
+    """Threads of the BLAS that NumPy uses (the oracle's matrix products), or None."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    import ctypes
+    import glob
+
+    import numpy as np
+
+    libs = glob.glob(os.path.join(os.path.dirname(np.__file__), os.pardir, "numpy.libs", "*openblas*"))
+    for path in libs:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, name, None)
+            if fn is not None:
+                return int(fn())
+    return None
 
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "c2b1d065ffc67ae9"
-TRAFFIC_BYTES = {1: 3.068e9, 2: 3.097e9, 3: 3.126e9}
+TRAFFIC_SOURCES_SHA = "98b2b6738e4a201a"
+TRAFFIC_BYTES = {1: 2.852e9, 2: 2.517e9, 3: 2.680e9}
 TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
 
 
@@ -294,6 +334,11 @@ def main():
     ap.add_argument("--vocab", type=int, default=None,
                     help="override V (profiling case with the full workload's per-launch GEMM shapes)")
     ap.add_argument("--chunk", type=int, default=None, help="override chunk")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (the memory / time sweep over sequence length)")
+    ap.add_argument("--divergence", default="kl", choices=["kl", "jsd", "skew_kl", "skew_rkl", "tv"],
+                    help="the loss's divergence (default: KL, the headline)")
+    ap.add_argument("--div-param", type=float, default=None, help="b for jsd, a for the skew forms")
     ap.add_argument("--mode", default="loss", choices=["loss", "teacher_topk"],
                     help="loss: the fused KL fwd+bwd step (the headline); teacher_topk: the offline "
                          "teacher cache producer on the same shapes")
@@ -326,6 +371,8 @@ def main():
     if args.vocab is not None or args.chunk is not None:
         w = dataclasses.replace(w, name=f"{w.name}_V{args.vocab or w.V}_chunk{args.chunk or w.chunk}",
                                 V=args.vocab or w.V, chunk=args.chunk or w.chunk)
+    if args.tokens is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_T{args.tokens}", T=args.tokens)
     x = workloads.make_inputs(w)
     T, d, V, K = w.T, w.d, w.V, w.K
 
@@ -344,9 +391,14 @@ def main():
     inputs_bytes = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
 
+    # divergences other than KL hand the student logits at the cached ids to the backward
+    div = dict(divergence=args.divergence, div_param=args.div_param)
+    s_ids = torch.empty((T, K), dtype=torch.float32, device=dev) if args.divergence != "kl" else None
+
     def step():
-        loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws)
-        fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW))
+        loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids, **div)
+        fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
+                     student_topk_logits=s_ids, **div)
         return loss
 
     for _ in range(args.warmup):
@@ -365,9 +417,11 @@ def main():
         start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws)
+            loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids,
+                                    **div)
             ev[i][1].record(stream)
-            fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW))
+            fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
+                         student_topk_logits=s_ids, **div)
             ev[i][2].record(stream)
         end.record(stream)
         barrier()
@@ -378,6 +432,8 @@ def main():
     peak_bytes = torch.cuda.max_memory_allocated(dev)
     fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
     bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
+    step_ms_median = statistics.median(ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     loss_val = loss.item()
 
     # ---------------------------------------------------------------- end to end (host buffers)
@@ -391,8 +447,9 @@ def main():
         def e2e_step():
             Hd = hH.to(dev, non_blocking=True)
             idd, zd, md = hidx.to(dev, non_blocking=True), hz.to(dev, non_blocking=True), hm.to(dev, non_blocking=True)
-            l, s = fkl.forward(Hd, Wt, idd, zd, md, w.tau, w.chunk, workspace=ws)
-            fkl.backward(Hd, Wt, idd, zd, md, s, None, w.tau, w.chunk, workspace=ws, out=(dH, dW))
+            l, s = fkl.forward(Hd, Wt, idd, zd, md, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids, **div)
+            fkl.backward(Hd, Wt, idd, zd, md, s, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
+                         student_topk_logits=s_ids, **div)
             hloss.copy_(l, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -420,15 +477,24 @@ def main():
     sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     burst = float(peaks["bf16_tflops"])
     traced = sum(v["launches"] for v in kernels.values())
-    launches_per_step = UNTRACED_LAUNCHES_PER_STEP + traced / args.steps
+    launches_per_step = UNTRACED_LAUNCHES_PER_STEP + (2 if args.divergence != "kl" else 0) + traced / args.steps
     clk = clocks.summary()
     dom = max(kernels, key=lambda k: kernels[k]["ms_total"])  # largest share of the step
+    nominal = None
+    if clk and clk.get("sm_mhz"):
+        at_clk = sms * BF16_FLOP_PER_CLK_PER_SM * clk["sm_mhz"] * 1e6 / 1e12
+        at_max = sms * BF16_FLOP_PER_CLK_PER_SM * clk["sm_max_mhz"] * 1e6 / 1e12
+        nominal = {"sms": sms, "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM,
+                   "tflops_at_median_clock": at_clk, "frac": kernels[dom]["tflops"] / at_clk,
+                   "step_frac": tflops / world / at_clk,
+                   "tflops_at_max_clock": at_max, "frac_of_max_clock": kernels[dom]["tflops"] / at_max}
     out = {
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "chunk": w.chunk,
-                   "l2": "inputs larger than L2 (W is 1.16 GB); no flush"},
+                   "divergence": args.divergence, "l2": "inputs larger than L2 (W is 1.16 GB); no flush"},
+        "ms_per_step_median": step_ms_median,
         "tflops": tflops,
         "tensor_frac_step": tflops / sustained,
         "peak_gib": peak_bytes / 2**30,
@@ -442,7 +508,8 @@ def main():
                      "flops_per_launch": kernels[dom]["flops_per_launch"],
                      "ms_per_launch": kernels[dom]["ms_per_launch"],
                      "traffic": traffic_per_launch(dom, kernels[dom]["flops_per_launch"], d)
-                     if T == 32768 else None},
+                     if T == 32768 else None,
+                     "nominal": nominal},
         "kernels": {KIND_NAMES[k]: {kk: round(vv, 4) if isinstance(vv, float) else vv for kk, vv in v.items()}
                     for k, v in kernels.items()},
         "clocks": clk,
@@ -451,8 +518,9 @@ def main():
     if e2e is not None:
         out["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
-        rate, dt, cores, _ = cpu_oracle_rate(x, args.cpu_rows)
-        out["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+        rate, dt, cores, _ = cpu_oracle_rate(x, args.cpu_rows, args.divergence, args.div_param)
+        out["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "blas_threads": blas_threads(),
+                               "kind": "oracle",
                                "sample": f"first {args.cpu_rows} tokens, full vocabulary, float64 "
                                          f"forward+backward, {dt:.1f} s"}
     print(json.dumps(out), flush=True)
