@@ -191,3 +191,42 @@ def backward(H, W, topk_idx, topk_logits, mask, tau: float, kind: str, param: fl
         dH[r] = ds @ W
         dW += ds.T @ H[r]
     return dH, dW
+
+
+def dH_rows(H, W, topk_idx, topk_logits, mask, tau: float, kind: str, param: float, rows: Sequence[int],
+            grad: float = 1.0, chunk: int = 64, norm: str = "tokens", seq_ids=None):
+    """Selected rows of dH: row t needs only row t of the logits (exact at any size)."""
+    param = check_param(kind, param)
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = _np(topk_idx, np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    row_scale = float(grad) * float(tau) * token_weights(mask, H.shape[0], norm, seq_ids)[rows]
+    p, _ = teacher_probs(_np(topk_logits)[rows], tau)
+    out = np.zeros((len(rows), H.shape[1]))
+    for b0 in range(0, len(rows), chunk):
+        r = rows[b0:b0 + chunk]
+        ds = ds_block(H[r] @ W.T, idx[r], p[b0:b0 + chunk], tau, row_scale[b0:b0 + chunk], kind, param)
+        out[b0:b0 + chunk] = ds @ W
+    return out
+
+
+def dW_rows(H, W, topk_idx, topk_logits, mask, tau: float, kind: str, param: float,
+            vocab_rows: Sequence[int], grad: float = 1.0, chunk: int = 64, norm: str = "tokens",
+            seq_ids=None):
+    """Selected rows of dW: row v sums dS[t, v] H[t] over the tokens with a nonzero weight, so it
+    needs those tokens' logits (affordable when few tokens are valid)."""
+    param = check_param(kind, param)
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    idx = _np(topk_idx, np.int64)
+    vr = np.asarray(vocab_rows, dtype=np.int64)
+    scale = float(grad) * float(tau) * token_weights(mask, H.shape[0], norm, seq_ids)
+    live = np.flatnonzero(scale)
+    p, _ = teacher_probs(_np(topk_logits)[live], tau)
+    out = np.zeros((len(vr), H.shape[1]))
+    for b0 in range(0, len(live), chunk):
+        r = live[b0:b0 + chunk]
+        ds = ds_block(H[r] @ W.T, idx[r], p[b0:b0 + chunk], tau, scale[r], kind, param)
+        out += ds[:, vr].T @ H[r]
+    return out

@@ -136,3 +136,35 @@ def test_divergence_zero_when_teacher_is_student(fkl):
     for kind, param in (("jsd", 0.5), ("skew_kl", 0.1), ("skew_rkl", 0.1), ("tv", None)):
         gpu = run_gpu(fkl, x, kind, param)
         assert gpu["status"] == 0 and abs(gpu["loss"]) < 1e-5, (kind, gpu["loss"])
+
+
+@pytest.mark.parametrize("kind,param", [("jsd", 0.5), ("tv", None)])
+def test_full_size_sparse_mask_exact(fkl, kind, param):
+    # The 32K workload's shapes, chunk and slabs (the benchmark's launches) with one valid token
+    # per 128-row block: the oracle then computes the exact loss and sampled rows of dH and dW.
+    import dataclasses
+
+    w = workloads.WORKLOADS["gptoss20b_32k"]
+    x = workloads.make_inputs(w)
+    rng = np.random.default_rng(8)
+    valid = np.arange(0, w.T, 128) + rng.integers(0, 128, size=w.T // 128)
+    mask = torch.zeros(w.T, dtype=torch.uint8)
+    mask[valid] = 1
+    x = dataclasses.replace(x, mask=mask)
+    gpu = run_gpu(fkl, x, kind, param)
+    assert gpu["status"] == 0
+    prm = 0.5 if param is None and kind == "jsd" else (0.0 if param is None else param)
+    H64, W64 = oracle.to_f64(x.H), oracle.to_f64(x.W)
+    rows = np.unique(np.concatenate([valid, rng.choice(w.T, 16, replace=False)]))
+    ref = dv.forward(H64, W64, x.topk_idx, x.topk_logits, mask, w.tau, kind, prm, rows=rows)
+    assert ref["loss"] is not None
+    assert abs(gpu["loss"] - ref["loss"]) <= 1e-3 * abs(ref["loss"])
+    assert np.max(np.abs(gpu["lse"][rows] - ref["lse"])) <= 1e-3
+    assert_s_close(gpu["s_ids"][rows], ref["s_at_ids"])
+    some = valid[:: max(1, len(valid) // 24)]
+    dH_ref = dv.dH_rows(H64, W64, x.topk_idx, x.topk_logits, mask, w.tau, kind, prm, some)
+    assert_grad_close(gpu["dH"][some], dH_ref, "dH rows")
+    hot = np.unique(x.topk_idx.numpy()[valid[:4]].ravel())[:24]
+    vr = np.unique(np.concatenate([hot, rng.choice(w.V, 24, replace=False), [0, w.V - 1]]))
+    dW_ref = dv.dW_rows(H64, W64, x.topk_idx, x.topk_logits, mask, w.tau, kind, prm, vr)
+    assert_grad_close(gpu["dW"][vr], dW_ref, "dW rows")

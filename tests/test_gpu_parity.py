@@ -82,6 +82,13 @@ CASES = {
     "single_slot": (257, 136, 300, 1, 1.0, 64, 0.05, 4),
     "one_token": (1, 64, 777, 8, 1.0, 1, 0.0, 5),
     "wide_d": (200, 1152, 3000, 32, 1.3, 512, 0.0, 6),
+    # the ABI's limits and extremes
+    "max_k": (136, 64, 3000, 1024, 1.0, 256, 0.0, 7),
+    "min_d": (300, 8, 2000, 16, 1.0, 128, 0.1, 8),
+    "d4096": (264, 4096, 2600, 24, 2.0, 512, 0.0, 9),
+    "cold_tau": (200, 128, 3000, 16, 0.05, 256, 0.0, 10),
+    "hot_tau": (200, 128, 3000, 16, 20.0, 256, 0.0, 11),
+    "vocab_below_one_tile": (300, 96, 100, 20, 1.0, 64, 0.0, 12),
 }
 
 

@@ -224,3 +224,18 @@ def test_parameter_ranges():
         dv.check_param("skew_rkl", 0.0)
     with pytest.raises(ValueError):
         dv.check_param("reverse_kl", 0.5)
+
+
+@pytest.mark.parametrize("kind,param", [("jsd", 0.3), ("skew_rkl", 0.2), ("tv", 0.0)])
+def test_row_samplers_match_the_full_backward(kind, param):
+    # dH_rows / dW_rows (used at full vocabulary size) are rows of the finite-difference-pinned
+    # backward
+    H, W, idx, z = rand_case(T=9, d=7, V=40, K=6, seed=13)
+    mask = np.array([1, 0, 1, 1, 0, 1, 1, 1, 0], np.uint8)
+    dH, dW = dv.backward(H, W, idx, z, mask, 1.4, kind, param, grad=0.6)
+    rows = [0, 3, 4, 8]
+    np.testing.assert_allclose(dv.dH_rows(H, W, idx, z, mask, 1.4, kind, param, rows, grad=0.6, chunk=3),
+                               dH[rows], rtol=1e-12, atol=1e-15)
+    vr = [0, 5, 17, 39]
+    np.testing.assert_allclose(dv.dW_rows(H, W, idx, z, mask, 1.4, kind, param, vr, grad=0.6, chunk=2),
+                               dW[vr], rtol=1e-12, atol=1e-15)
