@@ -23,6 +23,7 @@ namespace fkl {
 
 constexpr int kBM2 = 256;  // rows per CTA pair
 
+
 __host__ __device__ constexpr int stages2_for(int bn) { return bn == 256 ? 7 : 8; }
 // An MN-major B half that is not a whole number of 64-element (128-byte) rows uses the
 // 64-byte swizzle: 32-element atoms (a 192-wide tile: 96-wide halves, three atoms).
@@ -231,10 +232,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-// Clusters of this instantiation that fit on the device at once (cached per device).
+// Clusters of one kernel instantiation that fit on the device at once, cached per device in
+// `cached` (one array per instantiation: the occupancy depends on its shared memory).
 template <class Kern>
-int max_pair_clusters(Kern kern, size_t smem, int sms) {
-  static int cached[128] = {};
+int max_pair_clusters(Kern kern, size_t smem, int sms, int (&cached)[128]) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return sms / 2;
   if (cached[dev] > 0) return cached[dev];
@@ -260,7 +261,8 @@ cudaError_t launch_gemm2_t(const CUtensorMap& a, const CUtensorMap& b, const Gem
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
-  const int clusters = max_pair_clusters(kern, SMEM, sms);
+  static int cached[128] = {};  // one per instantiation of this template
+  const int clusters = max_pair_clusters(kern, SMEM, sms, cached);
   const int n = g.num_units < clusters ? g.num_units : clusters;
   kern<<<2 * n, kThreads, SMEM, st>>>(a, b, g, ep);
   return cudaGetLastError();

@@ -112,3 +112,16 @@ def test_pair_many_waves(L, a_mn, b_mn, bn):
 
 def test_pair_accumulate_long_k(L):
     assert run_gemm(L, 512, 384, 8192, True, True, 128, accumulate=True, seed=9, pair=True) < 5e-5
+
+
+# ---- a ragged last tile of 256-wide two-SM tiles at the d = 2880 shapes (8, 64 or 72 columns)
+
+@pytest.mark.parametrize("N", [2880, 2824, 2888, 320])
+@pytest.mark.parametrize("a_mn,b_mn", [(True, True), (False, True), (False, False)])
+def test_pair_ragged_last_tile(L, N, a_mn, b_mn):
+    # N = 2880 and 320: 64 columns in the last tile; 2824: 8; 2888: 72
+    assert run_gemm(L, 512, N, 192, a_mn, b_mn, 256, seed=N, pair=True) < 1e-5
+
+
+def test_pair_ragged_last_tile_accumulate(L):
+    assert run_gemm(L, 264, 2880, 520, True, True, 256, accumulate=True, seed=13, pair=True) < 2e-5
