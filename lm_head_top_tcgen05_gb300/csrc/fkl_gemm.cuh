@@ -482,13 +482,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Raises the kernel's dynamic shared-memory limit once per device (`done`: one array per
+// kernel instantiation), so that later launches, including launches recorded into a CUDA
+// graph, make no attribute call.
+template <class Kern>
+cudaError_t smem_limit_once(Kern kern, size_t smem, bool (&done)[128]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool slot = dev >= 0 && dev < 128;
+  if (slot && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess && slot) done[dev] = true;
+  return e;
+}
+
 template <int BN, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& g,
                           const typename Epi::Params& ep, int grid, cudaStream_t st) {
   constexpr size_t SMEM = smem_bytes_for(BN);
   auto kern = gemm_kernel<BN, A_MN, B_MN, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM));
+  static bool limit_set[128] = {};  // one per instantiation of this template
+  cudaError_t e = smem_limit_once(kern, SMEM, limit_set);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, SMEM, st>>>(a, b, g, ep);
   return cudaGetLastError();

@@ -23,7 +23,6 @@ namespace fkl {
 
 constexpr int kBM2 = 256;  // rows per CTA pair
 
-
 __host__ __device__ constexpr int stages2_for(int bn) { return bn == 256 ? 7 : 8; }
 // An MN-major B half that is not a whole number of 64-element (128-byte) rows uses the
 // 64-byte swizzle: 32-element atoms (a 192-wide tile: 96-wide halves, three atoms).
@@ -258,10 +257,10 @@ cudaError_t launch_gemm2_t(const CUtensorMap& a, const CUtensorMap& b, const Gem
                            const typename Epi::Params& ep, int sms, cudaStream_t st) {
   constexpr size_t SMEM = smem2_bytes_for(BN);
   auto kern = gemm2_kernel<BN, A_MN, B_MN, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM));
+  static bool limit_set[128] = {};  // per instantiation of this template, per device
+  static int cached[128] = {};
+  cudaError_t e = smem_limit_once(kern, SMEM, limit_set);
   if (e != cudaSuccess) return e;
-  static int cached[128] = {};  // one per instantiation of this template
   const int clusters = max_pair_clusters(kern, SMEM, sms, cached);
   const int n = g.num_units < clusters ? g.num_units : clusters;
   kern<<<2 * n, kThreads, SMEM, st>>>(a, b, g, ep);

@@ -1,0 +1,76 @@
+"""A whole forward + backward step captured in a CUDA graph and replayed.
+
+The library makes no synchronising call, allocates no memory and reads no host state that
+changes between calls once a shape has run (tensor maps are encoded on the host and passed
+as kernel parameters; occupancy and device queries are cached).  So after one eager call the
+step can be captured and replayed; replays must reproduce the eager results bit for bit,
+also after the inputs are refilled in place."""
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fkl(cuda_device):
+    from lm_head_top_tcgen05_gb300 import build
+
+    build.build()
+    import lm_head_top_tcgen05_gb300 as m
+
+    return m
+
+
+@pytest.mark.parametrize("divergence", ["kl", "jsd"])
+def test_graph_replay_matches_eager(fkl, divergence):
+    x = workloads.make_random(600, 320, 9000, 32, tau=1.3, chunk=128, seed=70, mask_frac=0.1)
+    y = workloads.make_random(600, 320, 9000, 32, tau=1.3, chunk=128, seed=71, mask_frac=0.2)
+    dev = torch.device("cuda")
+    H, W = x.H.to(dev), x.W.to(dev)
+    idx, z, m = x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev)
+    T, d = H.shape
+    V, K = W.shape[0], idx.shape[1]
+    ws = fkl.Workspace(dev)
+    ws.get(fkl.workspace_size(T, d, V, K, x.chunk), dev)
+    dH = torch.empty(T, d, device=dev)
+    dW = torch.empty(V, d, device=dev)
+    s_ids = torch.empty(T, K, device=dev) if divergence != "kl" else None
+    out = {}
+
+    def step():
+        loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk, workspace=ws, divergence=divergence,
+                                student_topk_logits=s_ids)
+        fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, workspace=ws, out=(dH, dW),
+                     divergence=divergence, student_topk_logits=s_ids)
+        out["loss"] = loss
+
+    def eager(inp):
+        for dst, src in zip((H, W, idx, z, m), (inp.H, inp.W, inp.topk_idx, inp.topk_logits, inp.mask)):
+            dst.copy_(src.to(dev))
+        step()
+        torch.cuda.synchronize()
+        return out["loss"].clone(), dH.clone(), dW.clone()
+
+    ref_x = eager(x)  # also warms up every launch of this shape
+    ref_y = eager(y)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+
+    for inp, ref in ((x, ref_x), (y, ref_y), (x, ref_x)):
+        for dst, src in zip((H, W, idx, z, m), (inp.H, inp.W, inp.topk_idx, inp.topk_logits, inp.mask)):
+            dst.copy_(src.to(dev))
+        dH.fill_(float("nan"))
+        dW.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert fkl.read_status(ws) == 0
+        assert torch.equal(out["loss"], ref[0])
+        assert torch.equal(dH, ref[1]) and torch.equal(dW, ref[2])
