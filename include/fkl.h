@@ -239,16 +239,31 @@ int32_t fkl_trace_read(float* ms, int32_t* kind, double* flops, int32_t capacity
  * states Ht (bf16 [T, d]) and LM head Wt (bf16 [V, d]), writes the K largest logits of each
  * row of s = Ht Wt^T (fp32 accumulation) and their ids, ordered by logit descending, ties by
  * the lower id: topk_idx int32 [T, K] and topk_logits fp32 [T, K] - the cache that
- * fkl_forward reads.  The T x V logits are never written: the projection runs twice, once to
- * find a per-row lower bound of the K-th largest logit, once to collect the logits at or
- * above it (at most max(512, 4K) per row; more, which needs massive ties, is reported as
- * FKL_ERR_TOPK_OVERFLOW with id -1 and logit NaN in that row).  Limits: 1 <= K <= V,
+ * fkl_forward reads.  The T x V logits are never written.  A first pass over every s-th
+ * vocabulary row (s = 4 for large V; fewer when V is small) finds a per-row lower bound of
+ * the K-th largest logit; a second, full projection collects the logits at or above it (at
+ * most max(512, 4 s K) per row; more, which needs massive ties or a teacher whose largest
+ * logits all avoid the sampled rows, is reported as FKL_ERR_TOPK_OVERFLOW with id -1 and
+ * logit NaN in that row).  The result is exact either way.  Limits: 1 <= K <= V,
  * d % 8 == 0; when V > 4096 also K <= 256 and K <= 8 * ceil(V / 256).
  */
 size_t fkl_teacher_topk_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K);
 fkl_status fkl_teacher_topk(const uint16_t* Ht, const uint16_t* Wt, int64_t T, int64_t d, int64_t V,
                             int64_t K, int32_t* topk_idx, float* topk_logits, void* workspace,
                             size_t ws_bytes, void* stream);
+
+/*
+ * fkl_teacher_topk with a cap on the bound pass's sampling stride: max_bound_stride = 1 reads
+ * every vocabulary row in the first pass (its bound is then the K-th largest of every split's
+ * largest logits, the tightest one, and the second pass collects at most about 4K per row),
+ * 2 or 4 allow sampling, 0 is the default (4).  A run that reported FKL_ERR_TOPK_OVERFLOW
+ * because of sampling succeeds with 1.  The workspace of fkl_teacher_topk_workspace_size
+ * serves every stride.  Other errors as fkl_teacher_topk, plus FKL_ERR_INVALID_ARG for
+ * another max_bound_stride.
+ */
+fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt, int64_t T, int64_t d, int64_t V,
+                               int64_t K, int32_t max_bound_stride, int32_t* topk_idx, float* topk_logits,
+                               void* workspace, size_t ws_bytes, void* stream);
 
 /* Static text for a status code. */
 const char* fkl_status_string(int status);

@@ -241,9 +241,12 @@ def fused_kl(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
 
 
 def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int = 100,
-                 workspace: Optional[Workspace] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                 workspace: Optional[Workspace] = None, max_bound_stride: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
     """Offline teacher cache: (topk_idx int32 [T, K], topk_logits float32 [T, K]) of the K
-    largest teacher logits Ht Wt^T per row, by logit descending (ties: lower id first)."""
+    largest teacher logits Ht Wt^T per row, by logit descending (ties: lower id first).
+
+    ``max_bound_stride`` caps the first pass's vocabulary sampling (0: default 4; 1: every
+    row, for a teacher whose sampled run reported FKL_ERR_TOPK_OVERFLOW)."""
     if not (Ht.is_cuda and Wt.is_cuda) or Ht.dtype != torch.bfloat16 or Wt.dtype != torch.bfloat16:
         raise TypeError("Ht and Wt must be bfloat16 CUDA tensors")
     if Ht.dim() != 2 or Wt.dim() != 2 or Ht.shape[1] != Wt.shape[1] or not (Ht.is_contiguous() and Wt.is_contiguous()):
@@ -256,7 +259,7 @@ def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int = 100,
     ws = _ws_for(workspace, int(n), Ht.device)
     idx = torch.empty((T, K), dtype=torch.int32, device=Ht.device)
     val = torch.empty((T, K), dtype=torch.float32, device=Ht.device)
-    st = lib().fkl_teacher_topk(_ptr(Ht), _ptr(Wt), T, d, V, K, _ptr(idx), _ptr(val), _ptr(ws), ws.numel(),
-                                _stream(Ht.device))
-    check(st, "fkl_teacher_topk")
+    st = lib().fkl_teacher_topk_ex(_ptr(Ht), _ptr(Wt), T, d, V, K, int(max_bound_stride), _ptr(idx), _ptr(val),
+                                   _ptr(ws), ws.numel(), _stream(Ht.device))
+    check(st, "fkl_teacher_topk_ex")
     return idx, val

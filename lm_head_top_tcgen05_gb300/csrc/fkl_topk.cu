@@ -6,10 +6,14 @@
 // teacher's LM-head projection s = Ht Wt^T is fused with the selection, so the T x V logits
 // are never written; two passes over the projection run on the two-SM GEMM:
 //
-//   1. bound pass   each row keeps, per vocabulary split, its kTopR largest logits in
-//                   registers (EpiTopR).  bound_kernel takes the K-th largest of those
-//                   S * kTopR values: theta_t, a lower bound of the row's K-th largest logit
-//                   (it is the K-th largest of a subset of the row), usually a tight one.
+//   1. bound pass   over every s-th vocabulary row of Wt (a strided tensor-map view; s
+//                   up to kMaxBoundStride, as long as enough values are kept), each row
+//                   keeps, per vocabulary split, its kTopR largest logits in registers
+//                   (EpiTopR).  bound_kernel takes the K-th largest of those S * kTopR
+//                   values: theta_t, a lower bound of the row's K-th largest logit (it is
+//                   the K-th largest of a subset of the row).  About s * K logits of a row
+//                   reach it, so the pass costs 1/s of a projection and the candidate
+//                   buffer holds 4 s K.
 //   2. candidate    recompute; every logit >= theta_t is appended to the row's candidate
 //      pass         buffer (EpiCand; an integer atomic counter per row).  All of the row's
 //                   top K are among them.
@@ -32,6 +36,7 @@ namespace fkl {
 
 constexpr int kTopR = 8;                // logits kept per (row, split) in the bound pass
 constexpr int kMaxBoundSplits = 32;     // splits of the bound pass
+constexpr int kMaxBoundStride = 4;      // the bound pass reads every s-th vocabulary row, s <= 4
 constexpr int64_t kAllCandidatesV = 4096;
 
 struct TopRParams {
@@ -231,17 +236,32 @@ __global__ void fill_kernel(float* __restrict__ a, int64_t n, float v) {
 // ---------------------------------------------------------------- planning
 struct TopkPlan {
   bool bound_pass;
+  int stride;      // bound pass: every stride-th vocabulary row
+  int64_t Vs;      // bound pass: rows it reads, ceil(V / stride)
   int cap;
   size_t off_topr, off_theta, off_cnt, off_cand, total;
 };
 
-static bool make_topk_plan(int64_t T, int64_t d, int64_t V, int64_t K, TopkPlan* p) {
+// Values the bound pass keeps for a row over n vocabulary rows: kTopR per split.
+static int64_t kept_values(int64_t n) {
+  const int64_t tiles = (n + kVocabTile - 1) / kVocabTile;
+  return (tiles < kMaxBoundSplits ? tiles : kMaxBoundSplits) * kTopR;
+}
+
+// max_stride: the largest sampling stride of the bound pass the caller allows (1, 2 or 4).
+static bool make_topk_plan(int64_t T, int64_t d, int64_t V, int64_t K, TopkPlan* p, int max_stride = kMaxBoundStride) {
   if (T < 0 || T >= (int64_t{1} << 31) || d < 8 || d % 8 != 0 || d >= (int64_t{1} << 20)) return false;
   if (V < 1 || V > (int64_t{1} << 30) || K < 1 || K > V) return false;
   p->bound_pass = V > kAllCandidatesV;
-  if (p->bound_pass && K > kMaxBoundSplits * kTopR) return false;
-  if (p->bound_pass && (V + 255) / 256 * kTopR < K) return false;
-  p->cap = p->bound_pass ? static_cast<int>(K * 4 > 512 ? K * 4 : 512) : static_cast<int>(V);
+  p->stride = 1;
+  p->Vs = V;
+  if (p->bound_pass) {
+    if (kept_values(V) < K) return false;
+    while (p->stride < max_stride && kept_values((V + 2 * p->stride - 1) / (2 * p->stride)) >= K) p->stride *= 2;
+    p->Vs = (V + p->stride - 1) / p->stride;
+  }
+  const int64_t cap = 4 * K * p->stride;
+  p->cap = p->bound_pass ? static_cast<int>(cap > 512 ? cap : 512) : static_cast<int>(V);
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   size_t off = 256;  // status header
   p->off_topr = off;  off = up(off + static_cast<size_t>(T) * (p->bound_pass ? kMaxBoundSplits * kTopR * 4 : 0));
@@ -269,9 +289,17 @@ extern "C" size_t fkl_teacher_topk_workspace_size(int64_t T, int64_t d, int64_t 
 extern "C" fkl_status fkl_teacher_topk(const uint16_t* Ht, const uint16_t* Wt, int64_t T, int64_t d, int64_t V,
                                        int64_t K, int32_t* topk_idx, float* topk_logits, void* workspace,
                                        size_t ws_bytes, void* stream) {
+  return fkl_teacher_topk_ex(Ht, Wt, T, d, V, K, 0, topk_idx, topk_logits, workspace, ws_bytes, stream);
+}
+
+extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt, int64_t T, int64_t d, int64_t V,
+                                          int64_t K, int32_t max_bound_stride, int32_t* topk_idx, float* topk_logits,
+                                          void* workspace, size_t ws_bytes, void* stream) {
   set_last_error_message("");
+  if (max_bound_stride != 0 && max_bound_stride != 1 && max_bound_stride != 2 && max_bound_stride != 4)
+    return topk_fail(FKL_ERR_INVALID_ARG, "max_bound_stride must be 0 (default), 1, 2 or 4");
   TopkPlan pl;
-  if (!make_topk_plan(T, d, V, K, &pl))
+  if (!make_topk_plan(T, d, V, K, &pl, max_bound_stride == 0 ? kMaxBoundStride : max_bound_stride))
     return topk_fail(FKL_ERR_INVALID_ARG,
                      "unsupported shape (need d % 8 == 0, 1 <= K <= V, and K <= 256 with K <= 8 * ceil(V / 256) "
                      "when V > 4096)");
@@ -300,22 +328,24 @@ extern "C" fkl_status fkl_teacher_topk(const uint16_t* Ht, const uint16_t* Wt, i
   if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(T) * 4, st) != cudaSuccess)
     return topk_fail(FKL_ERR_CUDA, "cudaMemsetAsync failed");
 
-  CUtensorMap mH, mW;
-  if (!encode_map_bf16(&mH, Ht, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, Wt, d, V, d * 2, 64, kVocabTile / 2))
+  CUtensorMap mH, mW, mWs;
+  if (!encode_map_bf16(&mH, Ht, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, Wt, d, V, d * 2, 64, kVocabTile / 2) ||
+      !encode_map_bf16(&mWs, Wt, d, pl.Vs, d * 2 * pl.stride, 64, kVocabTile / 2))
     return topk_fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const int pairs = sms / 2;
   const int m_tiles = static_cast<int>((T + 255) / 256), n_tiles = static_cast<int>((V + kVocabTile - 1) / kVocabTile);
   if (pl.bound_pass) {
-    const int ns = n_tiles < kMaxBoundSplits ? n_tiles : kMaxBoundSplits;
-    const GemmShape g = make_shape(T, V, d, kVocabTile, ns, status, 256);
+    const int s_tiles = static_cast<int>((pl.Vs + kVocabTile - 1) / kVocabTile);
+    const int ns = s_tiles < kMaxBoundSplits ? s_tiles : kMaxBoundSplits;
+    const GemmShape g = make_shape(T, pl.Vs, d, kVocabTile, ns, status, 256);
     TopRParams tp;
     tp.topr = topr;
     tp.T = static_cast<int>(T);
-    tp.V = static_cast<int>(V);
+    tp.V = static_cast<int>(pl.Vs);
     trace_launch_begin(st);
-    if (launch_gemm2_t<kVocabTile, false, false, EpiTopR>(mH, mW, g, tp, sms, st) != cudaSuccess)
+    if (launch_gemm2_t<kVocabTile, false, false, EpiTopR>(mH, mWs, g, tp, sms, st) != cudaSuccess)
       return topk_fail(FKL_ERR_CUDA, "bound-pass GEMM launch failed");
-    trace_launch_end(st, 5, 2.0 * T * V * d);
+    trace_launch_end(st, 5, 2.0 * T * pl.Vs * d);
     bound_kernel<<<static_cast<unsigned>((T + kBoundWarps - 1) / kBoundWarps), kBoundWarps * 32, 0, st>>>(
         topr, ns, T, static_cast<int>(K), theta);
   } else {

@@ -207,3 +207,9 @@ def test_options_struct_layout_matches_header(tmp_path):
     out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     assert out[0] == ctypes.sizeof(FklOptions)
     assert out[1:] == [getattr(FklOptions, f).offset for f in fields]
+
+
+def test_teacher_topk_stride_is_checked_on_host(L):
+    n = L.fkl_teacher_topk_workspace_size(64, 64, 8192, 16)
+    for bad in (3, 8, -1):
+        assert L.fkl_teacher_topk_ex(16, 16, 64, 64, 8192, 16, bad, 16, 16, 256, n, None) == INVALID

@@ -91,3 +91,28 @@ def test_cache_feeds_the_loss(fkl):
     loss, lse = fkl.forward(H.cuda(), W.cuda(), idx, val, None, 1.0, 64)
     ref = oracle.forward(oracle.to_f64(H), oracle.to_f64(W), idx.cpu(), val.cpu(), None, 1.0)
     assert abs(loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
+
+
+def test_teacher_whose_top_logits_avoid_the_sampled_rows(fkl):
+    # Every 4th vocabulary row (the rows the default first pass samples) is scaled down: its
+    # bound is loose, far more logits reach it than the buffer holds, and the overflow is
+    # reported; the exact first pass (max_bound_stride=1) gives the right cache.
+    Ht, Wt = teacher(96, 128, 20000, seed=9)
+    Wt[::4] = (Wt[::4].float() * 0.05).to(torch.bfloat16)
+    idx, val = fkl.teacher_topk(Ht.cuda(), Wt.cuda(), 100)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 10  # FKL_ERR_TOPK_OVERFLOW
+    idx, val = fkl.teacher_topk(Ht.cuda(), Wt.cuda(), 100, max_bound_stride=1)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 0
+    check_cache(Ht, Wt, 100, idx, val)
+
+
+@pytest.mark.parametrize("stride", [1, 2, 4])
+def test_every_bound_stride_gives_the_same_cache(fkl, stride):
+    Ht, Wt = teacher(200, 192, 30000, seed=10)
+    a = fkl.teacher_topk(Ht.cuda(), Wt.cuda(), 100, max_bound_stride=stride)
+    b = fkl.teacher_topk(Ht.cuda(), Wt.cuda(), 100, max_bound_stride=1)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 0
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
