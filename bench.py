@@ -268,6 +268,9 @@ def run_teacher_topk(args, world, rank, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = workloads.WORKLOADS[args.workload]
+    if args.vocab is not None or args.tokens is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_V{args.vocab or w.V}_T{args.tokens or w.T}",
+                                V=args.vocab or w.V, T=args.tokens or w.T)
     x = workloads.make_inputs(w)
     T, d, V, K = w.T, w.d, w.V, w.K
     Ht, Wt = x.H.to(dev), x.W.to(dev)

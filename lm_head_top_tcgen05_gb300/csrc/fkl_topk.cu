@@ -122,18 +122,33 @@ struct EpiCand {
     th = t < p.T ? p.theta[t] : INFINITY;
   }
 
-  __device__ __forceinline__ void chunk(const float (&v)[32], int col0) {
+  __device__ __forceinline__ bool hit(float x, int col) const { return x >= th && col < p.V; }
+
+  __device__ __forceinline__ int count(const float (&v)[32], int col0) const {
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c += hit(v[j], col0 + j) ? 1 : 0;
+    return c;
+  }
+
+  __device__ __forceinline__ void write(const float (&v)[32], int col0, int& pos) const {
+    int2* row = p.cand + static_cast<size_t>(t) * p.cap;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      if (v[j] >= th && col0 + j < p.V) {
-        const int pos = atomicAdd(&p.cnt[t], 1);
-        if (pos < p.cap) p.cand[static_cast<size_t>(t) * p.cap + pos] = make_int2(__float_as_int(v[j]), col0 + j);
+      if (hit(v[j], col0 + j)) {
+        if (pos < p.cap) row[pos] = make_int2(__float_as_int(v[j]), col0 + j);
+        ++pos;
       }
     }
   }
 
+  // Two passes over the tile's accumulator: count the row's candidates, claim their slots
+  // with one atomic per row, then read the accumulator again and write them.  One atomic
+  // round trip per tile instead of one per candidate column keeps the epilogue shorter than
+  // the tile's MMAs.  tcgen05.ld is warp-collective, so both passes run on the whole warp.
   template <int BN>
   __device__ __forceinline__ void tile(uint32_t taddr, int n, int) {
+    int total = 0;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; c += 2) {
       float v0[32], v1[32];
@@ -142,8 +157,22 @@ struct EpiCand {
       tmem_wait_ld();
       pin(v0);
       pin(v1);
-      chunk(v0, n * BN + c * 32);
-      chunk(v1, n * BN + c * 32 + 32);
+      total += count(v0, n * BN + c * 32) + count(v1, n * BN + c * 32 + 32);
+    }
+    if (!__any_sync(0xffffffffu, total > 0)) return;
+    int pos = total > 0 ? atomicAdd(&p.cnt[t], total) : 0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; c += 2) {
+      float v0[32], v1[32];
+      tmem_ld32(taddr + c * 32, v0);
+      tmem_ld32(taddr + c * 32 + 32, v1);
+      tmem_wait_ld();
+      pin(v0);
+      pin(v1);
+      if (total > 0) {
+        write(v0, n * BN + c * 32, pos);
+        write(v1, n * BN + c * 32 + 32, pos);
+      }
     }
   }
 
