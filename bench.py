@@ -213,8 +213,8 @@ def blas_threads():
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "7ff4a6baae3767f9"
-TRAFFIC_BYTES = {1: 3.005e9, 2: 2.589e9, 3: 2.768e9}
+TRAFFIC_SOURCES_SHA = "59db5024c832ce1c"
+TRAFFIC_BYTES = {1: 1.961e9, 2: 3.395e9, 3: 3.603e9}
 TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
 
 

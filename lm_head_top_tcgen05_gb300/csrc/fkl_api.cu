@@ -111,6 +111,7 @@ GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint3
   g.k_blocks = static_cast<int>(cdiv(Kd, 64));
   g.nsplit = nsplit;
   g.num_units = g.m_tiles * nsplit;
+  g.group_m = 1;
   g.a_box3d = 0;
   g.b_box3d = 0;
   g.status = status;
@@ -235,6 +236,15 @@ static fkl_status device_info(DevInfo* out) {
                 out->major, out->minor);
   return FKL_OK;
 }
+
+// Row blocks per group in the unit order of the products over the vocabulary (forward,
+// dS recompute, the teacher cache's passes): units run split-major within a group, so the
+// 76 pairs running together cover 19 row blocks of about 4 vocabulary splits and share
+// each W tile in L2.  At the 32K shapes this cut the forward's DRAM reads 4.4x (L2 hit
+// rate 72 % -> 91 %).  dW and dH keep row-major order, in which each A block is read once.
+constexpr int kGroupRows = 19;
+
+int group_rows(int m_tiles) { return kGroupRows < m_tiles ? kGroupRows : m_tiles; }
 
 // Tile width along d for the dW and dH products: the width with the least estimated time,
 // counting padded columns and the measured relative cost per column of each width on GB300
@@ -400,7 +410,8 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H or W");
     const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(V, kVocabTile);
     const int nsplit = plan_splits(m_tiles, n_tiles, di.sms / 2);
-    const GemmShape g = make_shape(T, V, d, kVocabTile, nsplit, &hdr->status, 256);
+    GemmShape g = make_shape(T, V, d, kVocabTile, nsplit, &hdr->status, 256);
+    g.group_m = group_rows(g.m_tiles);
     FwdParams fp;
     fp.pairs = pairs;
     fp.part = part;
@@ -505,7 +516,8 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
 
     // dS[:, slab] = g tau w_t (q - ptilde), recomputing S = H W_slab^T.
     const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(w, kVocabTile);
-    const GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
+    GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
+    g3.group_m = group_rows(g3.m_tiles);
     DsParams dp;
     dp.pairs = pairs; dp.lse = lse; dp.wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
     dp.arow = dv.kind != FKL_DIV_KL ? arow : nullptr;

@@ -38,10 +38,18 @@ __host__ __device__ constexpr size_t smem_bytes_for(int bn) {
   return static_cast<size_t>(stages_for(bn)) * (kBM * kBK * 2 + bn * kBK * 2) + 1024 + 256;
 }
 
+// Unit u -> (row block, vocabulary split).  Units are numbered in groups of group_m row
+// blocks; within a group the split varies slowest, so the pairs running at the same time
+// cover group_m row blocks of the same few splits and share their B tiles in L2.
 __device__ __forceinline__ void unit_range(const GemmShape& g, int u, int& m_blk, int& n_begin,
                                            int& n_end, int& split) {
-  m_blk = u / g.nsplit;
-  split = u - m_blk * g.nsplit;
+  const int per_group = g.group_m * g.nsplit;
+  const int grp = u / per_group;
+  const int r = u - grp * per_group;
+  const int m0 = grp * g.group_m;
+  const int rows = min(g.group_m, g.m_tiles - m0);
+  split = r / rows;
+  m_blk = m0 + (r - split * rows);
   n_begin = static_cast<int>(static_cast<long long>(split) * g.n_tiles / g.nsplit);
   n_end = static_cast<int>(static_cast<long long>(split + 1) * g.n_tiles / g.nsplit);
 }
@@ -482,8 +490,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Raises the kernel's dynamic shared-memory limit once per device (`done`: one array per
-// kernel instantiation), so that later launches, including launches recorded into a CUDA
+// Host-side launch state of one kernel instantiation, per device: whether its dynamic
+// shared-memory limit was raised, and how many clusters of it fit at once.  It lives in a
+// function with internal linkage, so every copy of this library (and every translation
+// unit) keeps its own: a static local of an externally visible template would be merged
+// across two copies of the library loaded into one process, and the second copy would then
+// skip raising the limit for its own kernels.
+template <class Key>
+struct LaunchState {
+  bool limit_set[128];
+  int clusters[128];
+};
+namespace {
+template <class Key>
+LaunchState<Key>& launch_state() {
+  static LaunchState<Key> s = {};
+  return s;
+}
+}  // namespace
+template <int Kind, int BN, bool A_MN, bool B_MN, class Epi>
+struct KernelKey {};
+
+// Raises the kernel's dynamic shared-memory limit once per device (`done`: the launch state
+// of this instantiation), so that later launches, including launches recorded into a CUDA
 // graph, make no attribute call.
 template <class Kern>
 cudaError_t smem_limit_once(Kern kern, size_t smem, bool (&done)[128]) {
@@ -502,8 +531,7 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const Gemm
                           const typename Epi::Params& ep, int grid, cudaStream_t st) {
   constexpr size_t SMEM = smem_bytes_for(BN);
   auto kern = gemm_kernel<BN, A_MN, B_MN, Epi>;
-  static bool limit_set[128] = {};  // one per instantiation of this template
-  cudaError_t e = smem_limit_once(kern, SMEM, limit_set);
+  cudaError_t e = smem_limit_once(kern, SMEM, launch_state<KernelKey<1, BN, A_MN, B_MN, Epi>>().limit_set);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, SMEM, st>>>(a, b, g, ep);
   return cudaGetLastError();

@@ -257,11 +257,10 @@ cudaError_t launch_gemm2_t(const CUtensorMap& a, const CUtensorMap& b, const Gem
                            const typename Epi::Params& ep, int sms, cudaStream_t st) {
   constexpr size_t SMEM = smem2_bytes_for(BN);
   auto kern = gemm2_kernel<BN, A_MN, B_MN, Epi>;
-  static bool limit_set[128] = {};  // per instantiation of this template, per device
-  static int cached[128] = {};
-  cudaError_t e = smem_limit_once(kern, SMEM, limit_set);
+  LaunchState<KernelKey<2, BN, A_MN, B_MN, Epi>>& state = launch_state<KernelKey<2, BN, A_MN, B_MN, Epi>>();
+  cudaError_t e = smem_limit_once(kern, SMEM, state.limit_set);
   if (e != cudaSuccess) return e;
-  const int clusters = max_pair_clusters(kern, SMEM, sms, cached);
+  const int clusters = max_pair_clusters(kern, SMEM, sms, state.clusters);
   const int n = g.num_units < clusters ? g.num_units : clusters;
   kern<<<2 * n, kThreads, SMEM, st>>>(a, b, g, ep);
   return cudaGetLastError();

@@ -98,13 +98,17 @@ cudaError_t launch_wait_timeout_test(uint32_t* status, uint64_t limit_ns, cudaSt
 struct GemmShape {
   int M, N, Kd;
   int m_tiles, n_tiles, k_blocks;
-  int nsplit;     // units per 128-row block
+  int nsplit;     // units per row block
   int num_units;  // m_tiles * nsplit
+  int group_m;    // row blocks per group: units run split-major within a group (1 = row-major)
   int a_box3d;    // MN-major A loaded by one 3-D box per tile (else 64-wide 2-D boxes)
   int b_box3d;    // same for B
   uint32_t* status;
   uint64_t limit_ns;
 };
+
+// Row blocks per group of the unit order for products over the vocabulary (see fkl_api.cu).
+int group_rows(int m_tiles);
 
 // rows_per_unit: 128 for the one-SM kernel, 256 for the two-SM (CTA pair) kernel.
 GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status,

@@ -366,7 +366,8 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
   if (pl.bound_pass) {
     const int s_tiles = static_cast<int>((pl.Vs + kVocabTile - 1) / kVocabTile);
     const int ns = s_tiles < kMaxBoundSplits ? s_tiles : kMaxBoundSplits;
-    const GemmShape g = make_shape(T, pl.Vs, d, kVocabTile, ns, status, 256);
+    GemmShape g = make_shape(T, pl.Vs, d, kVocabTile, ns, status, 256);
+    g.group_m = group_rows(g.m_tiles);
     TopRParams tp;
     tp.topr = topr;
     tp.T = static_cast<int>(T);
@@ -381,7 +382,8 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
     fill_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(theta, T, -INFINITY);
   }
   if (cudaGetLastError() != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "bound kernel launch failed");
-  const GemmShape g2 = make_shape(T, V, d, kVocabTile, plan_splits(m_tiles, n_tiles, pairs), status, 256);
+  GemmShape g2 = make_shape(T, V, d, kVocabTile, plan_splits(m_tiles, n_tiles, pairs), status, 256);
+  g2.group_m = group_rows(g2.m_tiles);
   CandParams cp;
   cp.theta = theta;
   cp.cnt = cnt;

@@ -125,3 +125,20 @@ def test_pair_ragged_last_tile(L, N, a_mn, b_mn):
 
 def test_pair_ragged_last_tile_accumulate(L):
     assert run_gemm(L, 264, 2880, 520, True, True, 256, accumulate=True, seed=13, pair=True) < 2e-5
+
+
+def test_two_copies_of_the_library_in_one_process(L, tmp_path):
+    # Each copy keeps its own per-kernel launch state (shared-memory limit, occupancy): the
+    # second copy must raise the limit for its own kernels, not inherit the first's flag.
+    import shutil
+
+    from lm_head_top_tcgen05_gb300 import _lib
+
+    assert run_gemm(L, 512, 512, 128, False, False, 256, pair=True) < 1e-5  # first copy, state set
+    dup = tmp_path / "libfkl_copy.so"
+    shutil.copy(_lib.LIB_PATH, dup)
+    L2 = ctypes.CDLL(str(dup))
+    for name, (res, args) in _lib._SIGNATURES.items():
+        fn = getattr(L2, name)
+        fn.restype, fn.argtypes = res, args
+    assert run_gemm(L2, 512, 512, 128, False, False, 256, pair=True) < 1e-5
