@@ -213,19 +213,25 @@ def blas_threads():
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "59db5024c832ce1c"
+TRAFFIC_SOURCES_SHA = "e7a3aa79a89c7529"
 TRAFFIC_BYTES = {1: 1.961e9, 2: 3.395e9, 3: 3.603e9}
 TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
 
 
+# The sources that define the loss's tensor-core GEMMs and how they are launched (tiles,
+# ring, epilogues, unit order, slab planning): the measured traffic above is valid while
+# these are unchanged.  The light kernels (prep, combine, weights), the teacher cache and the
+# trace do not enter.
+GEMM_SOURCES = ("fkl_api.cu", "fkl_gemm.cuh", "fkl_gemm2.cu", "fkl_gemm2.cuh", "fkl_internal.h", "fkl_ptx.cuh")
+
+
 def csrc_sha() -> str:
-    import glob
     import hashlib
 
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "lm_head_top_tcgen05_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for name in GEMM_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "lm_head_top_tcgen05_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 

@@ -31,62 +31,157 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 constexpr int kPrepWarps = 8;
+constexpr int kSortMaxK = 128;  // up to this K a row's pairs are sorted in registers
+
+// Teacher side of one row from its valid slots: log Z over the tempered logits (zz = z / tau,
+// -inf for ids outside [0, V)), then p_k = exp(zz_k - zmax - log Z) and c += p_k log p_k.
+__device__ __forceinline__ float teacher_p(float zz, bool valid, float zmax, float logZ, float& c) {
+  if (!valid || !(zz > -INFINITY)) return 0.f;
+  const float lp = (zz - zmax) - logZ;
+  const float pk = expf(lp);
+  c = fmaf(pk, lp, c);
+  return pk;
+}
+
+// Sorts 128 keys held 4 per lane (element i = e * 32 + lane in keys[e]) ascending: a bitonic
+// network, exchanging across lanes by shuffles for distances below 32 and inside the lane's
+// registers for 32 and 64.
+__device__ __forceinline__ void warp_sort128(unsigned long long (&keys)[4], int lane) {
+#pragma unroll
+  for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {
+        const int je = j >> 5;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e & je) continue;
+          const int e2 = e | je;
+          const bool asc = (((e << 5) | lane) & k) == 0;
+          const unsigned long long a = keys[e], b = keys[e2];
+          const unsigned long long lo = a < b ? a : b, hi = a < b ? b : a;
+          keys[e] = asc ? lo : hi;
+          keys[e2] = asc ? hi : lo;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, keys[e], j);
+          const bool asc = (((e << 5) | lane) & k) == 0;
+          const bool lower = (lane & j) == 0;
+          const unsigned long long a = keys[e];
+          keys[e] = (asc == lower) ? (a < o ? a : o) : (a < o ? o : a);
+        }
+      }
+    }
+  }
+}
 
 // One warp per token row.  The row's K ids and logits are read with coalesced loads
-// (consecutive lanes, consecutive slots); ids are staged in shared memory to rank them.
+// (consecutive lanes, consecutive slots).  The (id, slot) pairs are ordered by id, then
+// slot: for K <= 128 by a register bitonic sort of 64-bit keys (id << 32 | slot), otherwise
+// by ranking each pair against the row's ids staged in shared memory.  Both give the same
+// order.
 __global__ void __launch_bounds__(kPrepWarps * 32)
     prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ z, int64_t T, int K, int V,
                 float inv_tau, int2* __restrict__ pairs, int* __restrict__ slot, float* __restrict__ crow,
                 uint32_t* __restrict__ status) {
-  extern __shared__ int sid[];
+  extern __shared__ int sid[];  // [kPrepWarps][K]: p by slot (sort path) or ids (rank path)
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kPrepWarps + w;
   if (t >= T) return;  // uniform per warp
   int* my = sid + w * K;
   const int32_t* ri = idx + t * K;
   const float* rz = z + t * K;
-
   uint32_t bad = 0;
-  float zmax = -INFINITY;
-  for (int k = lane; k < K; k += 32) {
-    int id = ri[k];
-    if (id < 0 || id >= V) {
-      bad |= kStatusBadIdBit;
-      id = INT_MAX;  // never matches a column; sorts last
-    } else {
-      zmax = fmaxf(zmax, rz[k] * inv_tau);
-    }
-    my[k] = id;
-  }
-  zmax = warp_max(zmax);
-  const bool row_ok = zmax > -INFINITY;
-  float Z = 0.f;
-  if (row_ok) {
-    for (int k = lane; k < K; k += 32)
-      if (my[k] != INT_MAX) Z += expf(rz[k] * inv_tau - zmax);
-  }
-  Z = warp_sum(Z);
-  const float logZ = row_ok ? logf(Z) : 0.f;
-  __syncwarp();
   float c = 0.f;
-  for (int k = lane; k < K; k += 32) {
-    const int id = my[k];
-    float pk = 0.f;
-    if (row_ok && id != INT_MAX) {
-      const float zz = rz[k] * inv_tau;
-      if (zz > -INFINITY) {
-        const float lp = (zz - zmax) - logZ;
-        pk = expf(lp);
-        c = fmaf(pk, lp, c);
+  bool row_ok;
+
+  if (K <= kSortMaxK) {
+    int id[4];
+    float zz[4];
+    float zmax = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = (e << 5) | lane;
+      id[e] = INT_MAX;
+      zz[e] = -INFINITY;
+      if (k < K) {
+        const int v = ri[k];
+        if (v < 0 || v >= V) {
+          bad |= kStatusBadIdBit;  // INT_MAX never matches a column and sorts last
+        } else {
+          id[e] = v;
+          zz[e] = rz[k] * inv_tau;
+          zmax = fmaxf(zmax, zz[e]);
+        }
       }
     }
-    int rank = 0;  // position of (id, k) in the order by id, then slot
-    for (int j = 0; j < K; ++j) {
-      const int o = my[j];
-      rank += (o < id) || (o == id && j < k);
+    zmax = warp_max(zmax);
+    row_ok = zmax > -INFINITY;
+    float Z = 0.f;
+    if (row_ok) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (id[e] != INT_MAX) Z += expf(zz[e] - zmax);
     }
-    pairs[t * K + rank] = make_int2(id, __float_as_int(pk));
-    if (slot) slot[t * K + rank] = k;
+    Z = warp_sum(Z);
+    const float logZ = row_ok ? logf(Z) : 0.f;
+    float* sp = reinterpret_cast<float*>(my);
+    unsigned long long keys[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = (e << 5) | lane;
+      keys[e] = ~0ull;  // padding sorts after every slot
+      if (k < K) {
+        sp[k] = teacher_p(zz[e], row_ok && id[e] != INT_MAX, zmax, logZ, c);
+        keys[e] = (static_cast<unsigned long long>(static_cast<uint32_t>(id[e])) << 32) | static_cast<uint32_t>(k);
+      }
+    }
+    warp_sort128(keys, lane);
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = (e << 5) | lane;
+      if (i < K) {
+        const int k = static_cast<int>(keys[e] & 0xffffffffull);
+        pairs[t * K + i] = make_int2(static_cast<int>(keys[e] >> 32), __float_as_int(sp[k]));
+        if (slot) slot[t * K + i] = k;
+      }
+    }
+  } else {
+    float zmax = -INFINITY;
+    for (int k = lane; k < K; k += 32) {
+      int v = ri[k];
+      if (v < 0 || v >= V) {
+        bad |= kStatusBadIdBit;
+        v = INT_MAX;
+      } else {
+        zmax = fmaxf(zmax, rz[k] * inv_tau);
+      }
+      my[k] = v;
+    }
+    zmax = warp_max(zmax);
+    row_ok = zmax > -INFINITY;
+    float Z = 0.f;
+    if (row_ok) {
+      for (int k = lane; k < K; k += 32)
+        if (my[k] != INT_MAX) Z += expf(rz[k] * inv_tau - zmax);
+    }
+    Z = warp_sum(Z);
+    const float logZ = row_ok ? logf(Z) : 0.f;
+    __syncwarp();
+    for (int k = lane; k < K; k += 32) {
+      const int v = my[k];
+      const float pk = teacher_p(rz[k] * inv_tau, row_ok && v != INT_MAX, zmax, logZ, c);
+      int rank = 0;  // position of (id, k) in the order by id, then slot
+      for (int j = 0; j < K; ++j) {
+        const int o = my[j];
+        rank += (o < v) || (o == v && j < k);
+      }
+      pairs[t * K + rank] = make_int2(v, __float_as_int(pk));
+      if (slot) slot[t * K + rank] = k;
+    }
   }
   c = warp_sum(c);
   if (!row_ok) bad |= kStatusBadRowBit;
