@@ -128,16 +128,17 @@ typedef struct fkl_options {
 /*
  * Bytes of workspace that fkl_forward and fkl_backward need for this shape (one buffer
  * serves both; no state is carried between calls in it).  `chunk` bounds the backward's
- * dS buffer: it holds at most chunk * V bfloat16 values (rounded so that a vocabulary
- * slab is a whole number of 256-column tiles, and at least one tile wide).  The result
+ * dS buffer: it holds one block of the backward (a range of tokens x a vocabulary slab of
+ * whole 256-column tiles, at least one tile wide), at most chunk * V bfloat16 values.  The result
  * does not depend on `chunk` beyond floating-point summation order.  Returns 0 for
  * invalid shapes.
  */
 size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
 
 /*
- * Number of vocabulary slabs the backward pass walks for this shape: each slab is one
- * dS-recompute GEMM, one dW GEMM and one dH GEMM launch.  0 for T = 0 or invalid shapes.
+ * Number of blocks (token block x vocabulary slab) the backward pass walks for this shape:
+ * each is one dS-recompute GEMM, one dW GEMM and one dH GEMM launch.  0 for T = 0 or
+ * invalid shapes.
  */
 int64_t fkl_backward_slabs(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
 

@@ -37,6 +37,14 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
                          void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The backward's blocking for this shape (host only, no device call): out[0] = tokens per
+ * block Ct, out[1] = token blocks, out[2] = vocabulary columns per slab Vc, out[3] =
+ * vocabulary slabs.  The dS buffer of one block holds Ct x Vc bf16 values.  Returns
+ * FKL_ERR_INVALID_ARG for shapes fkl_workspace_size rejects.
+ */
+fkl_status fkl_test_backward_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, int64_t* out);
+
+/*
  * Runs one pipeline wait on a barrier that nothing completes, with a time limit of
  * limit_ns nanoseconds (at most one second), so that the bounded-wait path can be
  * checked without hanging the GPU: afterwards fkl_read_status(workspace, stream) must

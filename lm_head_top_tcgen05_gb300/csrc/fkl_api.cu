@@ -47,19 +47,43 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   p->T = T; p->d = d; p->V = V; p->K = K; p->chunk = chunk;
   const int64_t vpad = cdiv(V, kVocabTile) * kVocabTile;
   if (T == 0) {
+    p->Ct = 0;
+    p->nt = 0;
     p->Vc = kVocabTile;
     p->nslabs = 0;
   } else {
-    // The dS slab holds at most chunk * V values: slab width = chunk * V / T columns,
-    // rounded down to whole tiles (at least one), then evened out over the slabs.
-    const int64_t c = chunk < T ? chunk : T;
-    int64_t vc = (c * V) / T;
-    vc = (vc / kVocabTile) * kVocabTile;
-    if (vc < kVocabTile) vc = kVocabTile;
-    if (vc > vpad) vc = vpad;
-    const int64_t ns = cdiv(V, vc);
-    const int64_t even = cdiv(cdiv(V, ns), kVocabTile) * kVocabTile;
-    p->Vc = even < vc ? even : vc;
+    // The backward walks blocks of Ct tokens x Vc vocabulary columns; the dS buffer of one
+    // block holds at most chunk * V values (Vc whole 256-column tiles, at least one, evened
+    // out over the slabs).  dH is rewritten once per vocabulary slab and dW once per token
+    // block; full-height slabs (Ct = T) write dW once, and lower blocks are taken only when
+    // they cut that read-modify-write traffic by a quarter or more (long sequences).
+    const int64_t budget = (chunk < T ? chunk : T) * V;
+    auto width = [&](int64_t ct) {
+      int64_t vc = budget / ct;
+      vc = (vc / kVocabTile) * kVocabTile;
+      if (vc < kVocabTile) vc = kVocabTile;
+      if (vc > vpad) vc = vpad;
+      const int64_t ns = cdiv(V, vc);
+      const int64_t even = cdiv(cdiv(V, ns), kVocabTile) * kVocabTile;
+      return even < vc ? even : vc;
+    };
+    auto rmw = [&](int64_t nt, int64_t ns) {  // bytes of dH and dW traffic
+      return static_cast<double>(2 * ns - 1) * T * d * 4 + static_cast<double>(2 * nt - 1) * V * d * 4;
+    };
+    int64_t best_ct = T, best_vc = width(T);
+    const double full = rmw(1, cdiv(V, best_vc));
+    double best = full;
+    for (int64_t n = 2; n <= kMaxTokenBlocks; ++n) {
+      const int64_t ct = cdiv(cdiv(T, n), kVocabTile) * kVocabTile;
+      if (ct >= T) continue;
+      const int64_t vc = width(ct);
+      const double c = rmw(cdiv(T, ct), cdiv(V, vc));
+      if (c < best) { best = c; best_ct = ct; best_vc = vc; }
+    }
+    if (best > 0.75 * full) { best_ct = T; best_vc = width(T); }
+    p->Ct = best_ct;
+    p->nt = cdiv(T, best_ct);
+    p->Vc = best_vc;
     p->nslabs = cdiv(V, p->Vc);
   }
   p->nb = cdiv(T, 256);
@@ -72,7 +96,7 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   const size_t nbb = static_cast<size_t>(p->nb > 0 ? p->nb : 1);
   p->off_bsum = off;  off = align_up(off + nbb * 8, 256);
   p->off_bcnt = off;  off = align_up(off + nbb * 4, 256);
-  p->off_ds = off;    off = align_up(off + static_cast<size_t>(T) * p->Vc * 2, 256);
+  p->off_ds = off;    off = align_up(off + static_cast<size_t>(p->Ct) * p->Vc * 2, 256);
   p->off_slot = off;  off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
   p->off_sg = off;    off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
   p->off_arow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
@@ -338,7 +362,7 @@ size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t ch
 
 int64_t fkl_backward_slabs(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk) {
   Plan p;
-  return make_plan(T, d, V, K, chunk, &p) ? p.nslabs : 0;
+  return make_plan(T, d, V, K, chunk, &p) ? p.nt * p.nslabs : 0;
 }
 
 const char* fkl_last_error(void) { return g_last_error.c_str(); }
@@ -492,65 +516,73 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
     return cuda_fail(e, "divergence kernel");
 
   // All three products use two-SM tiles (256 rows per CTA pair, B split between the CTAs).
+  // Blocks of Ct tokens x Vc vocabulary columns, token blocks outer: dW of a slab
+  // accumulates over the token blocks and dH of a token block over the slabs, both in a
+  // fixed order (deterministic).
   const int bnd = choose_bn_d(d, true);
-  CUtensorMap mH_k, mH_mn;
-  if (!encode_map_bf16(&mH_k, H, d, T, d * 2, 64, 128)) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
-  bool h3d = false;
-  if (!encode_b_mn_pair(&mH_mn, H, d, T, d * 2, bnd, true, &h3d))
-    return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H");
   const int64_t Vc = pl.Vc;
-  for (int64_t j = 0; j < pl.nslabs; ++j) {
-    const int64_t v0 = j * Vc;
-    const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
-    const uint16_t* Wj = W + v0 * d;
-    CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
-    // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
-    // 3-D view may span round_up(w, 64) columns.
-    bool w3d = false;
-    const bool wmap = encode_b_mn_pair(&mW_mn, Wj, d, w, d * 2, bnd, true, &w3d);
-    const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, T, Vc * 2, 128);
-    if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) || !wmap ||
-        (!d3d && !encode_map_bf16(&mD_mn, ds, w, T, Vc * 2, 64, 64)) ||
-        !encode_map_bf16(&mD_k, ds, w, T, Vc * 2, 64, 128))
-      return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for slab %lld", (long long)j);
+  const float* wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
+  for (int64_t b = 0; b < pl.nt; ++b) {
+    const int64_t r0 = b * pl.Ct;
+    const int64_t rows = (T - r0) < pl.Ct ? (T - r0) : pl.Ct;
+    const uint16_t* Hb = H + r0 * d;
+    CUtensorMap mH_k, mH_mn;
+    bool h3d = false;
+    if (!encode_map_bf16(&mH_k, Hb, d, rows, d * 2, 64, 128) || !encode_b_mn_pair(&mH_mn, Hb, d, rows, d * 2, bnd, true, &h3d))
+      return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H block %lld", (long long)b);
+    for (int64_t j = 0; j < pl.nslabs; ++j) {
+      const int64_t v0 = j * Vc;
+      const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
+      const uint16_t* Wj = W + v0 * d;
+      CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
+      // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
+      // 3-D view may span round_up(w, 64) columns.
+      bool w3d = false;
+      const bool wmap = encode_b_mn_pair(&mW_mn, Wj, d, w, d * 2, bnd, true, &w3d);
+      const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, rows, Vc * 2, 128);
+      if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) || !wmap ||
+          (!d3d && !encode_map_bf16(&mD_mn, ds, w, rows, Vc * 2, 64, 64)) ||
+          !encode_map_bf16(&mD_k, ds, w, rows, Vc * 2, 64, 128))
+        return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for block (%lld, %lld)", (long long)b, (long long)j);
 
-    // dS[:, slab] = g tau w_t (q - ptilde), recomputing S = H W_slab^T.
-    const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(w, kVocabTile);
-    GemmShape g3 = make_shape(T, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
-    g3.group_m = group_rows(g3.m_tiles);
-    DsParams dp;
-    dp.pairs = pairs; dp.lse = lse; dp.wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
-    dp.arow = dv.kind != FKL_DIV_KL ? arow : nullptr;
-    dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
-    dp.T = (int)T; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
-    dp.scale2 = 1.4426950408889634f / tau;
-    const double slab_flops = 2.0 * T * w * d;
-    trace_launch_begin(st);
-    if ((e = launch_gemm2_ds(mH_k, mW_k, g3, dp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "dS GEMM");
-    trace_launch_end(st, 1, slab_flops);
+      // dS[block] = g tau w_t (q - ptilde), recomputing S = H_block W_slab^T.
+      const int m_tiles = (int)cdiv(rows, 256), n_tiles = (int)cdiv(w, kVocabTile);
+      GemmShape g3 = make_shape(rows, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
+      g3.group_m = group_rows(g3.m_tiles);
+      DsParams dp;
+      dp.pairs = pairs + r0 * K; dp.lse = lse + r0; dp.wrow = wrow + r0;
+      dp.arow = dv.kind != FKL_DIV_KL ? arow + r0 : nullptr;
+      dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
+      dp.T = (int)rows; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
+      dp.scale2 = 1.4426950408889634f / tau;
+      const double block_flops = 2.0 * rows * w * d;
+      trace_launch_begin(st);
+      if ((e = launch_gemm2_ds(mH_k, mW_k, g3, dp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "dS GEMM");
+      trace_launch_end(st, 1, block_flops);
 
-    // dW[slab] = dS[:, slab]^T H  (complete for this slab: plain store).
-    GemmShape g4 = make_shape(w, d, T, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
-    g4.a_box3d = d3d ? 1 : 0;
-    g4.b_box3d = h3d ? 1 : 0;
-    F32Params p4;
-    p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
-    p4.accumulate = (accum & FKL_ACCUMULATE_DW) ? 1 : 0; p4.vec_ok = 1;
-    trace_launch_begin(st);
-    if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
-      return cuda_fail(e, "dW GEMM");
-    trace_launch_end(st, 2, slab_flops);
+      // dW[slab] (+)= dS[block]^T H_block  (token blocks in order).
+      GemmShape g4 = make_shape(w, d, rows, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
+      g4.a_box3d = d3d ? 1 : 0;
+      g4.b_box3d = h3d ? 1 : 0;
+      F32Params p4;
+      p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
+      p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0; p4.vec_ok = 1;
+      trace_launch_begin(st);
+      if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
+        return cuda_fail(e, "dW GEMM");
+      trace_launch_end(st, 2, block_flops);
 
-    // dH (+)= dS[:, slab] W[slab]  (slabs in order: deterministic accumulation).
-    GemmShape g5 = make_shape(T, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
-    g5.b_box3d = w3d ? 1 : 0;
-    F32Params p5;
-    p5.out = dH; p5.ldo = d; p5.M = (int)T; p5.N = (int)d;
-    p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = 1;
-    trace_launch_begin(st);
-    if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
-      return cuda_fail(e, "dH GEMM");
-    trace_launch_end(st, 3, slab_flops);
+      // dH[block] (+)= dS[block] W[slab]  (slabs in order).
+      GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
+      g5.b_box3d = w3d ? 1 : 0;
+      F32Params p5;
+      p5.out = dH + r0 * d; p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
+      p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = 1;
+      trace_launch_begin(st);
+      if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
+        return cuda_fail(e, "dH GEMM");
+      trace_launch_end(st, 3, block_flops);
+    }
   }
   if ((e = launch_poison(dH, T * d, dW, V * d, &hdr->status, di.sms, st)) != cudaSuccess)
     return cuda_fail(e, "poison kernel");
@@ -622,6 +654,18 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
            : launch_gemm_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p,
                              g.num_units < di.sms ? g.num_units : di.sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "test GEMM");
+  return FKL_OK;
+}
+
+fkl_status fkl_test_backward_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, int64_t* out) {
+  g_last_error.clear();
+  if (out == nullptr) return fail(FKL_ERR_INVALID_ARG, "out is NULL");
+  Plan pl;
+  if (!make_plan(T, d, V, K, chunk, &pl)) return fail(FKL_ERR_INVALID_ARG, "unsupported shape");
+  out[0] = pl.Ct;
+  out[1] = pl.nt;
+  out[2] = pl.Vc;
+  out[3] = pl.nslabs;
   return FKL_OK;
 }
 

@@ -26,13 +26,16 @@ struct WsHeader {
 
 constexpr int kVocabTile = 256;                   // tile width of the vocabulary axis
 constexpr int kMaxSplit = 32;                     // most vocabulary splits per row block
+constexpr int64_t kMaxTokenBlocks = 64;           // most token blocks of the backward
 constexpr uint64_t kWaitLimitNs = 5000000000ull;  // per pipeline wait
 
 // Where each buffer lives inside the caller's workspace, and the backward's slabbing.
 struct Plan {
   int64_t T, d, V, K, chunk;
+  int64_t Ct;      // tokens per backward block (T, or a multiple of 256 below it)
+  int64_t nt;      // token blocks of the backward
   int64_t Vc;      // vocabulary columns per backward slab (multiple of kVocabTile)
-  int64_t nslabs;  // number of backward slabs
+  int64_t nslabs;  // vocabulary slabs of the backward
   int64_t nb;      // row blocks of the combine step (256 rows each)
   size_t off_pairs, off_crow, off_wrow, off_scnt, off_part, off_bsum, off_bcnt, off_ds;
   size_t off_slot;  // int32 [T][K]: original slot of each sorted pair

@@ -213,3 +213,36 @@ def test_teacher_topk_stride_is_checked_on_host(L):
     n = L.fkl_teacher_topk_workspace_size(64, 64, 8192, 16)
     for bad in (3, 8, -1):
         assert L.fkl_teacher_topk_ex(16, 16, 64, 64, 8192, 16, bad, 16, 16, 256, n, None) == INVALID
+
+
+def _plan(L, T, d, V, K, chunk):
+    out = (ctypes.c_int64 * 4)()
+    assert L.fkl_test_backward_plan(T, d, V, K, chunk, out) == 0
+    return tuple(out)
+
+
+@pytest.mark.parametrize("T,d,V,K,chunk", [(32768, 2880, 201088, 100, 2048), (262144, 2880, 201088, 100, 4096),
+                                           (65536, 4096, 151936, 100, 4096), (8192, 3072, 128256, 100, 1024),
+                                           (4000, 64, 2999, 16, 512), (300, 200, 5000, 16, 128), (1, 64, 777, 8, 1)])
+def test_backward_blocks_respect_the_chunk_bound(L, T, d, V, K, chunk):
+    Ct, nt, Vc, ns = _plan(L, T, d, V, K, chunk)
+    assert Vc % 256 == 0 and Vc >= 256 and ns * Vc >= V and (ns - 1) * Vc < V
+    assert nt * Ct >= T and (nt - 1) * Ct < T
+    assert Ct == T or Ct % 256 == 0
+    # the dS buffer of one block: at most chunk * V values, or one 256-wide tile of Ct rows
+    assert Ct * Vc <= max(min(chunk, T) * V, Ct * 256)
+    assert L.fkl_backward_slabs(T, d, V, K, chunk) == nt * ns
+
+
+def test_backward_block_choice(L):
+    # 32K: full-height slabs (dW written once); 256K and long sequences: lower blocks cut the
+    # read-modify-write of dH, which otherwise grows with the number of narrow slabs
+    assert _plan(L, 32768, 2880, 201088, 100, 2048)[1] == 1
+    Ct, nt, Vc, ns = _plan(L, 262144, 2880, 201088, 100, 4096)
+    assert nt > 1 and Ct < 262144
+
+    def rmw(T, d, V, nt, ns):
+        return (2 * ns - 1) * T * d * 4 + (2 * nt - 1) * V * d * 4
+
+    assert rmw(262144, 2880, 201088, nt, ns) < 0.3 * rmw(262144, 2880, 201088, 1, 66)
+    assert _plan(L, 4000, 64, 2999, 16, 512)[1] > 1

@@ -63,6 +63,12 @@ def test_divergence_parity(fkl, kind, param):
     assert_s_close(gpu["s_ids"], ref["s_ids"])
 
 
+def test_divergence_token_blocks(fkl):
+    # 4 token blocks x 3 vocabulary slabs in the backward (a long sequence, small vocabulary)
+    x = workloads.make_random(4000, 64, 2999, 16, tau=1.2, chunk=512, seed=59, mask_frac=0.1)
+    assert_parity(run_gpu(fkl, x, "skew_rkl", 0.2), run_oracle(x, "skew_rkl", 0.2))
+
+
 @pytest.mark.parametrize("kind,param", [("jsd", 0.5), ("tv", None)])
 def test_divergence_parity_wide_shape(fkl, kind, param):
     # several 256-row blocks and vocabulary slabs, ragged on every axis

@@ -152,3 +152,28 @@ def test_long_context_256k(fkl):
     dH_ref = oracle.dH_rows(H64, W64, sub.topk_idx, sub.topk_logits, None, w.tau, np.arange(len(rows)),
                             grad=len(rows) / w.T)
     close_rows(gpu["dH"].numpy()[rows].astype(np.float64), dH_ref, "dH rows")
+
+
+def test_long_context_256k_dw_identities(fkl):
+    # 256K tokens: the backward runs in token blocks x vocabulary slabs, dW accumulating over
+    # the token blocks.  dW is checked through identities that hold at any size:
+    # sum_v dW_v = 0 (every valid row of dS sums to zero) and sum_t dH_t . H_t = sum_v dW_v . W_v.
+    w = workloads.WORKLOADS["gptoss20b_256k"]
+    x = workloads.make_inputs(w)
+    gpu = run_gpu(fkl, x)
+    assert gpu["status"] == 0
+    dH, dW = gpu["dH"], gpu["dW"]
+    lhs = rhs = scale = 0.0
+    for i in range(0, w.T, 16384):
+        a, h = dH[i:i + 16384].double(), x.H[i:i + 16384].double()
+        lhs += float((a * h).sum())
+        scale += float((a.abs() * h.abs()).sum())
+    colsum = torch.zeros(w.d, dtype=torch.float64)
+    colabs = torch.zeros(w.d, dtype=torch.float64)
+    for i in range(0, w.V, 16384):
+        g = dW[i:i + 16384].double()
+        rhs += float((g * x.W[i:i + 16384].double()).sum())
+        colsum += g.sum(0)
+        colabs += g.abs().sum(0)
+    assert abs(lhs - rhs) <= 1e-3 * scale, (lhs, rhs, scale)
+    assert colsum.abs().max().item() <= 1e-3 * colabs.max().item()

@@ -89,6 +89,9 @@ CASES = {
     "cold_tau": (200, 128, 3000, 16, 0.05, 256, 0.0, 10),
     "hot_tau": (200, 128, 3000, 16, 20.0, 256, 0.0, 11),
     "vocab_below_one_tile": (300, 96, 100, 20, 1.0, 64, 0.0, 12),
+    # long sequence against a small vocabulary: the backward walks 4 token blocks x 3 slabs
+    # (dW accumulates over the token blocks), the last block and slab ragged
+    "token_blocks": (4000, 64, 2999, 16, 1.0, 512, 0.1, 13),
 }
 
 
@@ -263,5 +266,24 @@ def test_gradient_accumulation(fkl):
     fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, out=(dH, dW), accumulate=True)
     torch.cuda.synchronize()
     ref = run_oracle(x, grad=2.0)  # two micro-batches of the same gradient
+    assert_grad_close((dH - dH0).double().cpu().numpy(), ref["dH"], "accumulated dH")
+    assert_grad_close((dW - dW0).double().cpu().numpy(), ref["dW"], "accumulated dW")
+
+
+def test_token_blocks_with_variants(fkl):
+    # the blocked backward with the sequence mean and with accumulation into given gradients
+    x = workloads.make_random(4000, 64, 2999, 16, tau=1.5, chunk=512, seed=44, mask_frac=0.1)
+    seq = np.repeat(np.arange(5), 800).astype(np.int32)
+    H, W, idx, z, m = to_dev(x)
+    sid = torch.from_numpy(seq).cuda()
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk, seq_ids=sid, num_seqs=5)
+    g = torch.Generator(device="cuda").manual_seed(1)
+    dH0 = torch.randn(H.shape, device="cuda", generator=g)
+    dW0 = torch.randn(W.shape, device="cuda", generator=g)
+    dH, dW = dH0.clone(), dW0.clone()
+    fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, out=(dH, dW), accumulate=True, seq_ids=sid, num_seqs=5)
+    torch.cuda.synchronize()
+    ref = run_oracle_seq(x, seq)
+    assert abs(loss.item() - ref["loss"]) <= LOSS_RTOL * abs(ref["loss"])
     assert_grad_close((dH - dH0).double().cpu().numpy(), ref["dH"], "accumulated dH")
     assert_grad_close((dW - dW0).double().cpu().numpy(), ref["dW"], "accumulated dW")
