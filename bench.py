@@ -213,8 +213,8 @@ def blas_threads():
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "e7a3aa79a89c7529"
-TRAFFIC_BYTES = {1: 1.961e9, 2: 3.395e9, 3: 3.603e9}
+TRAFFIC_SOURCES_SHA = "85f25f350d7127f1"
+TRAFFIC_BYTES = {1: 1.908e9, 2: 2.644e9, 3: 2.734e9}
 TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
 
 
