@@ -213,26 +213,31 @@ def blas_threads():
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "85f25f350d7127f1"
+TRAFFIC_SOURCES_SHA = "5223c7bf718da5e3"
 TRAFFIC_BYTES = {1: 1.908e9, 2: 2.644e9, 3: 2.734e9}
 TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
 
 
 # The sources that define the loss's tensor-core GEMMs and how they are launched (tiles,
-# ring, epilogues, unit order, slab planning): the measured traffic above is valid while
-# these are unchanged.  The light kernels (prep, combine, weights), the teacher cache and the
+# ring, epilogues, unit order, block planning): the measured traffic above is valid while
+# their code (comments aside) is unchanged.  The light kernels (prep, combine, weights), the teacher cache and the
 # trace do not enter.
 GEMM_SOURCES = ("fkl_api.cu", "fkl_gemm.cuh", "fkl_gemm2.cu", "fkl_gemm2.cuh", "fkl_internal.h", "fkl_ptx.cuh")
 
 
 def csrc_sha() -> str:
+    """Hash of the GEMM sources' code: comments and whitespace do not enter."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "lm_head_top_tcgen05_gb300", "csrc", name), encoding="utf-8") as fh:
+            code = fh.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
         h.update(name.encode())
-        with open(os.path.join(ROOT, "lm_head_top_tcgen05_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,8 +22,9 @@
  *
  * where ptilde_t is p_t added at the ids of row t and g the upstream gradient of L.
  * N = 0 gives L = 0 and zero gradients.  No T x V tensor is ever written to memory:
- * logits live only in tensor memory, one tile at a time; the backward writes dS one
- * vocabulary slab at a time into the caller's workspace, bounded by `chunk` (below).
+ * logits live only in tensor memory, one tile at a time; the backward writes dS one block
+ * (a range of tokens x a vocabulary slab) at a time into the caller's workspace, bounded
+ * by `chunk` (below).
  *
  * Conventions for every entry point:
  *   - Device pointers are CUDA device memory of the current device; all buffers are

@@ -29,7 +29,7 @@ constexpr int kMaxSplit = 32;                     // most vocabulary splits per 
 constexpr int64_t kMaxTokenBlocks = 64;           // most token blocks of the backward
 constexpr uint64_t kWaitLimitNs = 5000000000ull;  // per pipeline wait
 
-// Where each buffer lives inside the caller's workspace, and the backward's slabbing.
+// Where each buffer lives inside the caller's workspace, and the backward's blocks.
 struct Plan {
   int64_t T, d, V, K, chunk;
   int64_t Ct;      // tokens per backward block (T, or a multiple of 256 below it)
@@ -126,8 +126,10 @@ struct FwdParams {
   float scale2;       // log2(e) / tau
 };
 
-// Backward recompute: dS = g tau w_t (a_t q - r) for one vocabulary slab, bf16, with r the
-// pairs' second field added at their ids (KL: a_t = 1, r = p, i.e. q - ptilde).
+// Backward recompute: dS = g tau w_t (a_t q - r) for one block (a range of T tokens x a
+// vocabulary slab of slab_w columns from v0), bf16, with r the pairs' second field added
+// at their ids (KL: a_t = 1, r = p, i.e. q - ptilde).  The per-token pointers start at the
+// block's first token.
 struct DsParams {
   const int2* pairs;
   const float* lse;
