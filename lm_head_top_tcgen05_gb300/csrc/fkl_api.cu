@@ -263,10 +263,13 @@ static fkl_status device_info(DevInfo* out) {
 
 // Row blocks per group in the unit order of the products over the vocabulary (forward,
 // dS recompute, the teacher cache's passes): units run split-major within a group, so the
-// 76 pairs running together cover 19 row blocks of about 4 vocabulary splits and share
-// each W tile in L2.  At the 32K shapes this cut the forward's DRAM reads 4.4x (L2 hit
-// rate 72 % -> 91 %).  dW and dH keep row-major order, in which each A block is read once.
-constexpr int kGroupRows = 19;
+// 76 pairs running together cover 38 row blocks of about 2 vocabulary splits and share
+// each W tile in L2.  Against row-major order (about 6 row blocks per W tile) this cut the
+// forward's DRAM reads 4.4x at the 32K shapes.  In same-process A/Bs, 38 beat 19 by 0.9 %
+// per step at 32K and 1.5 % at 256K (forward 6 % faster there), and 76 was 7-8 % slower
+// than 38 (76 row blocks of H no longer stay in L2).  dW and dH keep row-major order, in
+// which each A block is read once.
+constexpr int kGroupRows = 38;
 
 int group_rows(int m_tiles) { return kGroupRows < m_tiles ? kGroupRows : m_tiles; }
 
