@@ -213,8 +213,8 @@ def blas_threads():
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
 # of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "5223c7bf718da5e3"
-TRAFFIC_BYTES = {1: 1.908e9, 2: 2.644e9, 3: 2.734e9}
+TRAFFIC_SOURCES_SHA = "577e2c0676a68c18"
+TRAFFIC_BYTES = {1: 1.911e9, 2: 2.526e9, 3: 2.684e9}
 TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
 
 
