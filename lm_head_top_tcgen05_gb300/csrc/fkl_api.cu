@@ -104,24 +104,32 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   return true;
 }
 
-int plan_splits(int m_tiles, int n_tiles, int sms) {
+int plan_splits(int m_tiles, int n_tiles, int sms, int group) {
   // Pick the number of vocabulary splits per row block that minimises the critical path
   // (waves of units x tiles per unit).  At least sms/32 splits keep the row blocks in
-  // flight at once (each re-read from L2 for every tile of its unit) to a few dozen.
+  // flight at once (each re-read from L2 for every tile of its unit) to a few dozen.  With
+  // units in groups of `group` row blocks, a count within 1 % of the best that makes a
+  // group a whole number of waves is preferred: no wave then straddles two groups, which
+  // would double the row blocks of A held in L2 (measured on the 32K forward, 16 or 10
+  // splits instead of 13: 1.2-1.3 % faster).
   int lo = (sms + 31) / 32;
   if (lo > n_tiles) lo = n_tiles;
   if (lo < 1) lo = 1;
   int hi = n_tiles < kMaxSplit ? n_tiles : kMaxSplit;
-  int best = lo;
-  int64_t best_cost = INT64_MAX;
-  for (int s = lo; s <= hi; ++s) {
+  auto cost = [&](int s) {
     const int64_t units = static_cast<int64_t>(m_tiles) * s;
-    const int64_t waves = cdiv(units, sms);
-    const int64_t per_unit = cdiv(n_tiles, s);
-    const int64_t cost = waves * per_unit;
-    if (cost < best_cost) { best_cost = cost; best = s; }
-  }
-  return best;
+    return cdiv(units, sms) * cdiv(n_tiles, s);
+  };
+  int best = lo;
+  for (int s = lo; s <= hi; ++s)
+    if (cost(s) < cost(best)) best = s;
+  const int64_t rows = group < m_tiles ? group : m_tiles;
+  if (rows <= 1 || (rows * best) % sms == 0) return best;
+  int aligned = 0;
+  for (int s = lo; s <= hi; ++s)
+    if ((rows * s) % sms == 0 && 100 * cost(s) <= 101 * cost(best) && (aligned == 0 || cost(s) < cost(aligned)))
+      aligned = s;
+  return aligned ? aligned : best;
 }
 
 GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status,
@@ -436,7 +444,7 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
     if (!encode_map_bf16(&mH, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, W, d, V, d * 2, 64, kVocabTile / 2))
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H or W");
     const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(V, kVocabTile);
-    const int nsplit = plan_splits(m_tiles, n_tiles, di.sms / 2);
+    const int nsplit = plan_splits(m_tiles, n_tiles, di.sms / 2, group_rows(m_tiles));
     GemmShape g = make_shape(T, V, d, kVocabTile, nsplit, &hdr->status, 256);
     g.group_m = group_rows(g.m_tiles);
     FwdParams fp;
@@ -550,7 +558,8 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
 
       // dS[block] = g tau w_t (q - ptilde), recomputing S = H_block W_slab^T.
       const int m_tiles = (int)cdiv(rows, 256), n_tiles = (int)cdiv(w, kVocabTile);
-      GemmShape g3 = make_shape(rows, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
+      GemmShape g3 = make_shape(rows, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2, group_rows(m_tiles)),
+                                &hdr->status, 256);
       g3.group_m = group_rows(g3.m_tiles);
       DsParams dp;
       dp.pairs = pairs + r0 * K; dp.lse = lse + r0; dp.wrow = wrow + r0;

@@ -61,7 +61,8 @@ void trace_launch_end(cudaStream_t st, int kind, double flops);
 bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p);
 
 // Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.
-int plan_splits(int m_tiles, int n_tiles, int sms);
+// group: row blocks per group of the unit order (1 = row-major).
+int plan_splits(int m_tiles, int n_tiles, int sms, int group = 1);
 
 // ---------------------------------------------------------------- small kernels
 cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t T, int K, int V, float tau,

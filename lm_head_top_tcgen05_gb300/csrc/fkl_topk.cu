@@ -382,7 +382,7 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
     fill_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(theta, T, -INFINITY);
   }
   if (cudaGetLastError() != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "bound kernel launch failed");
-  GemmShape g2 = make_shape(T, V, d, kVocabTile, plan_splits(m_tiles, n_tiles, pairs), status, 256);
+  GemmShape g2 = make_shape(T, V, d, kVocabTile, plan_splits(m_tiles, n_tiles, pairs, group_rows(m_tiles)), status, 256);
   g2.group_m = group_rows(g2.m_tiles);
   CandParams cp;
   cp.theta = theta;
