@@ -452,7 +452,7 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
     fp.part = part;
     fp.sg = record_s ? sg : nullptr;
     fp.T = (int)T; fp.K = (int)K; fp.V = (int)V; fp.nsplit = nsplit;
-    fp.scale2 = 1.4426950408889634f / tau;
+    fp.scale2 = kLog2e / tau;
     trace_launch_begin(st);
     if ((e = launch_gemm2_fwd(mH, mW, g, fp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "forward GEMM");
     trace_launch_end(st, 0, 2.0 * T * V * d);
@@ -467,6 +467,89 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
   } else {
     if ((e = launch_combine(part, 1, crow, wrow, 0, tau, lse, bsum, bcnt, 0, hdr, loss, st)) != cudaSuccess)
       return cuda_fail(e, "combine kernels");
+  }
+  return FKL_OK;
+}
+
+// The backward's GEMMs, after the light kernels have prepared the pairs, the token weights
+// and the scales in the workspace.  All three products use two-SM tiles (256 rows per CTA
+// pair, B split between the CTAs) over blocks of Ct tokens x Vc vocabulary columns, token
+// blocks outer: dW of a slab accumulates over the token blocks and dH of a token block over
+// the slabs, both in a fixed order (deterministic).
+static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const uint16_t* H, const uint16_t* W,
+                                      const float* lse, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
+                                      const DivSpec& dv, int accum, uint8_t* ws, float* dH, float* dW,
+                                      cudaStream_t st) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const int2* pairs = reinterpret_cast<const int2*>(ws + pl.off_pairs);
+  const float* arow = reinterpret_cast<const float*>(ws + pl.off_arow);
+  uint16_t* ds = reinterpret_cast<uint16_t*>(ws + pl.off_ds);
+  cudaError_t e;
+  const int bnd = choose_bn_d(d, true);
+  const int64_t Vc = pl.Vc;
+  const float* wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
+  for (int64_t b = 0; b < pl.nt; ++b) {
+    const int64_t r0 = b * pl.Ct;
+    const int64_t rows = (T - r0) < pl.Ct ? (T - r0) : pl.Ct;
+    const uint16_t* Hb = H + r0 * d;
+    CUtensorMap mH_k, mH_mn;
+    bool h3d = false;
+    if (!encode_map_bf16(&mH_k, Hb, d, rows, d * 2, 64, 128) || !encode_b_mn_pair(&mH_mn, Hb, d, rows, d * 2, bnd, true, &h3d))
+      return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H block %lld", (long long)b);
+    for (int64_t j = 0; j < pl.nslabs; ++j) {
+      const int64_t v0 = j * Vc;
+      const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
+      const uint16_t* Wj = W + v0 * d;
+      CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
+      // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
+      // 3-D view may span round_up(w, 64) columns.
+      bool w3d = false;
+      const bool wmap = encode_b_mn_pair(&mW_mn, Wj, d, w, d * 2, bnd, true, &w3d);
+      const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, rows, Vc * 2, 128);
+      if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) || !wmap ||
+          (!d3d && !encode_map_bf16(&mD_mn, ds, w, rows, Vc * 2, 64, 64)) ||
+          !encode_map_bf16(&mD_k, ds, w, rows, Vc * 2, 64, 128))
+        return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for block (%lld, %lld)", (long long)b, (long long)j);
+
+      // dS[block] = g tau w_t (q - ptilde), recomputing S = H_block W_slab^T.
+      const int m_tiles = (int)cdiv(rows, 256), n_tiles = (int)cdiv(w, kVocabTile);
+      GemmShape g3 = make_shape(rows, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2, group_rows(m_tiles)),
+                                &hdr->status, 256);
+      g3.group_m = group_rows(g3.m_tiles);
+      DsParams dp;
+      dp.pairs = pairs + r0 * K; dp.lse = lse + r0; dp.wrow = wrow + r0;
+      dp.arow = dv.kind != FKL_DIV_KL ? arow + r0 : nullptr;
+      dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
+      dp.T = (int)rows; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
+      dp.scale2 = kLog2e / tau;
+      const double block_flops = 2.0 * rows * w * d;
+      trace_launch_begin(st);
+      if ((e = launch_gemm2_ds(mH_k, mW_k, g3, dp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "dS GEMM");
+      trace_launch_end(st, 1, block_flops);
+
+      // dW[slab] (+)= dS[block]^T H_block  (token blocks in order).
+      GemmShape g4 = make_shape(w, d, rows, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
+      g4.a_box3d = d3d ? 1 : 0;
+      g4.b_box3d = h3d ? 1 : 0;
+      F32Params p4;
+      p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
+      p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0; p4.vec_ok = 1;
+      trace_launch_begin(st);
+      if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
+        return cuda_fail(e, "dW GEMM");
+      trace_launch_end(st, 2, block_flops);
+
+      // dH[block] (+)= dS[block] W[slab]  (slabs in order).
+      GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
+      g5.b_box3d = w3d ? 1 : 0;
+      F32Params p5;
+      p5.out = dH + r0 * d; p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
+      p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = 1;
+      trace_launch_begin(st);
+      if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
+        return cuda_fail(e, "dH GEMM");
+      trace_launch_end(st, 3, block_flops);
+    }
   }
   return FKL_OK;
 }
@@ -513,8 +596,6 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
   }
   int2* pairs = reinterpret_cast<int2*>(ws + pl.off_pairs);
   float* crow = reinterpret_cast<float*>(ws + pl.off_crow);
-  uint16_t* ds = reinterpret_cast<uint16_t*>(ws + pl.off_ds);
-
   int* slot = reinterpret_cast<int*>(ws + pl.off_slot);
   float* arow = reinterpret_cast<float*>(ws + pl.off_arow);
   if ((e = launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, slot, crow, &hdr->status, st)) !=
@@ -526,76 +607,7 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
       (e = launch_div_coef(dv, pairs, slot, opts->student_topk_logits, lse, T, (int)K, tau, arow, st)) != cudaSuccess)
     return cuda_fail(e, "divergence kernel");
 
-  // All three products use two-SM tiles (256 rows per CTA pair, B split between the CTAs).
-  // Blocks of Ct tokens x Vc vocabulary columns, token blocks outer: dW of a slab
-  // accumulates over the token blocks and dH of a token block over the slabs, both in a
-  // fixed order (deterministic).
-  const int bnd = choose_bn_d(d, true);
-  const int64_t Vc = pl.Vc;
-  const float* wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
-  for (int64_t b = 0; b < pl.nt; ++b) {
-    const int64_t r0 = b * pl.Ct;
-    const int64_t rows = (T - r0) < pl.Ct ? (T - r0) : pl.Ct;
-    const uint16_t* Hb = H + r0 * d;
-    CUtensorMap mH_k, mH_mn;
-    bool h3d = false;
-    if (!encode_map_bf16(&mH_k, Hb, d, rows, d * 2, 64, 128) || !encode_b_mn_pair(&mH_mn, Hb, d, rows, d * 2, bnd, true, &h3d))
-      return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H block %lld", (long long)b);
-    for (int64_t j = 0; j < pl.nslabs; ++j) {
-      const int64_t v0 = j * Vc;
-      const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
-      const uint16_t* Wj = W + v0 * d;
-      CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
-      // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
-      // 3-D view may span round_up(w, 64) columns.
-      bool w3d = false;
-      const bool wmap = encode_b_mn_pair(&mW_mn, Wj, d, w, d * 2, bnd, true, &w3d);
-      const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, rows, Vc * 2, 128);
-      if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) || !wmap ||
-          (!d3d && !encode_map_bf16(&mD_mn, ds, w, rows, Vc * 2, 64, 64)) ||
-          !encode_map_bf16(&mD_k, ds, w, rows, Vc * 2, 64, 128))
-        return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for block (%lld, %lld)", (long long)b, (long long)j);
-
-      // dS[block] = g tau w_t (q - ptilde), recomputing S = H_block W_slab^T.
-      const int m_tiles = (int)cdiv(rows, 256), n_tiles = (int)cdiv(w, kVocabTile);
-      GemmShape g3 = make_shape(rows, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2, group_rows(m_tiles)),
-                                &hdr->status, 256);
-      g3.group_m = group_rows(g3.m_tiles);
-      DsParams dp;
-      dp.pairs = pairs + r0 * K; dp.lse = lse + r0; dp.wrow = wrow + r0;
-      dp.arow = dv.kind != FKL_DIV_KL ? arow + r0 : nullptr;
-      dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
-      dp.T = (int)rows; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
-      dp.scale2 = 1.4426950408889634f / tau;
-      const double block_flops = 2.0 * rows * w * d;
-      trace_launch_begin(st);
-      if ((e = launch_gemm2_ds(mH_k, mW_k, g3, dp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "dS GEMM");
-      trace_launch_end(st, 1, block_flops);
-
-      // dW[slab] (+)= dS[block]^T H_block  (token blocks in order).
-      GemmShape g4 = make_shape(w, d, rows, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
-      g4.a_box3d = d3d ? 1 : 0;
-      g4.b_box3d = h3d ? 1 : 0;
-      F32Params p4;
-      p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
-      p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0; p4.vec_ok = 1;
-      trace_launch_begin(st);
-      if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
-        return cuda_fail(e, "dW GEMM");
-      trace_launch_end(st, 2, block_flops);
-
-      // dH[block] (+)= dS[block] W[slab]  (slabs in order).
-      GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
-      g5.b_box3d = w3d ? 1 : 0;
-      F32Params p5;
-      p5.out = dH + r0 * d; p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
-      p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = 1;
-      trace_launch_begin(st);
-      if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
-        return cuda_fail(e, "dH GEMM");
-      trace_launch_end(st, 3, block_flops);
-    }
-  }
+  if ((s = run_backward_blocks(pl, di, H, W, lse, T, d, V, K, tau, dv, accum, ws, dH, dW, st)) != FKL_OK) return s;
   if ((e = launch_poison(dH, T * d, dW, V * d, &hdr->status, di.sms, st)) != cudaSuccess)
     return cuda_fail(e, "poison kernel");
   return FKL_OK;

@@ -201,7 +201,7 @@ struct EpiDs {
     t = row0 + row;
     row_ok = t < p.T;
     if (row_ok) {
-      lse2 = p.lse[t] * 1.4426950408889634f;
+      lse2 = p.lse[t] * kLog2e;
       f = p.hdr->gtau * p.wrow[t];
       a = p.arow != nullptr ? p.arow[t] : 1.f;
       dst = p.ds + static_cast<size_t>(t) * p.ld_ds;

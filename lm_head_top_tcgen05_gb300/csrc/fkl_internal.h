@@ -28,6 +28,8 @@ constexpr int kVocabTile = 256;                   // tile width of the vocabular
 constexpr int kMaxSplit = 32;                     // most vocabulary splits per row block
 constexpr int64_t kMaxTokenBlocks = 64;           // most token blocks of the backward
 constexpr uint64_t kWaitLimitNs = 5000000000ull;  // per pipeline wait
+constexpr float kLog2e = 1.4426950408889634f;      // log2(e): natural-log scale to base 2
+constexpr float kLn2 = 0.69314718055994531f;       // ln(2): base-2 log back to natural
 
 // Where each buffer lives inside the caller's workspace, and the backward's blocks.
 struct Plan {

@@ -122,7 +122,7 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
   fp.part = part;
   fp.sg = nullptr;
   fp.T = (int)T; fp.K = (int)K; fp.V = (int)V; fp.nsplit = nsplit;
-  fp.scale2 = 1.4426950408889634f / tau;
+  fp.scale2 = kLog2e / tau;
   if (launch_gemm_fwd(mH, mW, g, fp, g.num_units < sms ? g.num_units : sms, st) != cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "forward GEMM launch failed");
   if (launch_combine(part, nsplit, crow, wrow, T, tau, lse, bsum, bcnt, pl.nb, hdr, loss, st) != cudaSuccess)

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kCombineThreads)
       L += part[plane + i] * exp2f(part[i] - M);
       G += part[2 * plane + i];
     }
-    const float lse_t = (M + log2f(L)) * 0.69314718055994531f;
+    const float lse_t = (M + log2f(L)) * kLn2;
     lse[t] = lse_t;
     const float w = wrow[t];
     if (w != 0.f) {
