@@ -137,9 +137,10 @@ typedef struct fkl_options {
 size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
 
 /*
- * Number of blocks (token block x vocabulary slab) the backward pass walks for this shape:
- * each is one dS-recompute GEMM, one dW GEMM and one dH GEMM launch.  0 for T = 0 or
- * invalid shapes.
+ * Number of blocks (token block x vocabulary slab) the backward pass walks for this shape
+ * on the current device (the slab width depends on its SM count; a GB300's 152 SMs are
+ * assumed when no device is visible): each is one dS-recompute GEMM, one dW GEMM and one dH
+ * GEMM launch.  0 for T = 0 or invalid shapes.
  */
 int64_t fkl_backward_slabs(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
 

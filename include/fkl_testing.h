@@ -37,12 +37,14 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
                          void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * The backward's blocking for this shape (host only, no device call): out[0] = tokens per
- * block Ct, out[1] = token blocks, out[2] = vocabulary columns per slab Vc, out[3] =
- * vocabulary slabs.  The dS buffer of one block holds Ct x Vc bf16 values.  Returns
- * FKL_ERR_INVALID_ARG for shapes fkl_workspace_size rejects.
+ * The backward's blocking for this shape on a device with `sms` SMs (host only, no device
+ * call): out[0] = tokens per block Ct, out[1] = token blocks, out[2] = vocabulary columns per
+ * slab Vc, out[3] = vocabulary slabs, out[4] = the widest slab the workspace's dS buffer
+ * holds (Ct x out[4] bf16 values; Vc <= out[4]).  out has room for 5 values.  Returns
+ * FKL_ERR_INVALID_ARG for shapes fkl_workspace_size rejects or sms < 2.
  */
-fkl_status fkl_test_backward_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, int64_t* out);
+fkl_status fkl_test_backward_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, int32_t sms,
+                                  int64_t* out);
 
 /*
  * Runs one pipeline wait on a barrier that nothing completes, with a time limit of

@@ -50,6 +50,7 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
     p->Ct = 0;
     p->nt = 0;
     p->Vc = kVocabTile;
+    p->Vmax = kVocabTile;
     p->nslabs = 0;
   } else {
     // The backward walks blocks of Ct tokens x Vc vocabulary columns; the dS buffer of one
@@ -85,6 +86,9 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
     p->nt = cdiv(T, best_ct);
     p->Vc = best_vc;
     p->nslabs = cdiv(V, p->Vc);
+    int64_t vmax = (budget / best_ct / kVocabTile) * kVocabTile;
+    if (vmax > vpad) vmax = vpad;
+    p->Vmax = vmax > best_vc ? vmax : best_vc;
   }
   p->nb = cdiv(T, 256);
   size_t off = 256;  // header
@@ -96,12 +100,17 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   const size_t nbb = static_cast<size_t>(p->nb > 0 ? p->nb : 1);
   p->off_bsum = off;  off = align_up(off + nbb * 8, 256);
   p->off_bcnt = off;  off = align_up(off + nbb * 4, 256);
-  p->off_ds = off;    off = align_up(off + static_cast<size_t>(p->Ct) * p->Vc * 2, 256);
+  p->off_ds = off;    off = align_up(off + static_cast<size_t>(p->Ct) * p->Vmax * 2, 256);
   p->off_slot = off;  off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
   p->off_sg = off;    off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
   p->off_arow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
   p->total = off;
   return true;
+}
+
+// Critical path of a vocabulary GEMM in tiles: waves of units times tiles per unit.
+static int64_t split_cost(int m_tiles, int n_tiles, int sms, int s) {
+  return cdiv(static_cast<int64_t>(m_tiles) * s, sms) * cdiv(n_tiles, s);
 }
 
 int plan_splits(int m_tiles, int n_tiles, int sms, int group) {
@@ -116,10 +125,7 @@ int plan_splits(int m_tiles, int n_tiles, int sms, int group) {
   if (lo > n_tiles) lo = n_tiles;
   if (lo < 1) lo = 1;
   int hi = n_tiles < kMaxSplit ? n_tiles : kMaxSplit;
-  auto cost = [&](int s) {
-    const int64_t units = static_cast<int64_t>(m_tiles) * s;
-    return cdiv(units, sms) * cdiv(n_tiles, s);
-  };
+  auto cost = [&](int s) { return split_cost(m_tiles, n_tiles, sms, s); };
   int best = lo;
   for (int s = lo; s <= hi; ++s)
     if (cost(s) < cost(best)) best = s;
@@ -300,6 +306,48 @@ static int choose_bn_d(int64_t d, bool pair) {
   return best;
 }
 
+// Vocabulary tiles per backward slab, at most the dS buffer's width and at least half of it.
+// A slab's three GEMMs run in waves of CTA pairs: dW in (slab tiles x d tiles) units and dH in
+// (Ct/256 x d tiles) units of one tile each, the dS recompute in units of plan_splits.  A slab
+// width whose dW unit count falls just past a whole number of waves leaves most pairs idle in
+// the last one (47 tiles x 12 d tiles = 564 units on 76 pairs: 7.4 waves, run as 8), so the
+// width is the one with the shortest critical path over all slabs, counted in 64-deep k-steps
+// of a 256 x 256 tile, plus a fixed cost per slab for the three launches' ramp and the dH
+// read-modify-write (about 0.2 ms at 32K tokens; measured: 44-tile slabs beat 47 by 1 % per
+// step at 32K, with dW 5 % faster).
+void choose_slab_width(Plan* p, int pairs) {
+  if (p->T == 0 || pairs < 1) return;
+  constexpr double kSlabFixedSteps = 600.0;
+  const int bnd = choose_bn_d(p->d, true);
+  const int64_t nd = cdiv(p->d, bnd), mt = cdiv(p->Ct, 256), kd = cdiv(p->d, 64), kt = cdiv(p->Ct, 64);
+  const double bs = bnd / 256.0;
+  auto slab = [&](int64_t wt) {
+    const int s = plan_splits(static_cast<int>(mt), static_cast<int>(wt), pairs, group_rows(static_cast<int>(mt)));
+    return static_cast<double>(split_cost(static_cast<int>(mt), static_cast<int>(wt), pairs, s) * kd) +
+           static_cast<double>(cdiv(wt * nd, pairs) * kt) * bs +
+           static_cast<double>(cdiv(mt * nd, pairs) * 4 * wt) * bs + kSlabFixedSteps;
+  };
+  const int64_t vt = cdiv(p->V, kVocabTile), mmax = p->Vmax / kVocabTile;
+  int64_t best_m = mmax;
+  double best = 1e300;
+  for (int64_t m = mmax; m >= 1 && 2 * m >= mmax; --m) {
+    const int64_t ns = cdiv(vt, m);
+    const double c = static_cast<double>(ns - 1) * slab(m) + slab(vt - (ns - 1) * m);
+    if (c < best) { best = c; best_m = m; }
+  }
+  p->Vc = best_m * kVocabTile;
+  p->nslabs = cdiv(p->V, p->Vc);
+}
+
+// CTA pairs of the current device, for planning only (76, a GB300's, when none is visible).
+static int planning_pairs() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      sms >= 2)
+    return sms / 2;
+  return 76;
+}
+
 static fkl_status check_options(const fkl_options* o, int64_t T) {
   if (o == nullptr) return FKL_OK;
   if (o->reserved != 0) return fail(FKL_ERR_INVALID_ARG, "fkl_options.reserved must be 0");
@@ -373,7 +421,9 @@ size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t ch
 
 int64_t fkl_backward_slabs(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk) {
   Plan p;
-  return make_plan(T, d, V, K, chunk, &p) ? p.nt * p.nslabs : 0;
+  if (!make_plan(T, d, V, K, chunk, &p)) return 0;
+  choose_slab_width(&p, planning_pairs());
+  return p.nt * p.nslabs;
 }
 
 const char* fkl_last_error(void) { return g_last_error.c_str(); }
@@ -584,6 +634,7 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
     return fail(FKL_ERR_ALIGNMENT, "lse and grad_loss must be 4-byte aligned");
   DevInfo di;
   if ((s = device_info(&di)) != FKL_OK) return s;
+  choose_slab_width(&pl, di.sms / 2);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -681,15 +732,19 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
   return FKL_OK;
 }
 
-fkl_status fkl_test_backward_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, int64_t* out) {
+fkl_status fkl_test_backward_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, int32_t sms,
+                                  int64_t* out) {
   g_last_error.clear();
   if (out == nullptr) return fail(FKL_ERR_INVALID_ARG, "out is NULL");
+  if (sms < 2) return fail(FKL_ERR_INVALID_ARG, "sms must be at least 2");
   Plan pl;
   if (!make_plan(T, d, V, K, chunk, &pl)) return fail(FKL_ERR_INVALID_ARG, "unsupported shape");
+  choose_slab_width(&pl, sms / 2);
   out[0] = pl.Ct;
   out[1] = pl.nt;
   out[2] = pl.Vc;
   out[3] = pl.nslabs;
+  out[4] = pl.Vmax;
   return FKL_OK;
 }
 

@@ -37,6 +37,7 @@ struct Plan {
   int64_t Ct;      // tokens per backward block (T, or a multiple of 256 below it)
   int64_t nt;      // token blocks of the backward
   int64_t Vc;      // vocabulary columns per backward slab (multiple of kVocabTile)
+  int64_t Vmax;    // widest slab the dS buffer holds (Vc <= Vmax)
   int64_t nslabs;  // vocabulary slabs of the backward
   int64_t nb;      // row blocks of the combine step (256 rows each)
   size_t off_pairs, off_crow, off_wrow, off_scnt, off_part, off_bsum, off_bcnt, off_ds;
@@ -65,6 +66,8 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
 // Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.
 // group: row blocks per group of the unit order (1 = row-major).
 int plan_splits(int m_tiles, int n_tiles, int sms, int group = 1);
+// Sets p->Vc and p->nslabs for a device with `pairs` CTA pairs (see fkl_api.cu).
+void choose_slab_width(Plan* p, int pairs);
 
 // ---------------------------------------------------------------- small kernels
 cudaError_t launch_prep(const int32_t* idx, const float* logits, int64_t T, int K, int V, float tau,

@@ -215,9 +215,9 @@ def test_teacher_topk_stride_is_checked_on_host(L):
         assert L.fkl_teacher_topk_ex(16, 16, 64, 64, 8192, 16, bad, 16, 16, 256, n, None) == INVALID
 
 
-def _plan(L, T, d, V, K, chunk):
-    out = (ctypes.c_int64 * 4)()
-    assert L.fkl_test_backward_plan(T, d, V, K, chunk, out) == 0
+def _plan(L, T, d, V, K, chunk, sms=152):
+    out = (ctypes.c_int64 * 5)()
+    assert L.fkl_test_backward_plan(T, d, V, K, chunk, sms, out) == 0
     return tuple(out)
 
 
@@ -225,20 +225,23 @@ def _plan(L, T, d, V, K, chunk):
                                            (65536, 4096, 151936, 100, 4096), (8192, 3072, 128256, 100, 1024),
                                            (4000, 64, 2999, 16, 512), (300, 200, 5000, 16, 128), (1, 64, 777, 8, 1)])
 def test_backward_blocks_respect_the_chunk_bound(L, T, d, V, K, chunk):
-    Ct, nt, Vc, ns = _plan(L, T, d, V, K, chunk)
-    assert Vc % 256 == 0 and Vc >= 256 and ns * Vc >= V and (ns - 1) * Vc < V
-    assert nt * Ct >= T and (nt - 1) * Ct < T
-    assert Ct == T or Ct % 256 == 0
-    # the dS buffer of one block: at most chunk * V values, or one 256-wide tile of Ct rows
-    assert Ct * Vc <= max(min(chunk, T) * V, Ct * 256)
-    assert L.fkl_backward_slabs(T, d, V, K, chunk) == nt * ns
+    for sms in (152, 148, 132, 2):
+        Ct, nt, Vc, ns, Vmax = _plan(L, T, d, V, K, chunk, sms)
+        assert Vc % 256 == 0 and Vc >= 256 and ns * Vc >= V and (ns - 1) * Vc < V
+        assert nt * Ct >= T and (nt - 1) * Ct < T
+        assert Ct == T or Ct % 256 == 0
+        # the dS buffer of one block: at most chunk * V values, or one 256-wide tile of Ct rows
+        assert Vc <= Vmax and 2 * Vc >= Vmax - 256
+        assert Ct * Vmax <= max(min(chunk, T) * V, Ct * 256)
+    # no device here: the slab count is planned for a GB300's 152 SMs
+    assert L.fkl_backward_slabs(T, d, V, K, chunk) == _plan(L, T, d, V, K, chunk)[1] * _plan(L, T, d, V, K, chunk)[3]
 
 
 def test_backward_block_choice(L):
     # 32K: full-height slabs (dW written once); 256K and long sequences: lower blocks cut the
     # read-modify-write of dH, which otherwise grows with the number of narrow slabs
     assert _plan(L, 32768, 2880, 201088, 100, 2048)[1] == 1
-    Ct, nt, Vc, ns = _plan(L, 262144, 2880, 201088, 100, 4096)
+    Ct, nt, Vc, ns, _ = _plan(L, 262144, 2880, 201088, 100, 4096)
     assert nt > 1 and Ct < 262144
 
     def rmw(T, d, V, nt, ns):
@@ -246,3 +249,16 @@ def test_backward_block_choice(L):
 
     assert rmw(262144, 2880, 201088, nt, ns) < 0.3 * rmw(262144, 2880, 201088, 1, 66)
     assert _plan(L, 4000, 64, 2999, 16, 512)[1] > 1
+
+
+def test_slab_width_fills_the_dw_waves(L):
+    # 32K tokens, d = 2880 (12 tiles of 256): the widest slab the chunk allows is 49 tiles and
+    # evening it over the slabs gives 47, whose dW GEMM has 47 x 12 = 564 one-tile units, 7.4
+    # waves of 76 CTA pairs run as 8.  44-tile slabs give 528 units, 6.95 waves.
+    Ct, nt, Vc, ns, Vmax = _plan(L, 32768, 2880, 201088, 100, 2048, 152)
+    assert (Ct, nt, Vmax) == (32768, 1, 49 * 256)
+    assert (Vc, ns) == (44 * 256, 18)
+    units = Vc // 256 * 12
+    assert units / 76 > 0.9 * -(-units // 76)
+    # the slab width follows the device: half the pairs, other waves
+    assert _plan(L, 32768, 2880, 201088, 100, 2048, 76)[2] != Vc
