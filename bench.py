@@ -170,6 +170,7 @@ def max_over_ranks(value: float, device=None) -> float:
 
 
 KIND_NAMES = {0: "forward projection + logsumexp/top-K", 1: "dS recompute", 2: "dW", 3: "dH"}
+FIXUP_KIND = 4
 KERNEL_NAMES = {0: "gemm2_kernel<256,0,0,EpiFwd> (two-SM)", 1: "gemm2_kernel<256,0,0,EpiDs> (two-SM)",
                 2: "gemm2_kernel<256,1,1,EpiF32> (two-SM, dW)", 3: "gemm2_kernel<256,0,1,EpiF32> (two-SM, dH)"}
 # Launches per step outside the GEMM trace: forward prep, 3 token-weight kernels, 2 combine;
@@ -211,11 +212,11 @@ def blas_threads():
     return None
 
 # DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
-# of the 32K workload's slab shape (T=32768, d=2880, slab width 12032; profiles/
+# of the 32K workload's slab shape (T=32768, d=2880, slab width 11264; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "577e2c0676a68c18"
-TRAFFIC_BYTES = {1: 1.911e9, 2: 2.526e9, 3: 2.684e9}
-TRAFFIC_FLOPS = 2.0 * 32768 * 12032 * 2880
+TRAFFIC_SOURCES_SHA = "d12e6410b85dbd2c"
+TRAFFIC_BYTES = {1: 1.498e9, 2: 2.272e9, 3: 2.530e9}
+TRAFFIC_FLOPS = 2.0 * 32768 * 11264 * 2880
 
 
 # The sources that define the loss's tensor-core GEMMs and how they are launched (tiles,
@@ -258,14 +259,25 @@ def trace_summary(L, cap):
     n = L.fkl_trace_read(ms, kind, flops, cap)
     if n < 0:
         raise RuntimeError("fkl_trace_read failed")
+    # kind 4 is the fixup of the K-split units of the dW or dH launch just before it: its time
+    # belongs to that product and its launch is counted as the product's fixup launch
     per = {}
+    prev = None
     for i in range(n):
-        a = per.setdefault(kind[i], [0, 0.0, 0.0])
+        k = kind[i]
+        if k == FIXUP_KIND and prev is not None:
+            a = per[prev]
+            a[1] += ms[i]
+            a[3] += 1
+            continue
+        a = per.setdefault(k, [0, 0.0, 0.0, 0])
         a[0] += 1
         a[1] += ms[i]
         a[2] += flops[i]
-    return {k: {"launches": c, "ms_total": t, "ms_per_launch": t / c, "flops_per_launch": f / c,
-                "tflops": f / (t / 1e3) / 1e12} for k, (c, t, f) in sorted(per.items())}
+        prev = k
+    return {k: {"launches": c, "fixup_launches": fx, "ms_total": t, "ms_per_launch": t / c,
+                "flops_per_launch": f / c, "tflops": f / (t / 1e3) / 1e12}
+            for k, (c, t, f, fx) in sorted(per.items())}
 
 
 def run_teacher_topk(args, world, rank, local_rank):
@@ -495,7 +507,7 @@ def main():
     tflops = world * w.flops_fwd_bwd * args.steps / elapsed / 1e12
     sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     burst = float(peaks["bf16_tflops"])
-    traced = sum(v["launches"] for v in kernels.values())
+    traced = sum(v["launches"] + v["fixup_launches"] for v in kernels.values())
     launches_per_step = UNTRACED_LAUNCHES_PER_STEP + (2 if args.divergence != "kl" else 0) + traced / args.steps
     clk = clocks.summary()
     dom = max(kernels, key=lambda k: kernels[k]["ms_total"])  # largest share of the step

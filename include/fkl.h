@@ -131,8 +131,9 @@ typedef struct fkl_options {
  * serves both; no state is carried between calls in it).  `chunk` bounds the backward's
  * dS buffer: it holds one block of the backward (a range of tokens x a vocabulary slab of
  * whole 256-column tiles, at least one tile wide), at most chunk * V bfloat16 values.  The result
- * does not depend on `chunk` beyond floating-point summation order.  Returns 0 for
- * invalid shapes.
+ * does not depend on `chunk` beyond floating-point summation order.  For T > 0 it also holds
+ * 80 fp32 partial tiles of 256 x 256 (20 MiB) for the dW and dH units that the backward splits
+ * along the reduction.  Returns 0 for invalid shapes.
  */
 size_t fkl_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
 
@@ -231,7 +232,9 @@ fkl_status fkl_trace_stop(void);
 /*
  * Waits for the recorded events and writes, for up to `capacity` recorded launches in launch
  * order, the duration in milliseconds (ms), the kind (0 forward projection + logsumexp,
- * 1 dS recompute, 2 dW, 3 dH, 5 teacher top-K bound pass, 6 teacher top-K candidate pass)
+ * 1 dS recompute, 2 dW, 3 dH, 4 the fixup that completes the K-split units of the dW or dH
+ * launch recorded just before it, with 0 FLOPs, 5 teacher top-K bound pass, 6 teacher top-K
+ * candidate pass)
  * and the launch's algorithmic FLOPs (2 * M * N * K of its product).  Any output pointer may be NULL.  Returns the number written, -1 on a CUDA error.
  */
 int32_t fkl_trace_read(float* ms, int32_t* kind, double* flops, int32_t capacity);

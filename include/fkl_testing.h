@@ -29,8 +29,11 @@ extern "C" {
  * multiple of 64 is loaded with one 3-D TMA box per tile, unless bit 1 of `accumulate` is
  * set (then 64-wide 2-D boxes, the path used for other extents).  Bit 0 of `accumulate`
  * selects accumulation.  Bit 2 selects the two-SM kernel (CTA pairs, 256-row tiles, the one
- * the loss uses; a 192-wide tile with MN-major B uses the 64-byte swizzle) instead of the one-SM kernel (128-row tiles).  `workspace`
- * needs 256 bytes (the status word).
+ * the loss uses; a 192-wide tile with MN-major B uses the 64-byte swizzle) instead of the one-SM kernel (128-row tiles).  Bit 3
+ * (with bit 2) splits the units of the last, partial wave of CTA pairs along K, as the
+ * backward does for dW and dH: their partial tiles go to the workspace after the first 256
+ * bytes (256 x bn fp32 each, as many as fit, at most 80) and a fixup kernel adds them.
+ * `workspace` needs 256 bytes (the status word) and the partial tiles' room.
  */
 fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t M, int64_t N,
                          int64_t Kd, int a_mn_major, int b_mn_major, int bn, int accumulate,

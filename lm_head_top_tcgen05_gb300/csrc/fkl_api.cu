@@ -104,6 +104,8 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   p->off_slot = off;  off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
   p->off_sg = off;    off = align_up(off + static_cast<size_t>(T) * K * 4, 256);
   p->off_arow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
+  p->off_kpart = off;
+  if (T > 0) off = align_up(off + static_cast<size_t>(kKsplitSlots) * 256 * 256 * 4, 256);
   p->total = off;
   return true;
 }
@@ -152,6 +154,9 @@ GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint3
   g.group_m = 1;
   g.a_box3d = 0;
   g.b_box3d = 0;
+  g.split_from = g.num_units;
+  g.ksplit = 1;
+  g.kpart = nullptr;
   g.status = status;
   g.limit_ns = kWaitLimitNs;
   return g;
@@ -339,6 +344,25 @@ void choose_slab_width(Plan* p, int pairs) {
   p->nslabs = cdiv(p->V, p->Vc);
 }
 
+// The units of a product's last wave, r = units mod pairs of them, would keep r pairs busy
+// for a whole unit while the others wait.  Split each into pairs / r pieces along K instead
+// (at least kKsplitMinBlocks k-blocks each, at most `slots` pieces in all): every pair then
+// runs at most one piece in that wave, and a fixup adds each unit's pieces in a fixed order.
+// Only for products with one tile per unit (dW, dH).  dH at 32K tokens: 1536 units on 76
+// pairs, 20.2 waves run as 21, become 20 waves and a quarter.
+void plan_ksplit(GemmShape* g, int pairs, float* kpart, int slots) {
+  if (kpart == nullptr || pairs < 2 || g->nsplit != g->n_tiles) return;
+  const int r = g->num_units % pairs;
+  if (r == 0) return;
+  int s = pairs / r;
+  if (s * r > slots) s = slots / r;
+  if (s > g->k_blocks / kKsplitMinBlocks) s = g->k_blocks / kKsplitMinBlocks;
+  if (s < 2) return;
+  g->split_from = g->num_units - r;
+  g->ksplit = s;
+  g->kpart = kpart;
+}
+
 // CTA pairs of the current device, for planning only (76, a GB300's, when none is visible).
 static int planning_pairs() {
   int dev = 0, sms = 0;
@@ -521,6 +545,15 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
   return FKL_OK;
 }
 
+// The fixup of a K-split product, traced (kind 4) right after the product it completes.
+static cudaError_t run_fixup(int bn, const GemmShape& g, const F32Params& p, cudaStream_t st) {
+  if (g.ksplit < 2) return cudaSuccess;
+  trace_launch_begin(st);
+  const cudaError_t e = launch_ksplit_fixup(bn, g, p, st);
+  if (e == cudaSuccess) trace_launch_end(st, 4, 0.0);
+  return e;
+}
+
 // The backward's GEMMs, after the light kernels have prepared the pairs, the token weights
 // and the scales in the workspace.  All three products use two-SM tiles (256 rows per CTA
 // pair, B split between the CTAs) over blocks of Ct tokens x Vc vocabulary columns, token
@@ -534,6 +567,7 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
   const int2* pairs = reinterpret_cast<const int2*>(ws + pl.off_pairs);
   const float* arow = reinterpret_cast<const float*>(ws + pl.off_arow);
   uint16_t* ds = reinterpret_cast<uint16_t*>(ws + pl.off_ds);
+  float* kpart = reinterpret_cast<float*>(ws + pl.off_kpart);
   cudaError_t e;
   const int bnd = choose_bn_d(d, true);
   const int64_t Vc = pl.Vc;
@@ -584,10 +618,12 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       F32Params p4;
       p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
       p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0; p4.vec_ok = 1;
+      plan_ksplit(&g4, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
         return cuda_fail(e, "dW GEMM");
       trace_launch_end(st, 2, block_flops);
+      if ((e = run_fixup(bnd, g4, p4, st)) != cudaSuccess) return cuda_fail(e, "dW K-split fixup");
 
       // dH[block] (+)= dS[block] W[slab]  (slabs in order).
       GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
@@ -595,10 +631,12 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       F32Params p5;
       p5.out = dH + r0 * d; p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
       p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = 1;
+      plan_ksplit(&g5, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
         return cuda_fail(e, "dH GEMM");
       trace_launch_end(st, 3, block_flops);
+      if ((e = run_fixup(bnd, g5, p5, st)) != cudaSuccess) return cuda_fail(e, "dH K-split fixup");
     }
   }
   return FKL_OK;
@@ -725,10 +763,16 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
   F32Params p;
   p.out = D; p.ldo = N; p.M = (int)M; p.N = (int)N; p.accumulate = (accumulate & 1) ? 1 : 0;
   p.vec_ok = (N % 4 == 0 && aligned(D, 16)) ? 1 : 0;
+  if (pair && (accumulate & 8)) {
+    const int slots = static_cast<int>((ws_bytes - 256) / (static_cast<size_t>(256) * bn * 4));
+    plan_ksplit(&g, di.sms / 2, reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256),
+                slots < kKsplitSlots ? slots : kKsplitSlots);
+  }
   e = pair ? launch_gemm2_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p, di.sms, st)
            : launch_gemm_f32(bn, a_mn_major != 0, b_mn_major != 0, mA, mB, g, p,
                              g.num_units < di.sms ? g.num_units : di.sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "test GEMM");
+  if ((e = launch_ksplit_fixup(bn, g, p, st)) != cudaSuccess) return cuda_fail(e, "test GEMM K-split fixup");
   return FKL_OK;
 }
 

@@ -54,6 +54,30 @@ __device__ __forceinline__ void unit_range(const GemmShape& g, int u, int& m_blk
   n_end = static_cast<int>(static_cast<long long>(split + 1) * g.n_tiles / g.nsplit);
 }
 
+// Work items of the two-SM kernel: the units before g.split_from whole, then ksplit pieces of
+// each later unit, a piece covering k-blocks [kb0, kb1).  slot is the piece's partial tile
+// in g.kpart, or -1 for a whole unit.
+__host__ __device__ __forceinline__ int num_items(const GemmShape& g) {
+  return g.split_from + (g.num_units - g.split_from) * g.ksplit;
+}
+
+__device__ __forceinline__ void item_range(const GemmShape& g, int it, int& m_blk, int& n_begin, int& n_end,
+                                           int& split, int& kb0, int& kb1, int& slot) {
+  if (it < g.split_from) {
+    unit_range(g, it, m_blk, n_begin, n_end, split);
+    kb0 = 0;
+    kb1 = g.k_blocks;
+    slot = -1;
+    return;
+  }
+  const int j = it - g.split_from;
+  const int piece = j % g.ksplit;
+  unit_range(g, g.split_from + j / g.ksplit, m_blk, n_begin, n_end, split);
+  kb0 = static_cast<int>(static_cast<long long>(piece) * g.k_blocks / g.ksplit);
+  kb1 = static_cast<int>(static_cast<long long>(piece + 1) * g.k_blocks / g.ksplit);
+  slot = j;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void pin(float (&v)[32]) {
 #pragma unroll
@@ -272,6 +296,7 @@ struct EpiF32 {
   using Params = F32Params;
   const Params& p;
   bool row_ok;
+  bool part;  // the tile is one K piece, stored whole to a partial tile (row stride BN)
   float* rowp;
 
   __device__ explicit EpiF32(const Params& prm) : p(prm) {}
@@ -279,7 +304,15 @@ struct EpiF32 {
   __device__ __forceinline__ void begin_unit(int row0, int, int, int row) {
     const int r = row0 + row;
     row_ok = r < p.M;
+    part = false;
     rowp = p.out + static_cast<size_t>(row_ok ? r : 0) * p.ldo;
+  }
+
+  // A K piece: this thread's row of the partial tile at `tile` (ld floats per row).
+  __device__ __forceinline__ void begin_part(float* tile, int ld, int row0, int row_in_tile, int row) {
+    row_ok = row0 + row < p.M;
+    part = true;
+    rowp = tile + static_cast<size_t>(row_in_tile) * ld;
   }
 
   template <int BN>
@@ -292,13 +325,13 @@ struct EpiF32 {
       tmem_ld32(taddr + c * 32, v);
       tmem_ld_wait(v);
       if (!row_ok) continue;
-      float* o = rowp + col0;
-      if (p.vec_ok && col0 + 32 <= p.N) {
+      float* o = part ? rowp + c * 32 : rowp + col0;
+      if (part || (p.vec_ok && col0 + 32 <= p.N)) {
         float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           float4 x = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          if (p.accumulate) {
+          if (p.accumulate && !part) {
             const float4 y = o4[j];
             x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
           }

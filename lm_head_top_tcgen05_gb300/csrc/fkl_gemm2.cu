@@ -1,5 +1,6 @@
 // Instantiations of the two-SM (cta_group::2) persistent GEMM: the loss's forward and dS
-// epilogues with 256 x 256 tiles, and the fp32 epilogue for dW / dH and the test hook.
+// epilogues with 256 x 256 tiles, and the fp32 epilogue for dW / dH and the test hook; and
+// the fixup that completes K-split fp32 units.
 #include "fkl_gemm2.cuh"
 
 namespace fkl {
@@ -31,6 +32,51 @@ cudaError_t launch_gemm2_f32(int bn, bool a_mn, bool b_mn, const CUtensorMap& a,
     case 128: return dispatch2<128>(a_mn, b_mn, a, b, g, ep, sms, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// One block per (split unit, slice of its rows): sums the unit's K pieces in piece order and
+// stores, or adds, the tile into the product's output.  BN columns per tile.
+__global__ void __launch_bounds__(256) ksplit_fixup_kernel(const GemmShape g, const F32Params p, int bn) {
+  const int r = static_cast<int>(blockIdx.x);
+  int m_blk, nb, ne, split;
+  unit_range(g, g.split_from + r, m_blk, nb, ne, split);
+  const size_t tile = static_cast<size_t>(kBM2) * bn;
+  const float* part = g.kpart + static_cast<size_t>(r) * g.ksplit * tile;
+  const int cols4 = bn / 4;
+  const int total = kBM2 * cols4;
+  for (int i = static_cast<int>(blockIdx.y * blockDim.x + threadIdx.x); i < total;
+       i += static_cast<int>(gridDim.y * blockDim.x)) {
+    const int tr = i / cols4;
+    const int tc = (i - tr * cols4) * 4;
+    const int row = m_blk * kBM2 + tr;
+    const int col = nb * bn + tc;
+    if (row >= p.M || col >= p.N) continue;
+    const float* src = part + static_cast<size_t>(tr) * bn + tc;
+    float4 s = *reinterpret_cast<const float4*>(src);
+    for (int q = 1; q < g.ksplit; ++q) {
+      const float4 y = *reinterpret_cast<const float4*>(src + q * tile);
+      s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
+    }
+    float* o = p.out + static_cast<size_t>(row) * p.ldo + col;
+    if (p.vec_ok && col + 4 <= p.N) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+      if (p.accumulate) {
+        const float4 y = *o4;
+        s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
+      }
+      *o4 = s;
+    } else {
+      const float sv[4] = {s.x, s.y, s.z, s.w};
+      for (int j = 0; j < 4 && col + j < p.N; ++j) o[j] = p.accumulate ? o[j] + sv[j] : sv[j];
+    }
+  }
+}
+
+cudaError_t launch_ksplit_fixup(int bn, const GemmShape& g, const F32Params& ep, cudaStream_t st) {
+  const int units = g.num_units - g.split_from;
+  if (units <= 0 || g.ksplit < 2) return cudaSuccess;
+  ksplit_fixup_kernel<<<dim3(static_cast<unsigned>(units), 16), 256, 0, st>>>(g, ep, bn);
+  return cudaGetLastError();
 }
 
 }  // namespace fkl

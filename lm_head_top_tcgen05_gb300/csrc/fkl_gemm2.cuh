@@ -17,6 +17,8 @@
 // the other CTA at a cluster barrier and frees TMEM of both CTAs together.
 #pragma once
 
+#include <type_traits>
+
 #include "fkl_gemm.cuh"
 
 namespace fkl {
@@ -102,13 +104,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
       bool ok = true;
-      for (int u = cluster; ok && u < g.num_units; u += nclusters) {
-        int m_blk, nb, ne, split;
-        unit_range(g, u, m_blk, nb, ne, split);
+      const int items = num_items(g);
+      for (int it = cluster; ok && it < items; it += nclusters) {
+        int m_blk, nb, ne, split, kb0, kb1, slot;
+        item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
         const int a_row = m_blk * kBM2 + static_cast<int>(rank) * kBM;
         for (int n = nb; ok && n < ne; ++n) {
           const int b_row = n * BN + static_cast<int>(rank) * BNH;
-          for (int kb = 0; kb < g.k_blocks; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             // the slot is released by the even CTA's tensor core (multicast commit)
             if (!mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, ctl)) { ok = false; break; }
             const uint32_t fb = full0_even + 8 * stage;
@@ -158,14 +161,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = cluster; ok && u < g.num_units; u += nclusters) {
-        int m_blk, nb, ne, split;
-        unit_range(g, u, m_blk, nb, ne, split);
+      const int items = num_items(g);
+      for (int it = cluster; ok && it < items; it += nclusters) {
+        int m_blk, nb, ne, split, kb0, kb1, slot;
+        item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
         for (int n = nb; ok && n < ne; ++n) {
           if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, ctl)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kb = 0; kb < g.k_blocks; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_cluster(full0 + 8 * stage, phase, ctl)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = stage0 + stage * STAGE_BYTES;
@@ -179,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint64_t bd = !B_MN ? smem_desc_sw128(sb + k * 32, 16, 1024)
                                   : B_SW64 ? smem_desc(sb + k * 1024, BOX64_BYTES, 512, 4u)
                                            : smem_desc_sw128(sb + k * 2048, BOX_BYTES, 1024);
-              tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
             }
             tc_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -202,10 +206,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int u = cluster; ok && u < g.num_units; u += nclusters) {
-      int m_blk, nb, ne, split;
-      unit_range(g, u, m_blk, nb, ne, split);
-      epi.begin_unit(m_blk * kBM2 + static_cast<int>(rank) * kBM, nb, split, row);
+    const int items = num_items(g);
+    for (int it = cluster; ok && it < items; it += nclusters) {
+      int m_blk, nb, ne, split, kb0, kb1, slot;
+      item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
+      const int row0 = m_blk * kBM2 + static_cast<int>(rank) * kBM;
+      if constexpr (std::is_same<Epi, EpiF32>::value) {
+        if (slot >= 0)
+          epi.begin_part(g.kpart + static_cast<size_t>(slot) * (kBM2 * BN), BN, row0,
+                         static_cast<int>(rank) * kBM + row, row);
+        else
+          epi.begin_unit(row0, nb, split, row);
+      } else {
+        epi.begin_unit(row0, nb, split, row);
+      }
       for (int n = nb; n < ne; ++n) {
         const bool got = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, ctl);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -261,7 +275,8 @@ cudaError_t launch_gemm2_t(const CUtensorMap& a, const CUtensorMap& b, const Gem
   cudaError_t e = smem_limit_once(kern, SMEM, state.limit_set);
   if (e != cudaSuccess) return e;
   const int clusters = max_pair_clusters(kern, SMEM, sms, state.clusters);
-  const int n = g.num_units < clusters ? g.num_units : clusters;
+  const int items = num_items(g);
+  const int n = items < clusters ? items : clusters;
   kern<<<2 * n, kThreads, SMEM, st>>>(a, b, g, ep);
   return cudaGetLastError();
 }

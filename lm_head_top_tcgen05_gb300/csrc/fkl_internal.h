@@ -44,6 +44,7 @@ struct Plan {
   size_t off_slot;  // int32 [T][K]: original slot of each sorted pair
   size_t off_sg;    // fp32 [T][K]: student logit at each sorted pair (other divergences)
   size_t off_arow;  // fp32 [T]: per-row factor a_t of dS (other divergences)
+  size_t off_kpart; // fp32 partial tiles of K-split dW / dH units
   size_t total;
 };
 
@@ -112,9 +113,23 @@ struct GemmShape {
   int group_m;    // row blocks per group: units run split-major within a group (1 = row-major)
   int a_box3d;    // MN-major A loaded by one 3-D box per tile (else 64-wide 2-D boxes)
   int b_box3d;    // same for B
+  // Units from split_from on (those of the last, partial wave) are split along K into ksplit
+  // pieces; each piece stores its fp32 partial tile in kpart, and a fixup kernel adds the
+  // pieces in order (fp32 products, two-SM kernel only; split_from = num_units: none).
+  int split_from;
+  int ksplit;
+  float* kpart;  // [(unit - split_from) * ksplit + piece][256][bn]
   uint32_t* status;
   uint64_t limit_ns;
 };
+
+// Partial tiles the workspace holds for K-split units (256 x 256 fp32 each).
+constexpr int kKsplitSlots = 80;
+// Fewest 64-deep k-blocks per K piece.
+constexpr int kKsplitMinBlocks = 4;
+// Splits the units of the last, partial wave of a one-tile-per-unit fp32 product along K
+// (see fkl_api.cu); leaves the shape unsplit when that does not pay.
+void plan_ksplit(GemmShape* g, int pairs, float* kpart, int slots);
 
 // Row blocks per group of the unit order for products over the vocabulary (see fkl_api.cu).
 int group_rows(int m_tiles);
@@ -181,6 +196,8 @@ cudaError_t launch_gemm2_ds(const CUtensorMap& a, const CUtensorMap& b, const Ge
                             const DsParams& ep, int sms, cudaStream_t st);
 cudaError_t launch_gemm2_f32(int bn, bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
                              const GemmShape& g, const F32Params& ep, int sms, cudaStream_t st);
+// Adds the K pieces of every split unit of `g` (plan_ksplit) in piece order into ep.out.
+cudaError_t launch_ksplit_fixup(int bn, const GemmShape& g, const F32Params& ep, cudaStream_t st);
 // F32-output GEMM for bn in {256, 192, 128} and either major-ness of A and B.
 cudaError_t launch_gemm_f32(int bn, bool a_mn, bool b_mn, const CUtensorMap& a,
                             const CUtensorMap& b, const GemmShape& g, const F32Params& ep,

@@ -22,7 +22,7 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0, force2d=False, pair=False):
+def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0, force2d=False, pair=False, ksplit=False):
     g = torch.Generator().manual_seed(seed)
     A = torch.randn(M, Kd, generator=g).to(torch.bfloat16)
     B = torch.randn(N, Kd, generator=g).to(torch.bfloat16)
@@ -30,10 +30,12 @@ def run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=False, seed=0, force2d=Fals
     Ad = (A.t().contiguous() if a_mn else A).cuda()
     Bd = (B.t().contiguous() if b_mn else B).cuda()
     D = D0.clone().cuda()
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    flags = int(accumulate) | (2 if force2d else 0) | (4 if pair else 0)
+    # room for 80 partial tiles of 256 x 256 fp32 when the last wave is split along K
+    nws = 256 + (80 * 256 * 256 * 4 if ksplit else 0)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    flags = int(accumulate) | (2 if force2d else 0) | (4 if pair else 0) | (8 if ksplit else 0)
     st = L.fkl_test_gemm(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, Kd, int(a_mn), int(b_mn), bn,
-                         flags, ws.data_ptr(), 256, _stream())
+                         flags, ws.data_ptr(), nws, _stream())
     assert st == 0, L.fkl_last_error()
     assert L.fkl_read_status(ws.data_ptr(), _stream()) == 0
     ref = A.double() @ B.double().T + D0.double()
@@ -142,3 +144,17 @@ def test_two_copies_of_the_library_in_one_process(L, tmp_path):
         fn = getattr(L2, name)
         fn.restype, fn.argtypes = res, args
     assert run_gemm(L2, 512, 512, 128, False, False, 256, pair=True) < 1e-5
+
+
+@pytest.mark.parametrize("M,N,Kd,a_mn,b_mn,bn,acc", [
+    (1792, 768, 1000, False, True, 256, False),  # 21 units on 76 pairs: all split, 3 pieces each
+    (2816, 2880, 1024, False, True, 256, True),  # 11 x 12 = 132 units: 56 left over, no split
+    (2304, 2880, 2048, True, True, 256, True),   # 9 x 12 = 108: 32 left over, 2 pieces each
+    (512, 2880, 1536, False, True, 256, False),  # 2 x 12 = 24: 3 pieces, ragged last column tile
+    (304, 520, 4000, True, True, 192, True),     # 2 x 3 = 6 units: 12 pieces of 5-6 k-blocks
+    (256, 256, 296, False, False, 256, False),   # 1 unit of 5 k-blocks: too short to split
+])
+def test_last_wave_split_along_k(L, M, N, Kd, a_mn, b_mn, bn, acc):
+    # the units of the last, partial wave are split along K into pieces that store partial
+    # tiles, and a fixup kernel adds them in piece order into the output (or onto it)
+    assert run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=acc, seed=11, pair=True, ksplit=True) < 3e-5
