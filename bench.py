@@ -211,12 +211,15 @@ def blas_threads():
                 return int(fn())
     return None
 
-# DRAM bytes (read + write) per launch from one ncu capture of each backward GEMM on a launch
-# of the 32K workload's slab shape (T=32768, d=2880, slab width 11264; profiles/
-# bwd_gemms_gptoss20b_32k_slab.md), valid only for the CUDA sources they were taken on.
-TRAFFIC_SOURCES_SHA = "d12e6410b85dbd2c"
-TRAFFIC_BYTES = {1: 1.498e9, 2: 2.272e9, 3: 2.530e9}
-TRAFFIC_FLOPS = 2.0 * 32768 * 11264 * 2880
+# DRAM bytes (read + write) per launch of each GEMM kind on the 32K workload (T=32768,
+# d=2880, V=201088), valid only for the CUDA sources they were taken on: the backward's from
+# one ncu capture of a launch of its slab shape (slab width 11264; profiles/
+# bwd_gemms_gptoss20b_32k_slab.md), scaled by work to the mean launch; the forward's from a
+# one-pass capture of the full-size launch itself (profiles/fwd_gemm_gptoss20b_32k_smallV.md).
+TRAFFIC_SOURCES_SHA = "f32c74cae54435f7"
+TRAFFIC_BYTES = {0: 43.317e9, 1: 1.676e9, 2: 2.609e9, 3: 2.903e9}
+TRAFFIC_FLOPS = {0: 2.0 * 32768 * 201088 * 2880, 1: 2.0 * 32768 * 11264 * 2880,
+                 2: 2.0 * 32768 * 11264 * 2880, 3: 2.0 * 32768 * 11264 * 2880}
 
 
 # The sources that define the loss's tensor-core GEMMs and how they are launched (tiles,
@@ -247,7 +250,7 @@ def traffic_per_launch(kind, flops_per_launch, d):
     these products grows in proportion to the slab width), or None when no capture applies."""
     if kind not in TRAFFIC_BYTES or d != 2880 or csrc_sha() != TRAFFIC_SOURCES_SHA:
         return None
-    return TRAFFIC_BYTES[kind] * flops_per_launch / TRAFFIC_FLOPS
+    return TRAFFIC_BYTES[kind] * flops_per_launch / TRAFFIC_FLOPS[kind]
 
 
 def trace_summary(L, cap):
@@ -259,6 +262,8 @@ def trace_summary(L, cap):
     n = L.fkl_trace_read(ms, kind, flops, cap)
     if n < 0:
         raise RuntimeError("fkl_trace_read failed")
+    if n >= cap:
+        raise RuntimeError(f"the trace filled its {cap} entries: launches of the timed steps were not recorded")
     # kind 4 is the fixup of the K-split units of the dW or dH launch just before it: its time
     # belongs to that product and its launch is counted as the product's fixup launch
     per = {}
@@ -303,7 +308,7 @@ def run_teacher_topk(args, world, rank, local_rank):
     torch.cuda.synchronize()
     assert fkl.read_status(ws) == 0
     L = fkl.lib()
-    cap = 2 * args.steps
+    cap = 2 * args.steps + 1
     fkl.check(L.fkl_trace_start(cap), "fkl_trace_start")
     stream = torch.cuda.current_stream(dev)
     with ClockSampler(local_rank) as clocks:
@@ -439,7 +444,9 @@ def main():
     stream = torch.cuda.current_stream(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     nslabs = int(fkl.lib().fkl_backward_slabs(T, d, V, K, w.chunk))
-    trace_cap = args.steps * (1 + 3 * nslabs)
+    # per step: the forward, three products per backward block and at most one K-split
+    # fixup each for dW and dH; one more entry so that a full trace is detected
+    trace_cap = args.steps * (1 + 5 * nslabs) + 1
     fkl.check(fkl.lib().fkl_trace_start(trace_cap), "fkl_trace_start")
     with ClockSampler(local_rank) as clocks:
         barrier()
@@ -539,7 +546,7 @@ def main():
                      "flops_per_launch": kernels[dom]["flops_per_launch"],
                      "ms_per_launch": kernels[dom]["ms_per_launch"],
                      "traffic": traffic_per_launch(dom, kernels[dom]["flops_per_launch"], d)
-                     if T == 32768 else None,
+                     if (T, V) == (32768, 201088) else None,
                      "nominal": nominal},
         "kernels": {KIND_NAMES[k]: {kk: round(vv, 4) if isinstance(vv, float) else vv for kk, vv in v.items()}
                     for k, v in kernels.items()},
