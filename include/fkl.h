@@ -32,7 +32,9 @@
  *     the library allocates no device memory.
  *   - H and W are bfloat16 bit patterns (uint16_t).  H, W, dH and dW must be 16-byte
  *     aligned, the workspace 256-byte aligned, everything else 4-byte aligned; d must be a
- *     multiple of 8 (TMA rows are whole 16-byte units).
+ *     multiple of 8 (TMA rows are whole 16-byte units).  dH and dW are written with 32-byte
+ *     vectors when they are 32-byte aligned (any CUDA allocation is) and element by element,
+ *     more slowly, when they are not.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous
  *     on `stream`; they never synchronise the device.
  *   - Shape limits: 0 <= T < 2^31, 1 <= V < 2^31, 8 <= d < 2^20, d % 8 == 0,

@@ -617,7 +617,7 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       g4.b_box3d = h3d ? 1 : 0;
       F32Params p4;
       p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
-      p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0; p4.vec_ok = 1;
+      p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0; p4.vec_ok = aligned(dW, 32) ? 1 : 0;
       plan_ksplit(&g4, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
@@ -630,7 +630,7 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       g5.b_box3d = w3d ? 1 : 0;
       F32Params p5;
       p5.out = dH + r0 * d; p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
-      p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = 1;
+      p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = aligned(dH, 32) ? 1 : 0;
       plan_ksplit(&g5, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
@@ -762,7 +762,7 @@ fkl_status fkl_test_gemm(const uint16_t* A, const uint16_t* B, float* D, int64_t
   g.b_box3d = b3d ? 1 : 0;
   F32Params p;
   p.out = D; p.ldo = N; p.M = (int)M; p.N = (int)N; p.accumulate = (accumulate & 1) ? 1 : 0;
-  p.vec_ok = (N % 4 == 0 && aligned(D, 16)) ? 1 : 0;
+  p.vec_ok = (N % 8 == 0 && aligned(D, 32)) ? 1 : 0;
   if (pair && (accumulate & 8)) {
     const int slots = static_cast<int>((ws_bytes - 256) / (static_cast<size_t>(256) * bn * 4));
     plan_ksplit(&g, di.sms / 2, reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256),

@@ -78,6 +78,19 @@ __device__ __forceinline__ void item_range(const GemmShape& g, int it, int& m_bl
   slot = j;
 }
 
+
+// 256-bit global store and load (32-byte aligned addresses): one full 32-byte sector per
+// thread, half the instructions of 16-byte vectors for the epilogues' row-wise output.
+__device__ __forceinline__ void st_v8(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                      uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d),
+               "r"(e), "r"(f), "r"(g), "r"(h) : "memory");
+}
+__device__ __forceinline__ void ld_v8(const void* ptr, float (&x)[8]) {
+  asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7])
+               : "l"(ptr) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void pin(float (&v)[32]) {
 #pragma unroll
@@ -256,20 +269,18 @@ struct EpiDs {
         if (cl0 + j >= p.slab_w) v[j] = 0.f;
     }
     if (!row_ok) return;
-    uint4* o = reinterpret_cast<uint4*>(dst + cl0);
+    uint16_t* o = dst + cl0;
     if (f == 0.f) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+      for (int j = 0; j < 2; ++j) st_v8(o + 16 * j, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
       return;
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 w;
-      w.x = pack_bf16x2(f * v[8 * j + 0], f * v[8 * j + 1]);
-      w.y = pack_bf16x2(f * v[8 * j + 2], f * v[8 * j + 3]);
-      w.z = pack_bf16x2(f * v[8 * j + 4], f * v[8 * j + 5]);
-      w.w = pack_bf16x2(f * v[8 * j + 6], f * v[8 * j + 7]);
-      o[j] = w;
+    for (int j = 0; j < 2; ++j) {
+      const float* q = v + 16 * j;
+      st_v8(o + 16 * j, pack_bf16x2(f * q[0], f * q[1]), pack_bf16x2(f * q[2], f * q[3]),
+            pack_bf16x2(f * q[4], f * q[5]), pack_bf16x2(f * q[6], f * q[7]), pack_bf16x2(f * q[8], f * q[9]),
+            pack_bf16x2(f * q[10], f * q[11]), pack_bf16x2(f * q[12], f * q[13]), pack_bf16x2(f * q[14], f * q[15]));
     }
   }
 
@@ -327,15 +338,19 @@ struct EpiF32 {
       if (!row_ok) continue;
       float* o = part ? rowp + c * 32 : rowp + col0;
       if (part || (p.vec_ok && col0 + 32 <= p.N)) {
-        float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float4 x = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int j = 0; j < 4; ++j) {
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = v[8 * j + i];
           if (p.accumulate && !part) {
-            const float4 y = o4[j];
-            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+            float y[8];
+            ld_v8(o + 8 * j, y);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] += y[i];
           }
-          o4[j] = x;
+          st_v8(o + 8 * j, __float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]),
+                __float_as_uint(x[4]), __float_as_uint(x[5]), __float_as_uint(x[6]), __float_as_uint(x[7]));
         }
       } else {
 #pragma unroll

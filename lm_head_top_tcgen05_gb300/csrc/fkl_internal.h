@@ -169,7 +169,7 @@ struct F32Params {
   int64_t ldo;
   int M, N;
   int accumulate;
-  int vec_ok;  // ldo and base allow 16-byte vector access
+  int vec_ok;  // ldo and base allow 32-byte vector access
 };
 
 bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

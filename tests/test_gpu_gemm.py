@@ -153,6 +153,7 @@ def test_two_copies_of_the_library_in_one_process(L, tmp_path):
     (512, 2880, 1536, False, True, 256, False),  # 2 x 12 = 24: 3 pieces, ragged last column tile
     (304, 520, 4000, True, True, 192, True),     # 2 x 3 = 6 units: 12 pieces of 5-6 k-blocks
     (256, 256, 296, False, False, 256, False),   # 1 unit of 5 k-blocks: too short to split
+    (1792, 300, 1000, False, False, 256, True),  # rows of 300 floats: element-wise output, 4 pieces
 ])
 def test_last_wave_split_along_k(L, M, N, Kd, a_mn, b_mn, bn, acc):
     # the units of the last, partial wave are split along K into pieces that store partial

@@ -287,3 +287,28 @@ def test_token_blocks_with_variants(fkl):
     assert abs(loss.item() - ref["loss"]) <= LOSS_RTOL * abs(ref["loss"])
     assert_grad_close((dH - dH0).double().cpu().numpy(), ref["dH"], "accumulated dH")
     assert_grad_close((dW - dW0).double().cpu().numpy(), ref["dW"], "accumulated dW")
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_gradients_16_but_not_32_byte_aligned(fkl, accumulate):
+    # dH and dW 16 bytes past a 32-byte boundary: the products' epilogues and the K-split
+    # fixup write them element by element instead of in 32-byte vectors
+    x = workloads.make_random(700, 136, 3000, 16, tau=1.2, chunk=256, seed=61, mask_frac=0.1)
+    H, W, idx, z, m = to_dev(x)
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    bh = torch.zeros(H.numel() + 4, device="cuda")
+    bw = torch.zeros(W.numel() + 4, device="cuda")
+    dH, dW = bh[4:].view(H.shape), bw[4:].view(W.shape)
+    assert dH.data_ptr() % 32 == 16 and dW.data_ptr() % 32 == 16
+    dH0 = torch.randn(H.shape, device="cuda", generator=g) if accumulate else torch.zeros(H.shape, device="cuda")
+    dW0 = torch.randn(W.shape, device="cuda", generator=g) if accumulate else torch.zeros(W.shape, device="cuda")
+    dH.copy_(dH0)
+    dW.copy_(dW0)
+    fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, out=(dH, dW), accumulate=accumulate)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 0
+    ref = run_oracle(x)
+    assert_grad_close(dH.cpu().numpy().astype(np.float64) - dH0.cpu().numpy(), ref["dH"], "dH")
+    assert_grad_close(dW.cpu().numpy().astype(np.float64) - dW0.cpu().numpy(), ref["dW"], "dW")
+    assert bh[:4].abs().max().item() == 0 and bw[:4].abs().max().item() == 0
