@@ -13,6 +13,9 @@
 //               to `tfull` of both CTAs (multicast commit); idle in the odd CTA;
 //   warps 2..5  epilogue (both CTAs) on its own 128 TMEM lanes; hands the accumulator
 //               back by arriving on the even CTA's `tempty` (8 arrivals: 4 warps x 2 CTAs).
+// All three roles walk the same sequence of work items (item_range): whole units, then, for
+// the fp32 products, the K pieces of the last wave's units (GemmShape::split_from), whose
+// partial tiles a fixup kernel adds up afterwards.
 // Every wait is bounded as in the one-SM kernel; teardown drains copies and MMAs, meets
 // the other CTA at a cluster barrier and frees TMEM of both CTAs together.
 #pragma once
