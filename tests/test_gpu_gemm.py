@@ -159,3 +159,23 @@ def test_last_wave_split_along_k(L, M, N, Kd, a_mn, b_mn, bn, acc):
     # the units of the last, partial wave are split along K into pieces that store partial
     # tiles, and a fixup kernel adds them in piece order into the output (or onto it)
     assert run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=acc, seed=11, pair=True, ksplit=True) < 3e-5
+
+
+def _random_split_case(i):
+    # seeded shapes for the two-SM kernel with the last wave split along K: every operand
+    # major-ness, tile widths 256 / 192 / 128, ragged tiles, plain and accumulating output
+    import numpy as np
+
+    rng = np.random.default_rng(5000 + i)
+    a_mn, b_mn = bool(rng.integers(2)), bool(rng.integers(2))
+    bn = int(rng.choice([256, 192, 128]))
+    M = 8 * int(rng.integers(1, 200))
+    N = 8 * int(rng.integers(1, 200))
+    Kd = 8 * int(rng.integers(32, 400))
+    return M, N, Kd, a_mn, b_mn, bn, bool(rng.integers(2))
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_last_wave_split_random_shapes(L, i):
+    M, N, Kd, a_mn, b_mn, bn, acc = _random_split_case(i)
+    assert run_gemm(L, M, N, Kd, a_mn, b_mn, bn, accumulate=acc, seed=100 + i, pair=True, ksplit=True) < 5e-5

@@ -15,7 +15,7 @@ from tests.test_gpu_parity import assert_parity, fkl, run_gpu, run_oracle  # noq
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 16
+N_CASES = 32
 
 
 def draw(i):
