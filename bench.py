@@ -373,6 +373,8 @@ def main():
     ap.add_argument("--divergence", default="kl", choices=["kl", "jsd", "skew_kl", "skew_rkl", "tv"],
                     help="the loss's divergence (default: KL, the headline)")
     ap.add_argument("--div-param", type=float, default=None, help="b for jsd, a for the skew forms")
+    ap.add_argument("--grad-dtype", default="fp32", choices=["fp32", "bf16"],
+                    help="dtype of the dH / dW outputs (default fp32; bf16: fp32 sums rounded once)")
     ap.add_argument("--bound-stride", type=int, default=0,
                     help="teacher_topk: largest vocabulary sampling stride of the bound pass (0: default)")
     ap.add_argument("--mode", default="loss", choices=["loss", "teacher_topk"],
@@ -421,8 +423,9 @@ def main():
     H, Wt = x.H.to(dev), x.W.to(dev)
     idx, z, m = x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev)
     ws = fkl.Workspace(dev)
-    dH = torch.empty((T, d), dtype=torch.float32, device=dev)
-    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    gdt = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
+    dH = torch.empty((T, d), dtype=gdt, device=dev)
+    dW = torch.empty((V, d), dtype=gdt, device=dev)
     torch.cuda.synchronize()
     inputs_bytes = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
@@ -434,7 +437,7 @@ def main():
     def step():
         loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids, **div)
         fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
-                     student_topk_logits=s_ids, **div)
+                     student_topk_logits=s_ids, grad_dtype=gdt, **div)
         return loss
 
     for _ in range(args.warmup):
@@ -459,7 +462,7 @@ def main():
                                     **div)
             ev[i][1].record(stream)
             fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
-                         student_topk_logits=s_ids, **div)
+                         student_topk_logits=s_ids, grad_dtype=gdt, **div)
             ev[i][2].record(stream)
         end.record(stream)
         barrier()
@@ -508,7 +511,7 @@ def main():
             Hd, idd, zd, md = bufs[b]
             l, s = fkl.forward(Hd, Wt, idd, zd, md, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids, **div)
             fkl.backward(Hd, Wt, idd, zd, md, s, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
-                         student_topk_logits=s_ids, **div)
+                         student_topk_logits=s_ids, grad_dtype=gdt, **div)
             free[b].record(stream)
             hloss.copy_(l, non_blocking=True)
 
@@ -560,7 +563,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "chunk": w.chunk,
-                   "divergence": args.divergence, "l2": "inputs larger than L2 (W is 1.16 GB); no flush"},
+                   "divergence": args.divergence, "grad_dtype": args.grad_dtype,
+                   "l2": "inputs larger than L2 (W is 1.16 GB); no flush"},
         "ms_per_step_median": step_ms_median,
         "tflops": tflops,
         "tensor_frac_step": tflops / sustained,
@@ -575,7 +579,7 @@ def main():
                      "flops_per_launch": kernels[dom]["flops_per_launch"],
                      "ms_per_launch": kernels[dom]["ms_per_launch"],
                      "traffic": traffic_per_launch(dom, kernels[dom]["flops_per_launch"], d)
-                     if (T, V) == (32768, 201088) else None,
+                     if (T, V) == (32768, 201088) and args.grad_dtype == "fp32" else None,
                      "nominal": nominal},
         "kernels": {KIND_NAMES[k]: {kk: round(vv, 4) if isinstance(vv, float) else vv for kk, vv in v.items()}
                     for k, v in kernels.items()},

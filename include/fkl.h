@@ -215,6 +215,30 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
                            void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Backward pass with bfloat16 gradients: the same computation as fkl_backward_ex, with dH
+ * [T, d] and dW [V, d] written as bfloat16 (uint16_t bit patterns, rounded to nearest even)
+ * instead of float.  The sums stay fp32 until their last term: dH of a token block is summed
+ * over the vocabulary slabs in an fp32 buffer in the workspace and rounded when the last
+ * slab is added; dW is rounded when its last token block is added (with several token
+ * blocks its sums live in an fp32 [V, d] buffer in the workspace).  The result equals
+ * fkl_backward_ex's fp32 result rounded to bfloat16, bit for bit.  The bf16 outputs halve
+ * the gradients' memory (dW is 1.16 GB instead of 2.32 GB at V = 201088, d = 2880) and are
+ * what a bf16 model's autograd wants.  opts->accumulate must be 0 (FKL_ERR_INVALID_ARG
+ * otherwise); dH and dW must be 16-byte aligned.  The workspace must hold
+ * fkl_backward_bf16_workspace_size bytes (it serves fkl_forward as well).
+ */
+fkl_status fkl_backward_bf16(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                             const float* topk_logits, const uint8_t* mask, const float* lse,
+                             const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
+                             int64_t chunk, const fkl_options* opts, uint16_t* dH, uint16_t* dW,
+                             void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace fkl_backward_bf16 needs: fkl_workspace_size plus the fp32 sums (Ct x d
+ * floats for dH's token block; V x d more when the backward takes several token blocks).
+ * 0 for invalid shapes. */
+size_t fkl_backward_bf16_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk);
+
+/*
  * Waits for `stream`, then returns the device-side status recorded in `workspace` by the
  * most recent fkl_forward / fkl_backward call that used it (FKL_OK if none failed), or
  * FKL_ERR_CUDA if the wait or the read fails.

@@ -32,8 +32,10 @@ __all__ = ["workspace_size", "Workspace", "forward", "backward", "read_status", 
            "FusedKL", "FklError", "STATUS", "teacher_topk"]
 
 
-def workspace_size(T: int, d: int, V: int, K: int, chunk: int) -> int:
-    n = lib().fkl_workspace_size(T, d, V, K, chunk)
+def workspace_size(T: int, d: int, V: int, K: int, chunk: int, bf16_grads: bool = False) -> int:
+    """Workspace bytes for forward and backward; ``bf16_grads`` sizes it for bf16 gradients."""
+    fn = lib().fkl_backward_bf16_workspace_size if bf16_grads else lib().fkl_workspace_size
+    n = fn(T, d, V, K, chunk)
     if n == 0:
         raise FklError(1, "fkl_workspace_size", f"unsupported shape T={T} d={d} V={V} K={K} chunk={chunk}")
     return int(n)
@@ -49,6 +51,9 @@ class Workspace:
     def get(self, nbytes: int, device) -> torch.Tensor:
         device = torch.device(device)
         if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            # release the old buffer first: both alive at once would raise the peak by its size
+            # (the caching allocator hands it back to this stream only after its queued work)
+            self.buf = None
             self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         return self.buf
 
@@ -164,11 +169,19 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
              out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None, seq_ids: Optional[torch.Tensor] = None,
              num_seqs: Optional[int] = None, accumulate: bool = False, divergence: str = "kl",
              div_param: Optional[float] = None,
-             student_topk_logits: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """dH [T, d] and dW [V, d] (float32), the gradient of g * loss (g = grad_loss or 1).
+             student_topk_logits: Optional[torch.Tensor] = None,
+             grad_dtype: torch.dtype = torch.float32) -> Tuple[torch.Tensor, torch.Tensor]:
+    """dH [T, d] and dW [V, d], the gradient of g * loss (g = grad_loss or 1), in float32 or,
+    with ``grad_dtype=torch.bfloat16``, in bfloat16 (fp32 sums rounded once by the library).
 
-    ``accumulate=True`` adds into the tensors given in ``out`` (gradient accumulation).  For
-    every divergence but "kl", ``student_topk_logits`` is the forward's output of that name."""
+    ``accumulate=True`` adds into the float32 tensors given in ``out`` (gradient
+    accumulation).  For every divergence but "kl", ``student_topk_logits`` is the forward's
+    output of that name."""
+    if grad_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("grad_dtype must be torch.float32 or torch.bfloat16")
+    bf16 = grad_dtype == torch.bfloat16
+    if bf16 and accumulate:
+        raise ValueError("bf16 gradients do not accumulate; use float32 gradients with accumulate=True")
     mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
     T, d = H.shape
     V, K = W.shape[0], topk_idx.shape[1]
@@ -177,23 +190,24 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
         raise ValueError("lse must be a CUDA float32 tensor of shape [T]")
     if grad_loss is not None:
         grad_loss = grad_loss.detach().to(device=H.device, dtype=torch.float32).reshape(()).contiguous()
-    ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk), H.device)
+    ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk, bf16), H.device)
     if out is None:
         if accumulate:
             raise ValueError("accumulate=True needs the gradients to add into, in `out`")
-        dH = torch.empty((T, d), dtype=torch.float32, device=H.device)
-        dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
+        dH = torch.empty((T, d), dtype=grad_dtype, device=H.device)
+        dW = torch.empty((V, d), dtype=grad_dtype, device=H.device)
     else:
         dH, dW = out
         for g, shape in ((dH, (T, d)), (dW, (V, d))):
-            if g.dtype != torch.float32 or tuple(g.shape) != shape or not g.is_contiguous() or g.device != H.device:
-                raise ValueError(f"out gradients must be contiguous float32 {shape} on {H.device}")
+            if g.dtype != grad_dtype or tuple(g.shape) != shape or not g.is_contiguous() or g.device != H.device:
+                raise ValueError(f"out gradients must be contiguous {grad_dtype} {shape} on {H.device}")
     flags = (FKL_ACCUMULATE_DH | FKL_ACCUMULATE_DW) if accumulate else 0
     opts, seq_ids = _options(T, seq_ids, num_seqs, flags, divergence, div_param, student_topk_logits)
-    st = lib().fkl_backward_ex(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask),
-                               _ptr(lse.contiguous()), _ptr(grad_loss), T, d, V, K, float(tau), chunk,
-                               ctypes.byref(opts), _ptr(dH), _ptr(dW), _ptr(ws), ws.numel(), _stream(H.device))
-    check(st, "fkl_backward_ex")
+    fn, name = (lib().fkl_backward_bf16, "fkl_backward_bf16") if bf16 else (lib().fkl_backward_ex, "fkl_backward_ex")
+    st = fn(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask), _ptr(lse.contiguous()),
+            _ptr(grad_loss), T, d, V, K, float(tau), chunk, ctypes.byref(opts), _ptr(dH), _ptr(dW), _ptr(ws),
+            ws.numel(), _stream(H.device))
+    check(st, name)
     return dH, dW
 
 
@@ -224,10 +238,11 @@ class FusedKL(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad):
         H, W, topk_idx, topk_logits, lse = ctx.saved_tensors
+        # H and W are bf16: the library writes bf16 gradients (fp32 sums, rounded once)
         dH, dW = backward(H, W, topk_idx, topk_logits, ctx.mask, lse, grad, ctx.tau, ctx.chunk,
                           seq_ids=ctx.seq_ids, num_seqs=ctx.num_seqs, divergence=ctx.divergence,
-                          div_param=ctx.div_param, student_topk_logits=ctx.s_ids)
-        return dH.to(H.dtype), dW.to(W.dtype), None, None, None, None, None, None, None, None, None
+                          div_param=ctx.div_param, student_topk_logits=ctx.s_ids, grad_dtype=torch.bfloat16)
+        return dH, dW, None, None, None, None, None, None, None, None, None
 
 
 def fused_kl(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,

@@ -58,6 +58,9 @@ _SIGNATURES = {
                                       ctypes.POINTER(FklOptions), _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_backward_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
                                        _I64, ctypes.POINTER(FklOptions), _P, _P, _P, ctypes.c_size_t, _P]),
+    "fkl_backward_bf16": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_float,
+                                       _I64, ctypes.POINTER(FklOptions), _P, _P, _P, ctypes.c_size_t, _P]),
+    "fkl_backward_bf16_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64, _I64]),
     "fkl_teacher_topk_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "fkl_teacher_topk": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P, ctypes.c_size_t, _P]),
     "fkl_test_backward_plan": (ctypes.c_int, [_I64, _I64, _I64, _I64, _I64, ctypes.c_int32, _P]),

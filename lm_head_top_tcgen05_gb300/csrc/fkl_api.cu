@@ -38,7 +38,7 @@ static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; 
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p) {
+bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p, bool bf16_grads) {
   if (T < 0 || T >= (int64_t{1} << 31)) return false;
   if (d < 8 || d % 8 != 0 || d >= (int64_t{1} << 20)) return false;
   if (V < 1 || V > (int64_t{1} << 30)) return false;
@@ -106,6 +106,10 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   p->off_arow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
   p->off_kpart = off;
   if (T > 0) off = align_up(off + static_cast<size_t>(kKsplitSlots) * 256 * 256 * 4, 256);
+  p->off_hsum = off;
+  if (bf16_grads && T > 0) off = align_up(off + static_cast<size_t>(p->Ct) * d * 4, 256);
+  p->off_wsum = off;
+  if (bf16_grads && p->nt > 1) off = align_up(off + static_cast<size_t>(V) * d * 4, 256);
   p->total = off;
   return true;
 }
@@ -412,8 +416,8 @@ static cudaError_t run_weights(const fkl_options* o, const uint8_t* mask, int64_
 
 static fkl_status check_common(const uint16_t* H, const uint16_t* W, const int32_t* idx, const float* z,
                                int64_t T, int64_t d, int64_t V, int64_t K, float tau, int64_t chunk,
-                               void* ws, size_t ws_bytes, Plan* plan) {
-  if (!make_plan(T, d, V, K, chunk, plan))
+                               void* ws, size_t ws_bytes, Plan* plan, bool bf16_grads = false) {
+  if (!make_plan(T, d, V, K, chunk, plan, bf16_grads))
     return fail(FKL_ERR_INVALID_ARG,
                 "unsupported shape T=%lld d=%lld V=%lld K=%lld chunk=%lld (need 0<=T<2^31, d%%8==0, "
                 "8<=d<2^20, 1<=V<=2^30, 1<=K<=1024, chunk>=1)",
@@ -554,6 +558,15 @@ static cudaError_t run_fixup(int bn, const GemmShape& g, const F32Params& p, cud
   return e;
 }
 
+// Gradient outputs of one backward call: fp32 (dH, dW) or bf16 (dH16, dW16).
+struct GradOut {
+  bool bf16;
+  float* dH;
+  float* dW;
+  uint16_t* dH16;
+  uint16_t* dW16;
+};
+
 // The backward's GEMMs, after the light kernels have prepared the pairs, the token weights
 // and the scales in the workspace.  All three products use two-SM tiles (256 rows per CTA
 // pair, B split between the CTAs) over blocks of Ct tokens x Vc vocabulary columns, token
@@ -561,13 +574,15 @@ static cudaError_t run_fixup(int bn, const GemmShape& g, const F32Params& p, cud
 // the slabs, both in a fixed order (deterministic).
 static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const uint16_t* H, const uint16_t* W,
                                       const float* lse, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
-                                      const DivSpec& dv, int accum, uint8_t* ws, float* dH, float* dW,
+                                      const DivSpec& dv, int accum, uint8_t* ws, const GradOut& out,
                                       cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int2* pairs = reinterpret_cast<const int2*>(ws + pl.off_pairs);
   const float* arow = reinterpret_cast<const float*>(ws + pl.off_arow);
   uint16_t* ds = reinterpret_cast<uint16_t*>(ws + pl.off_ds);
   float* kpart = reinterpret_cast<float*>(ws + pl.off_kpart);
+  float* hsum = reinterpret_cast<float*>(ws + pl.off_hsum);  // bf16 gradients: dH of a block over slabs
+  float* wsum = reinterpret_cast<float*>(ws + pl.off_wsum);  // bf16 gradients: dW over token blocks
   cudaError_t e;
   const int bnd = choose_bn_d(d, true);
   const int64_t Vc = pl.Vc;
@@ -616,8 +631,20 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       g4.a_box3d = d3d ? 1 : 0;
       g4.b_box3d = h3d ? 1 : 0;
       F32Params p4;
-      p4.out = dW + v0 * d; p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
-      p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0; p4.vec_ok = aligned(dW, 32) ? 1 : 0;
+      p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
+      if (!out.bf16) {
+        p4.out = out.dW + v0 * d;
+        p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0;
+        p4.vec_ok = aligned(out.dW, 32) ? 1 : 0;
+      } else {
+        // fp32 sums over token blocks in the workspace; the last block rounds them to bf16
+        p4.out = pl.nt > 1 ? wsum + v0 * d : nullptr;
+        p4.accumulate = b > 0 ? 1 : 0;
+        p4.vec_ok = 1;
+        if (b == pl.nt - 1) {
+          p4.out16 = out.dW16 + v0 * d; p4.ldo16 = d; p4.vec16_ok = aligned(out.dW16, 16) ? 1 : 0;
+        }
+      }
       plan_ksplit(&g4, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
@@ -629,8 +656,20 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
       g5.b_box3d = w3d ? 1 : 0;
       F32Params p5;
-      p5.out = dH + r0 * d; p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
-      p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0; p5.vec_ok = aligned(dH, 32) ? 1 : 0;
+      p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
+      if (!out.bf16) {
+        p5.out = out.dH + r0 * d;
+        p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0;
+        p5.vec_ok = aligned(out.dH, 32) ? 1 : 0;
+      } else {
+        // fp32 sums over the slabs in the workspace; the last slab rounds them to bf16
+        p5.out = hsum;
+        p5.accumulate = j > 0 ? 1 : 0;
+        p5.vec_ok = 1;
+        if (j == pl.nslabs - 1) {
+          p5.out16 = out.dH16 + r0 * d; p5.ldo16 = d; p5.vec16_ok = aligned(out.dH16, 16) ? 1 : 0;
+        }
+      }
       plan_ksplit(&g5, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
@@ -651,23 +690,30 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
                          workspace, ws_bytes, stream);
 }
 
-fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
-                           const float* topk_logits, const uint8_t* mask, const float* lse,
-                           const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K,
-                           float tau, int64_t chunk, const fkl_options* opts, float* dH, float* dW,
-                           void* workspace, size_t ws_bytes, void* stream) {
+// The backward of both entry points: fp32 gradients (fkl_backward_ex) or bf16 ones
+// (fkl_backward_bf16), which need the fp32 sums laid out by make_plan(bf16_grads).
+static fkl_status backward_impl(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                                const float* topk_logits, const uint8_t* mask, const float* lse,
+                                const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
+                                int64_t chunk, const fkl_options* opts, const GradOut& out, void* workspace,
+                                size_t ws_bytes, void* stream) {
   g_last_error.clear();
   Plan pl;
-  fkl_status s = check_common(H, W, topk_idx, topk_logits, T, d, V, K, tau, chunk, workspace, ws_bytes, &pl);
+  fkl_status s = check_common(H, W, topk_idx, topk_logits, T, d, V, K, tau, chunk, workspace, ws_bytes, &pl,
+                              out.bf16);
   if (s != FKL_OK) return s;
   if ((s = check_options(opts, T)) != FKL_OK) return s;
   const int accum = opts ? opts->accumulate : 0;
-  if (dW == nullptr || (T > 0 && (dH == nullptr || lse == nullptr)))
+  if (out.bf16 && accum != 0)
+    return fail(FKL_ERR_INVALID_ARG, "bf16 gradients do not accumulate (fkl_options.accumulate must be 0)");
+  const void* gH = out.bf16 ? static_cast<const void*>(out.dH16) : static_cast<const void*>(out.dH);
+  const void* gW = out.bf16 ? static_cast<const void*>(out.dW16) : static_cast<const void*>(out.dW);
+  if (gW == nullptr || (T > 0 && (gH == nullptr || lse == nullptr)))
     return fail(FKL_ERR_INVALID_ARG, "dH, dW and lse must not be NULL");
   const DivSpec dv{opts ? opts->divergence : FKL_DIV_KL, opts ? opts->div_param : 0.f};
   if (dv.kind != FKL_DIV_KL && T > 0 && opts->student_topk_logits == nullptr)
     return fail(FKL_ERR_INVALID_ARG, "this divergence's backward needs fkl_options.student_topk_logits");
-  if (!aligned(dW, 16) || (dH && !aligned(dH, 16))) return fail(FKL_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
+  if (!aligned(gW, 16) || (gH && !aligned(gH, 16))) return fail(FKL_ERR_ALIGNMENT, "dH and dW must be 16-byte aligned");
   if ((lse && !aligned(lse, 4)) || (grad_loss && !aligned(grad_loss, 4)))
     return fail(FKL_ERR_ALIGNMENT, "lse and grad_loss must be 4-byte aligned");
   DevInfo di;
@@ -679,7 +725,8 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
   if (T == 0) {
-    if (!(accum & FKL_ACCUMULATE_DW) && (e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * d * 4, st)) != cudaSuccess)
+    const size_t bytes = static_cast<size_t>(V) * d * (out.bf16 ? 2 : 4);
+    if (!(accum & FKL_ACCUMULATE_DW) && (e = cudaMemsetAsync(const_cast<void*>(gW), 0, bytes, st)) != cudaSuccess)
       return cuda_fail(e, "cudaMemsetAsync(dW)");
     return FKL_OK;
   }
@@ -696,10 +743,34 @@ fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* 
       (e = launch_div_coef(dv, pairs, slot, opts->student_topk_logits, lse, T, (int)K, tau, arow, st)) != cudaSuccess)
     return cuda_fail(e, "divergence kernel");
 
-  if ((s = run_backward_blocks(pl, di, H, W, lse, T, d, V, K, tau, dv, accum, ws, dH, dW, st)) != FKL_OK) return s;
-  if ((e = launch_poison(dH, T * d, dW, V * d, &hdr->status, di.sms, st)) != cudaSuccess)
-    return cuda_fail(e, "poison kernel");
+  if ((s = run_backward_blocks(pl, di, H, W, lse, T, d, V, K, tau, dv, accum, ws, out, st)) != FKL_OK) return s;
+  e = out.bf16 ? launch_poison16(out.dH16, T * d, out.dW16, V * d, &hdr->status, di.sms, st)
+               : launch_poison(out.dH, T * d, out.dW, V * d, &hdr->status, di.sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "poison kernel");
   return FKL_OK;
+}
+
+fkl_status fkl_backward_ex(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                           const float* topk_logits, const uint8_t* mask, const float* lse,
+                           const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K,
+                           float tau, int64_t chunk, const fkl_options* opts, float* dH, float* dW,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  return backward_impl(H, W, topk_idx, topk_logits, mask, lse, grad_loss, T, d, V, K, tau, chunk, opts,
+                       GradOut{false, dH, dW, nullptr, nullptr}, workspace, ws_bytes, stream);
+}
+
+fkl_status fkl_backward_bf16(const uint16_t* H, const uint16_t* W, const int32_t* topk_idx,
+                             const float* topk_logits, const uint8_t* mask, const float* lse,
+                             const float* grad_loss, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
+                             int64_t chunk, const fkl_options* opts, uint16_t* dH, uint16_t* dW,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  return backward_impl(H, W, topk_idx, topk_logits, mask, lse, grad_loss, T, d, V, K, tau, chunk, opts,
+                       GradOut{true, nullptr, nullptr, dH, dW}, workspace, ws_bytes, stream);
+}
+
+size_t fkl_backward_bf16_workspace_size(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk) {
+  Plan p;
+  return make_plan(T, d, V, K, chunk, &p, true) ? p.total : 0;
 }
 
 fkl_status fkl_read_status(const void* workspace, void* stream) {

@@ -309,6 +309,7 @@ struct EpiF32 {
   bool row_ok;
   bool part;  // the tile is one K piece, stored whole to a partial tile (row stride BN)
   float* rowp;
+  uint16_t* rowp16;
 
   __device__ explicit EpiF32(const Params& prm) : p(prm) {}
 
@@ -316,7 +317,42 @@ struct EpiF32 {
     const int r = row0 + row;
     row_ok = r < p.M;
     part = false;
-    rowp = p.out + static_cast<size_t>(row_ok ? r : 0) * p.ldo;
+    const size_t rr = static_cast<size_t>(row_ok ? r : 0);
+    rowp = p.out != nullptr ? p.out + rr * p.ldo : nullptr;
+    rowp16 = p.out16 != nullptr ? p.out16 + rr * p.ldo16 : nullptr;
+  }
+
+  // bf16 destination: adds the fp32 sum so far when accumulating, rounds to nearest even.
+  __device__ __forceinline__ void store16(float (&v)[32], int col0) {
+    const bool full = col0 + 32 <= p.N;
+    if (p.accumulate) {
+      const float* src = rowp + col0;
+      if (p.vec_ok && full) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float y[8];
+          ld_v8(src + 8 * j, y);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[8 * j + i] += y[i];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < p.N) v[j] += src[j];
+      }
+    }
+    uint16_t* o = rowp16 + col0;
+    if (p.vec16_ok && full) {
+      uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o4[j] = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                           pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.N) o[j] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.f) & 0xFFFFu);
+    }
   }
 
   // A K piece: this thread's row of the partial tile at `tile` (ld floats per row).
@@ -336,6 +372,10 @@ struct EpiF32 {
       tmem_ld32(taddr + c * 32, v);
       tmem_ld_wait(v);
       if (!row_ok) continue;
+      if (!part && p.out16 != nullptr) {
+        store16(v, col0);
+        continue;
+      }
       float* o = part ? rowp + c * 32 : rowp + col0;
       if (part || (p.vec_ok && col0 + 32 <= p.N)) {
 #pragma unroll

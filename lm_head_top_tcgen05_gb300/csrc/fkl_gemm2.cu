@@ -57,6 +57,16 @@ __global__ void __launch_bounds__(256) ksplit_fixup_kernel(const GemmShape g, co
       const float4 y = *reinterpret_cast<const float4*>(src + q * tile);
       s.x += y.x; s.y += y.y; s.z += y.z; s.w += y.w;
     }
+    if (p.out16 != nullptr) {  // bf16 destination: (fp32 sum so far +) pieces, rounded once
+      float sv[4] = {s.x, s.y, s.z, s.w};
+      const float* src = p.accumulate ? p.out + static_cast<size_t>(row) * p.ldo + col : nullptr;
+      uint16_t* o16 = p.out16 + static_cast<size_t>(row) * p.ldo16 + col;
+      for (int j = 0; j < 4 && col + j < p.N; ++j) {
+        const float x = src != nullptr ? src[j] + sv[j] : sv[j];
+        o16[j] = static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
+      }
+      continue;
+    }
     float* o = p.out + static_cast<size_t>(row) * p.ldo + col;
     if (p.vec_ok && col + 4 <= p.N) {
       float4* o4 = reinterpret_cast<float4*>(o);

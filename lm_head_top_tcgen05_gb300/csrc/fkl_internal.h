@@ -45,6 +45,8 @@ struct Plan {
   size_t off_sg;    // fp32 [T][K]: student logit at each sorted pair (other divergences)
   size_t off_arow;  // fp32 [T]: per-row factor a_t of dS (other divergences)
   size_t off_kpart; // fp32 partial tiles of K-split dW / dH units
+  size_t off_hsum;  // bf16 gradients only: fp32 [Ct][d], dH of the current token block over slabs
+  size_t off_wsum;  // bf16 gradients with several token blocks: fp32 [V][d], dW over token blocks
   size_t total;
 };
 
@@ -62,7 +64,8 @@ void set_last_error_message(const char* msg);
 void trace_launch_begin(cudaStream_t st);
 void trace_launch_end(cudaStream_t st, int kind, double flops);
 
-bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p);
+// bf16_grads: also lay out the fp32 sums that bf16 gradient outputs need (fkl_backward_bf16).
+bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p, bool bf16_grads = false);
 
 // Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.
 // group: row blocks per group of the unit order (1 = row-major).
@@ -100,6 +103,9 @@ cudaError_t launch_combine(const float* part, int nsplit, const float* crow, con
 cudaError_t launch_grad_scale(const float* grad, float tau, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_poison(float* a, int64_t na, float* b, int64_t nb, const uint32_t* status,
                           int sms, cudaStream_t st);
+// The same for bf16 gradients (NaN = 0x7FC0).
+cudaError_t launch_poison16(uint16_t* a, int64_t na, uint16_t* b, int64_t nb, const uint32_t* status,
+                            int sms, cudaStream_t st);
 cudaError_t launch_wait_timeout_test(uint32_t* status, uint64_t limit_ns, cudaStream_t st);
 
 // ---------------------------------------------------------------- GEMMs
@@ -170,6 +176,11 @@ struct F32Params {
   int M, N;
   int accumulate;
   int vec_ok;  // ldo and base allow 32-byte vector access
+  // bf16 destination: when set, the tile (plus out's fp32 values when accumulating) is
+  // rounded to bf16 and stored here instead of to out.
+  uint16_t* out16 = nullptr;
+  int64_t ldo16 = 0;
+  int vec16_ok = 0;  // ldo16 and out16 allow 16-byte vector access
 };
 
 bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

@@ -605,6 +605,20 @@ cudaError_t launch_poison(float* a, int64_t na, float* b, int64_t nb, const uint
   return cudaGetLastError();
 }
 
+__global__ void poison16_kernel(uint16_t* a, int64_t na, uint16_t* b, int64_t nb, const uint32_t* status) {
+  if (*reinterpret_cast<const volatile uint32_t*>(status) == 0u) return;
+  constexpr uint16_t kNan = 0x7FC0u;  // bf16 quiet NaN
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na; i += stride) a[i] = kNan;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nb; i += stride) b[i] = kNan;
+}
+
+cudaError_t launch_poison16(uint16_t* a, int64_t na, uint16_t* b, int64_t nb, const uint32_t* status,
+                            int sms, cudaStream_t st) {
+  poison16_kernel<<<sms * 4, 256, 0, st>>>(a, na, b, nb, status);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- timeout probe
 __global__ void wait_timeout_kernel(uint32_t* status, uint64_t limit_ns) {
   __shared__ alignas(8) uint64_t bar;

@@ -113,6 +113,30 @@ def test_backward_rejects_bad_arguments_on_host(L):
     assert st == ALIGN    # dH not 16-byte aligned
 
 
+def test_bf16_backward_checks_and_workspace(L):
+    from lm_head_top_tcgen05_gb300._lib import FklOptions
+
+    T, d, V, K, chunk = 4000, 64, 2999, 16, 512
+    n32 = L.fkl_workspace_size(T, d, V, K, chunk)
+    n16 = L.fkl_backward_bf16_workspace_size(T, d, V, K, chunk)
+    Ct, nt = _plan(L, T, d, V, K, chunk)[:2]
+    assert nt > 1 and n16 >= n32 + Ct * d * 4 + V * d * 4    # dH of a block and dW over blocks
+    T1 = 700
+    Ct1, nt1 = _plan(L, T1, d, V, K, chunk)[:2]
+    assert nt1 == 1 and L.fkl_backward_bf16_workspace_size(T1, d, V, K, chunk) >= \
+        L.fkl_workspace_size(T1, d, V, K, chunk) + Ct1 * d * 4
+    assert L.fkl_backward_bf16_workspace_size(T, 12, V, K, chunk) == 0
+    o = FklOptions()
+    o.accumulate = 3
+    # bf16 gradients do not accumulate; the fp32 workspace is too small for bf16 gradients
+    assert L.fkl_backward_bf16(16, 16, 16, 16, None, 16, None, T, d, V, K, 1.0, chunk, ctypes.byref(o), 256, 256,
+                               256, n16, None) == INVALID
+    assert L.fkl_backward_bf16(16, 16, 16, 16, None, 16, None, T, d, V, K, 1.0, chunk, None, 256, 256, 256, n32,
+                               None) == WS
+    assert L.fkl_backward_bf16(16, 16, 16, 16, None, 16, None, T, d, V, K, 1.0, chunk, None, 256 + 8, 256, 256, n16,
+                               None) == ALIGN
+
+
 def test_test_hooks_reject_bad_arguments(L):
     assert L.fkl_test_gemm(16, 16, 16, 0, 8, 8, 0, 0, 256, 0, 256, 256, None) == INVALID
     assert L.fkl_test_gemm(16, 16, 16, 8, 8, 8, 0, 0, 100, 0, 256, 256, None) == INVALID

@@ -177,3 +177,25 @@ def test_long_context_256k_dw_identities(fkl):
         colabs += g.abs().sum(0)
     assert abs(lhs - rhs) <= 1e-3 * scale, (lhs, rhs, scale)
     assert colsum.abs().max().item() <= 1e-3 * colabs.max().item()
+
+
+@pytest.mark.parametrize("name", ["gptoss20b_32k", "gptoss20b_256k"])
+def test_full_size_bf16_gradients(fkl, name):
+    # the bf16 gradient outputs are the fp32 ones rounded to nearest even, bit for bit, with one
+    # token block (32K: dW written once, dH summed over 18 slabs) and with 11 (256K: dW summed
+    # over the token blocks in the workspace)
+    x = workloads.make_inputs(workloads.WORKLOADS[name])
+    dev = "cuda"
+    H, W = x.H.to(dev), x.W.to(dev)
+    idx, z, m = x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev)
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk)
+    dH, dW = fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk)
+    ref_h, ref_w = dH.to(torch.bfloat16), dW.to(torch.bfloat16)
+    del dH, dW
+    dH16, dW16 = fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device=dev) == 0
+    assert torch.equal(dH16.view(torch.int16), ref_h.view(torch.int16))
+    assert torch.equal(dW16.view(torch.int16), ref_w.view(torch.int16))
+    del H, W, idx, z, m, dH16, dW16, ref_h, ref_w
+    torch.cuda.empty_cache()

@@ -312,3 +312,59 @@ def test_gradients_16_but_not_32_byte_aligned(fkl, accumulate):
     assert_grad_close(dH.cpu().numpy().astype(np.float64) - dH0.cpu().numpy(), ref["dH"], "dH")
     assert_grad_close(dW.cpu().numpy().astype(np.float64) - dW0.cpu().numpy(), ref["dW"], "dW")
     assert bh[:4].abs().max().item() == 0 and bw[:4].abs().max().item() == 0
+
+
+# ---------------------------------------------------------------- bf16 gradient outputs
+
+def _bf16_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy()
+
+
+@pytest.mark.parametrize("T,d,V,K,chunk,div", [
+    (300, 136, 3000, 16, 256, "kl"),      # K-split dW and dH, one token block, ragged everywhere
+    (4000, 64, 2999, 16, 512, "kl"),      # several token blocks: dW summed over blocks in fp32
+    (700, 200, 5000, 16, 100000, "kl"),   # one vocabulary slab: dH written once
+    (513, 96, 4100, 12, 64, "jsd"),       # another divergence
+])
+def test_bf16_gradients_are_the_rounded_fp32_ones(fkl, T, d, V, K, chunk, div):
+    # fkl_backward_bf16 keeps fp32 sums and rounds once: bit for bit the fp32 result rounded
+    x = workloads.make_random(T, d, V, K, tau=1.3, chunk=chunk, seed=70 + T % 97, mask_frac=0.1)
+    H, W, idx, z, m = to_dev(x)
+    s = None if div == "kl" else torch.empty((T, K), dtype=torch.float32, device="cuda")
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, chunk, divergence=div, student_topk_logits=s)
+    g = torch.tensor(0.75, device="cuda")
+    dH, dW = fkl.backward(H, W, idx, z, m, lse, g, x.tau, chunk, divergence=div, student_topk_logits=s)
+    dH16, dW16 = fkl.backward(H, W, idx, z, m, lse, g, x.tau, chunk, divergence=div, student_topk_logits=s,
+                              grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 0
+    assert dH16.dtype == torch.bfloat16 and dW16.dtype == torch.bfloat16
+    assert (_bf16_bits(dH16) == _bf16_bits(dH.to(torch.bfloat16))).all()
+    assert (_bf16_bits(dW16) == _bf16_bits(dW.to(torch.bfloat16))).all()
+
+
+def test_bf16_gradients_edge_cases(fkl):
+    x = workloads.make_random(64, 64, 512, 6, seed=19)
+    H, W, idx, z, m = to_dev(x)
+    loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk)
+    # accumulation is fp32 only
+    with pytest.raises(ValueError):
+        fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, grad_dtype=torch.bfloat16, accumulate=True,
+                     out=(torch.zeros(H.shape, dtype=torch.bfloat16, device="cuda"),
+                          torch.zeros(W.shape, dtype=torch.bfloat16, device="cuda")))
+    # T = 0: dW is zero
+    dH, dW = fkl.backward(H[:0], W, idx[:0], z[:0], m[:0], lse[:0], None, x.tau, x.chunk,
+                          grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert dW.dtype == torch.bfloat16 and dW.abs().max().item() == 0 and dH.numel() == 0
+    # a device-side error poisons the bf16 gradients with NaN
+    bad = idx.clone()
+    bad[3, 2] = 512
+    dH, dW = fkl.backward(H, W, bad, z, m, lse, None, x.tau, x.chunk, grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 6
+    assert torch.isnan(dH.float()).all() and torch.isnan(dW.float()).all()
+    assert fkl.read_status(device="cuda") == 6
+    fkl.forward(H, W, idx, z, m, x.tau, x.chunk)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 0
