@@ -567,6 +567,50 @@ struct GradOut {
   uint16_t* dW16;
 };
 
+// Where the dW product of token block b writes slab rows [v0, v0 + w): the caller's fp32 dW
+// (summed over token blocks in order), or, for bf16 gradients, fp32 sums in the workspace
+// (several token blocks) that the last block adds to its tile and rounds to bf16.
+static F32Params dw_output(const Plan& pl, const GradOut& out, int accum, float* wsum, int64_t b, int64_t v0,
+                           int64_t w, int64_t d) {
+  F32Params p;
+  p.ldo = d; p.M = (int)w; p.N = (int)d;
+  if (!out.bf16) {
+    p.out = out.dW + v0 * d;
+    p.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0;
+    p.vec_ok = aligned(out.dW, 32) ? 1 : 0;
+    return p;
+  }
+  p.out = pl.nt > 1 ? wsum + v0 * d : nullptr;
+  p.accumulate = b > 0 ? 1 : 0;
+  p.vec_ok = 1;
+  if (b == pl.nt - 1) {
+    p.out16 = out.dW16 + v0 * d; p.ldo16 = d; p.vec16_ok = aligned(out.dW16, 16) ? 1 : 0;
+  }
+  return p;
+}
+
+// Where the dH product of slab j writes the rows [r0, r0 + rows) of its token block: the
+// caller's fp32 dH (summed over slabs in order), or, for bf16 gradients, an fp32 sum in the
+// workspace that the last slab adds to its tile and rounds to bf16.
+static F32Params dh_output(const Plan& pl, const GradOut& out, int accum, float* hsum, int64_t j, int64_t r0,
+                           int64_t rows, int64_t d) {
+  F32Params p;
+  p.ldo = d; p.M = (int)rows; p.N = (int)d;
+  if (!out.bf16) {
+    p.out = out.dH + r0 * d;
+    p.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0;
+    p.vec_ok = aligned(out.dH, 32) ? 1 : 0;
+    return p;
+  }
+  p.out = hsum;
+  p.accumulate = j > 0 ? 1 : 0;
+  p.vec_ok = 1;
+  if (j == pl.nslabs - 1) {
+    p.out16 = out.dH16 + r0 * d; p.ldo16 = d; p.vec16_ok = aligned(out.dH16, 16) ? 1 : 0;
+  }
+  return p;
+}
+
 // The backward's GEMMs, after the light kernels have prepared the pairs, the token weights
 // and the scales in the workspace.  All three products use two-SM tiles (256 rows per CTA
 // pair, B split between the CTAs) over blocks of Ct tokens x Vc vocabulary columns, token
@@ -630,21 +674,7 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       GemmShape g4 = make_shape(w, d, rows, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
       g4.a_box3d = d3d ? 1 : 0;
       g4.b_box3d = h3d ? 1 : 0;
-      F32Params p4;
-      p4.ldo = d; p4.M = (int)w; p4.N = (int)d;
-      if (!out.bf16) {
-        p4.out = out.dW + v0 * d;
-        p4.accumulate = (b > 0 || (accum & FKL_ACCUMULATE_DW)) ? 1 : 0;
-        p4.vec_ok = aligned(out.dW, 32) ? 1 : 0;
-      } else {
-        // fp32 sums over token blocks in the workspace; the last block rounds them to bf16
-        p4.out = pl.nt > 1 ? wsum + v0 * d : nullptr;
-        p4.accumulate = b > 0 ? 1 : 0;
-        p4.vec_ok = 1;
-        if (b == pl.nt - 1) {
-          p4.out16 = out.dW16 + v0 * d; p4.ldo16 = d; p4.vec16_ok = aligned(out.dW16, 16) ? 1 : 0;
-        }
-      }
+      const F32Params p4 = dw_output(pl, out, accum, wsum, b, v0, w, d);
       plan_ksplit(&g4, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
@@ -655,21 +685,7 @@ static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const u
       // dH[block] (+)= dS[block] W[slab]  (slabs in order).
       GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
       g5.b_box3d = w3d ? 1 : 0;
-      F32Params p5;
-      p5.ldo = d; p5.M = (int)rows; p5.N = (int)d;
-      if (!out.bf16) {
-        p5.out = out.dH + r0 * d;
-        p5.accumulate = (j > 0 || (accum & FKL_ACCUMULATE_DH)) ? 1 : 0;
-        p5.vec_ok = aligned(out.dH, 32) ? 1 : 0;
-      } else {
-        // fp32 sums over the slabs in the workspace; the last slab rounds them to bf16
-        p5.out = hsum;
-        p5.accumulate = j > 0 ? 1 : 0;
-        p5.vec_ok = 1;
-        if (j == pl.nslabs - 1) {
-          p5.out16 = out.dH16 + r0 * d; p5.ldo16 = d; p5.vec16_ok = aligned(out.dH16, 16) ? 1 : 0;
-        }
-      }
+      const F32Params p5 = dh_output(pl, out, accum, hsum, j, r0, rows, d);
       plan_ksplit(&g5, di.sms / 2, kpart, kKsplitSlots);
       trace_launch_begin(st);
       if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
