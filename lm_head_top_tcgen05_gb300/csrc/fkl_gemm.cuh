@@ -182,15 +182,16 @@ struct EpiFwd {
     }
     const float new_m = fmaxf(m2, fmaxf(c0, c1) * p.scale2);
     if (new_m == -INFINITY) return;  // nothing inside the vocabulary yet
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    const float2 sc = make_float2(p.scale2, p.scale2), nm = make_float2(-new_m, -new_m);
+    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
-      s0 += ex2_approx(fmaf(v[j + 0], p.scale2, -new_m));
-      s1 += ex2_approx(fmaf(v[j + 1], p.scale2, -new_m));
-      s2 += ex2_approx(fmaf(v[j + 2], p.scale2, -new_m));
-      s3 += ex2_approx(fmaf(v[j + 3], p.scale2, -new_m));
+      const float2 a01 = ffma2(make_float2(v[j + 0], v[j + 1]), sc, nm);
+      const float2 a23 = ffma2(make_float2(v[j + 2], v[j + 3]), sc, nm);
+      s01 = fadd2(s01, make_float2(ex2_approx(a01.x), ex2_approx(a01.y)));
+      s23 = fadd2(s23, make_float2(ex2_approx(a23.x), ex2_approx(a23.y)));
     }
-    l = fmaf(l, ex2_approx(m2 - new_m), (s0 + s1) + (s2 + s3));
+    l = fmaf(l, ex2_approx(m2 - new_m), (s01.x + s01.y) + (s23.x + s23.y));
     m2 = new_m;
   }
 
@@ -254,8 +255,16 @@ struct EpiDs {
 
   __device__ __forceinline__ void chunk(float (&v)[32], int cl0) {
     const int cg0 = p.v0 + cl0;
+    {
+      const float2 sc = make_float2(p.scale2, p.scale2), nl = make_float2(-lse2, -lse2), aa = make_float2(a, a);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = a * ex2_approx(fmaf(v[j], p.scale2, -lse2));
+      for (int j = 0; j < 32; j += 2) {
+        const float2 x = ffma2(make_float2(v[j], v[j + 1]), sc, nl);
+        const float2 y = fmul2(aa, make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+        v[j] = y.x;
+        v[j + 1] = y.y;
+      }
+    }
     while (cur.nid < cg0 + 32) {  // subtract r at the teacher ids in this chunk (rare)
       const int jt = cur.nid - cg0;
 #pragma unroll
@@ -275,13 +284,17 @@ struct EpiDs {
       for (int j = 0; j < 2; ++j) st_v8(o + 16 * j, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u);
       return;
     }
+    const float2 ff = make_float2(f, f);
+    uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float* q = v + 16 * j;
-      st_v8(o + 16 * j, pack_bf16x2(f * q[0], f * q[1]), pack_bf16x2(f * q[2], f * q[3]),
-            pack_bf16x2(f * q[4], f * q[5]), pack_bf16x2(f * q[6], f * q[7]), pack_bf16x2(f * q[8], f * q[9]),
-            pack_bf16x2(f * q[10], f * q[11]), pack_bf16x2(f * q[12], f * q[13]), pack_bf16x2(f * q[14], f * q[15]));
+    for (int j = 0; j < 16; ++j) {
+      const float2 y = fmul2(ff, make_float2(v[2 * j], v[2 * j + 1]));
+      w[j] = pack_bf16x2(y.x, y.y);
     }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      st_v8(o + 16 * j, w[8 * j], w[8 * j + 1], w[8 * j + 2], w[8 * j + 3], w[8 * j + 4], w[8 * j + 5],
+            w[8 * j + 6], w[8 * j + 7]);
   }
 
   template <int BN>

@@ -304,6 +304,30 @@ __host__ __device__ constexpr uint32_t instr_desc_bf16(int M, int N, bool a_mn, 
 }
 
 // ---------------------------------------------------------------- math helpers
+// Packed fp32 pairs (two independent IEEE operations, round to nearest even, as fmaf /
+// + / * on each lane): half the instructions of the scalar forms.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 A, B, C, D;\n mov.b64 A, {%2, %3};\n mov.b64 B, {%4, %5};\n mov.b64 C, {%6, %7};\n"
+      " fma.rn.f32x2 D, A, B, C;\n mov.b64 {%0, %1}, D;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 A, B, D;\n mov.b64 A, {%2, %3};\n mov.b64 B, {%4, %5};\n"
+      " add.rn.f32x2 D, A, B;\n mov.b64 {%0, %1}, D;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 A, B, D;\n mov.b64 A, {%2, %3};\n mov.b64 B, {%4, %5};\n"
+      " mul.rn.f32x2 D, A, B;\n mov.b64 {%0, %1}, D;\n}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
