@@ -174,13 +174,13 @@ struct EpiFwd {
       if (p.sg != nullptr) p.sg[static_cast<size_t>(t) * p.K + cur.kp] = sv;
       cur.next();
     }
-    float c0 = fmaxf(v[0], v[1]), c1 = fmaxf(v[2], v[3]);
+    float c0 = fmax3(v[0], v[1], v[2]), c1 = fmax3(v[3], v[4], v[5]);
 #pragma unroll
-    for (int j = 4; j < 32; j += 2) {
-      c0 = fmaxf(c0, v[j]);
-      c1 = fmaxf(c1, v[j + 1]);
+    for (int j = 6; j < 30; j += 4) {
+      c0 = fmax3(c0, v[j], v[j + 1]);
+      c1 = fmax3(c1, v[j + 2], v[j + 3]);
     }
-    const float new_m = fmaxf(m2, fmaxf(c0, c1) * p.scale2);
+    const float new_m = fmaxf(m2, fmax3(c0, c1, fmaxf(v[30], v[31])) * p.scale2);
     if (new_m == -INFINITY) return;  // nothing inside the vocabulary yet
     const float2 sc = make_float2(p.scale2, p.scale2), nm = make_float2(-new_m, -new_m);
     float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
