@@ -316,7 +316,10 @@ struct EpiDs {
 };
 
 // ------------------------------------------------------------------ fp32 store epilogue
-struct EpiF32 {
+// kBf16: the tile goes to the bf16 destination (F32Params::out16); a separate instantiation,
+// so that the fp32 product carries none of that path.
+template <bool kBf16>
+struct EpiF32T {
   using Params = F32Params;
   const Params& p;
   bool row_ok;
@@ -324,7 +327,7 @@ struct EpiF32 {
   float* rowp;
   uint16_t* rowp16;
 
-  __device__ explicit EpiF32(const Params& prm) : p(prm) {}
+  __device__ explicit EpiF32T(const Params& prm) : p(prm) {}
 
   __device__ __forceinline__ void begin_unit(int row0, int, int, int row) {
     const int r = row0 + row;
@@ -385,9 +388,11 @@ struct EpiF32 {
       tmem_ld32(taddr + c * 32, v);
       tmem_ld_wait(v);
       if (!row_ok) continue;
-      if (!part && p.out16 != nullptr) {
-        store16(v, col0);
-        continue;
+      if constexpr (kBf16) {
+        if (!part) {
+          store16(v, col0);
+          continue;
+        }
       }
       float* o = part ? rowp + c * 32 : rowp + col0;
       if (part || (p.vec_ok && col0 + 32 <= p.N)) {
@@ -416,6 +421,8 @@ struct EpiF32 {
 
   __device__ __forceinline__ void end_unit(int, int) {}
 };
+using EpiF32 = EpiF32T<false>;
+using EpiF32Bf16 = EpiF32T<true>;
 
 // ------------------------------------------------------------------ the kernel
 template <int BN, bool A_MN, bool B_MN, class Epi>

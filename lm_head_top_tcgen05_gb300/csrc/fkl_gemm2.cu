@@ -18,6 +18,11 @@ cudaError_t launch_gemm2_ds(const CUtensorMap& a, const CUtensorMap& b, const Ge
 template <int BN>
 static cudaError_t dispatch2(bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
                              const GemmShape& g, const F32Params& ep, int sms, cudaStream_t st) {
+  if (ep.out16 != nullptr) {  // bf16 destination: the backward's dW (A, B MN-major) and dH (B MN-major)
+    if (a_mn && b_mn) return launch_gemm2_t<BN, true, true, EpiF32Bf16>(a, b, g, ep, sms, st);
+    if (!a_mn && b_mn) return launch_gemm2_t<BN, false, true, EpiF32Bf16>(a, b, g, ep, sms, st);
+    return cudaErrorInvalidValue;
+  }
   if (!a_mn && !b_mn) return launch_gemm2_t<BN, false, false, EpiF32>(a, b, g, ep, sms, st);
   if (!a_mn && b_mn) return launch_gemm2_t<BN, false, true, EpiF32>(a, b, g, ep, sms, st);
   if (a_mn && !b_mn) return launch_gemm2_t<BN, true, false, EpiF32>(a, b, g, ep, sms, st);

@@ -214,7 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int m_blk, nb, ne, split, kb0, kb1, slot;
       item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
       const int row0 = m_blk * kBM2 + static_cast<int>(rank) * kBM;
-      if constexpr (std::is_same<Epi, EpiF32>::value) {
+      if constexpr (std::is_same<Epi, EpiF32>::value || std::is_same<Epi, EpiF32Bf16>::value) {
         if (slot >= 0)
           epi.begin_part(g.kpart + static_cast<size_t>(slot) * (kBM2 * BN), BN, row0,
                          static_cast<int>(rank) * kBM + row, row);
