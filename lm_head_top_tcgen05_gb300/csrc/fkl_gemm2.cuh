@@ -36,28 +36,193 @@ __host__ __device__ constexpr size_t smem2_bytes_for(int bn) {
   return static_cast<size_t>(stages2_for(bn)) * (kBM * kBK * 2 + (bn / 2) * kBK * 2) + 1024 + 512;
 }
 
+// Shared-memory layout of the two-SM kernel for a B tile of BN rows (BN / 2 per CTA).
+template <int BN, bool B_MN>
+struct PairLayout {
+  static constexpr int STAGES = stages2_for(BN);
+  static constexpr int BNH = BN / 2;                   // rows of B held by each CTA
+  static constexpr uint32_t A_BYTES = kBM * kBK * 2;   // 16 KB
+  static constexpr uint32_t B_BYTES = BNH * kBK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t BOX_BYTES = 64 * kBK * 2;
+  static constexpr bool B_SW64 = b_sw64_for(BN, B_MN);
+  static constexpr uint32_t BOX64_BYTES = 32 * kBK * 2;  // one 32 x 64 MN-major box (64-byte swizzle), 4 KB
+};
+
+// What every role of one CTA of a pair needs: its place in the pair and the grid, the
+// shared-memory ring and barriers, the TMEM accumulators and the bounded-wait control.
+struct PairCtx {
+  uint32_t rank;
+  bool even;
+  int cluster, nclusters;
+  uint32_t stage0, full0, empty0, tfull0, tempty0, drain;
+  uint32_t tmem_base;
+  WaitCtl ctl;
+};
+
+// TMA producer (lane 0 of warp 0, both CTAs): loads this CTA's A rows and half of B into the
+// ring; the even CTA's `full` barrier counts the bytes of both CTAs.
+template <int BN, bool A_MN, bool B_MN>
+__device__ __forceinline__ void pair_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmShape& g,
+                                              const PairCtx& c) {
+  using L = PairLayout<BN, B_MN>;
+  const uint32_t full0_even = map_to_rank(c.full0, 0);  // the pair's `full` barriers
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, issued_par = 0;
+  bool ok = true;
+  const int items = num_items(g);
+  for (int it = c.cluster; ok && it < items; it += c.nclusters) {
+    int m_blk, nb, ne, split, kb0, kb1, slot;
+    item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
+    const int a_row = m_blk * kBM2 + static_cast<int>(c.rank) * kBM;
+    for (int n = nb; ok && n < ne; ++n) {
+      const int b_row = n * BN + static_cast<int>(c.rank) * L::BNH;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        // the slot is released by the even CTA's tensor core (multicast commit)
+        if (!mbar_wait_cluster(c.empty0 + 8 * stage, phase ^ 1u, c.ctl)) { ok = false; break; }
+        const uint32_t fb = full0_even + 8 * stage;
+        const uint32_t sa = c.stage0 + stage * L::STAGE_BYTES;
+        const uint32_t sb = sa + L::A_BYTES;
+        const int k0 = kb * kBK;
+        if (c.even) mbar_arrive_expect_tx(c.full0 + 8 * stage, 2 * L::STAGE_BYTES);
+        if (!A_MN) {
+          tma_load_2d_pair(sa, tmA, fb, k0, a_row);
+        } else if (g.a_box3d) {
+          tma_load_3d_pair(sa, tmA, fb, 0, k0, a_row / 64);
+        } else {
+          tma_load_2d_pair(sa, tmA, fb, a_row, k0);
+          tma_load_2d_pair(sa + L::BOX_BYTES, tmA, fb, a_row + 64, k0);
+        }
+        if (!B_MN) {
+          tma_load_2d_pair(sb, tmB, fb, k0, b_row);
+        } else if (L::B_SW64) {
+          if (g.b_box3d) {
+            tma_load_3d_pair(sb, tmB, fb, 0, k0, b_row / 32);
+          } else {
+#pragma unroll
+            for (int j = 0; j < L::BNH / 32; ++j) tma_load_2d_pair(sb + j * L::BOX64_BYTES, tmB, fb, b_row + j * 32, k0);
+          }
+        } else if (g.b_box3d) {
+          tma_load_3d_pair(sb, tmB, fb, 0, k0, b_row / 64);
+        } else {
+#pragma unroll
+          for (int j = 0; j < L::BNH / 64; ++j) tma_load_2d_pair(sb + j * L::BOX_BYTES, tmB, fb, b_row + j * 64, k0);
+        }
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+  }
+  // The even CTA drains the pair's copies (its `full` phases count both CTAs' bytes).
+  // The odd CTA's copies are covered by those phases; on the abort path its last copy
+  // was issued before a wait that ran for the full time limit.
+  if (c.even)
+    for (int s = 0; s < L::STAGES; ++s)
+      if ((issued >> s) & 1u) mbar_wait_drain(c.full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
+}
+
+// MMA issuer (lane 0 of warp 1, even CTA): 256 x BN x 16 MMAs into one of two TMEM
+// accumulators; commits free ring slots and announce finished tiles to both CTAs.
+template <int BN, bool A_MN, bool B_MN>
+__device__ __forceinline__ void pair_mma(const GemmShape& g, const PairCtx& c) {
+  using L = PairLayout<BN, B_MN>;
+  constexpr uint32_t IDESC = instr_desc_bf16(kBM2, BN, A_MN, B_MN);
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool ok = true;
+  const int items = num_items(g);
+  for (int it = c.cluster; ok && it < items; it += c.nclusters) {
+    int m_blk, nb, ne, split, kb0, kb1, slot;
+    item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
+    for (int n = nb; ok && n < ne; ++n) {
+      if (!mbar_wait_cluster(c.tempty0 + 8 * acc, acc_phase ^ 1u, c.ctl)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = c.tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait_cluster(c.full0 + 8 * stage, phase, c.ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = c.stage0 + stage * L::STAGE_BYTES;
+        const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, L::BOX_BYTES, 1024)
+                                   : smem_desc_sw128(sa + k * 32, 16, 1024);
+          // MN-major B, 64-byte swizzle: 64-byte rows, 8-row groups 512 B apart, atoms 4 KB
+          // apart, 16 rows = 1 KB per step.
+          const uint64_t bd = !B_MN ? smem_desc_sw128(sb + k * 32, 16, 1024)
+                              : L::B_SW64 ? smem_desc(sb + k * 1024, L::BOX64_BYTES, 512, 4u)
+                                       : smem_desc_sw128(sb + k * 2048, L::BOX_BYTES, 1024);
+          tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+        }
+        tc_commit_pair_mc(c.empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
+        if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit_pair_mc(c.tfull0 + 8 * acc, 0x3);  // both halves of the tile are complete
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  tc_commit_pair(c.drain);
+  mbar_wait_drain(c.drain, 0u, g.limit_ns);
+}
+
+// Epilogue (warps 2-5, both CTAs): each warp reads its 32 TMEM lanes of a finished tile,
+// runs the fused epilogue and hands the accumulator back to the even CTA.
+template <int BN, class Epi>
+__device__ __forceinline__ void pair_epilogue(const GemmShape& g, const typename Epi::Params& ep, const PairCtx& c,
+                                              int warp, int lane) {
+  const int row = (warp & 3) * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t remote_tempty0 = map_to_rank(c.tempty0, 0);
+  Epi epi(ep);
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool ok = true;
+  const int items = num_items(g);
+  for (int it = c.cluster; ok && it < items; it += c.nclusters) {
+    int m_blk, nb, ne, split, kb0, kb1, slot;
+    item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
+    const int row0 = m_blk * kBM2 + static_cast<int>(c.rank) * kBM;
+    if constexpr (std::is_same<Epi, EpiF32>::value || std::is_same<Epi, EpiF32Bf16>::value) {
+      if (slot >= 0)
+        epi.begin_part(g.kpart + static_cast<size_t>(slot) * (kBM2 * BN), BN, row0,
+                       static_cast<int>(c.rank) * kBM + row, row);
+      else
+        epi.begin_unit(row0, nb, split, row);
+    } else {
+      epi.begin_unit(row0, nb, split, row);
+    }
+    for (int n = nb; n < ne; ++n) {
+      const bool got = mbar_wait_cluster(c.tfull0 + 8 * acc, acc_phase, c.ctl);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      tc_fence_after();
+      epi.template tile<BN>(c.tmem_base + lane_base + static_cast<uint32_t>(acc * BN), n, row);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(remote_tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (ok) epi.end_unit(split, row);
+  }
+}
+
 template <int BN, bool A_MN, bool B_MN, class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmShape g, const __grid_constant__ typename Epi::Params ep) {
-  constexpr int STAGES = stages2_for(BN);
-  constexpr int BNH = BN / 2;                   // rows of B held by each CTA
-  constexpr uint32_t A_BYTES = kBM * kBK * 2;   // 16 KB
-  constexpr uint32_t B_BYTES = BNH * kBK * 2;
-  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t BOX_BYTES = 64 * kBK * 2;
-  constexpr uint32_t IDESC = instr_desc_bf16(kBM2, BN, A_MN, B_MN);
-  constexpr bool B_SW64 = b_sw64_for(BN, B_MN);
-  constexpr uint32_t BOX64_BYTES = 32 * kBK * 2;  // one 32 x 64 MN-major box (64-byte swizzle), 4 KB
+  using L = PairLayout<BN, B_MN>;
   static_assert(BN == 256 || BN == 192 || BN == 128, "two-SM tiles are 256 x {256, 192, 128}");
-  static_assert(!B_SW64 || (BN / 2) % 32 == 0, "64-byte swizzle halves are whole 32-wide atoms");
+  static_assert(!L::B_SW64 || (BN / 2) % 32 == 0, "64-byte swizzle halves are whole 32-wide atoms");
   static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators must fit in TMEM");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);  // [0] TMEM base, [1] abort
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::STAGES * L::STAGE_BYTES);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * L::STAGES + 5);  // [0] TMEM base, [1] abort
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -67,13 +232,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int nclusters = static_cast<int>(gridDim.x >> 1);
   const uint32_t stage0 = smem_addr(smem);
   const uint32_t full0 = smem_addr(bars);
-  const uint32_t empty0 = full0 + 8 * STAGES;
-  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t empty0 = full0 + 8 * L::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * L::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -100,142 +265,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = misc[0];
   const WaitCtl ctl{reinterpret_cast<volatile uint32_t*>(&misc[1]), g.status, g.limit_ns};
 
+  const PairCtx c{rank, even, cluster, nclusters, stage0, full0, empty0, tfull0, tempty0, drain, tmem_base, ctl};
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0) {
-      const uint32_t full0_even = map_to_rank(full0, 0);  // the pair's `full` barriers
-      int stage = 0;
-      uint32_t phase = 0, issued = 0, issued_par = 0;
-      bool ok = true;
-      const int items = num_items(g);
-      for (int it = cluster; ok && it < items; it += nclusters) {
-        int m_blk, nb, ne, split, kb0, kb1, slot;
-        item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
-        const int a_row = m_blk * kBM2 + static_cast<int>(rank) * kBM;
-        for (int n = nb; ok && n < ne; ++n) {
-          const int b_row = n * BN + static_cast<int>(rank) * BNH;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            // the slot is released by the even CTA's tensor core (multicast commit)
-            if (!mbar_wait_cluster(empty0 + 8 * stage, phase ^ 1u, ctl)) { ok = false; break; }
-            const uint32_t fb = full0_even + 8 * stage;
-            const uint32_t sa = stage0 + stage * STAGE_BYTES;
-            const uint32_t sb = sa + A_BYTES;
-            const int k0 = kb * kBK;
-            if (even) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * STAGE_BYTES);
-            if (!A_MN) {
-              tma_load_2d_pair(sa, &tmA, fb, k0, a_row);
-            } else if (g.a_box3d) {
-              tma_load_3d_pair(sa, &tmA, fb, 0, k0, a_row / 64);
-            } else {
-              tma_load_2d_pair(sa, &tmA, fb, a_row, k0);
-              tma_load_2d_pair(sa + BOX_BYTES, &tmA, fb, a_row + 64, k0);
-            }
-            if (!B_MN) {
-              tma_load_2d_pair(sb, &tmB, fb, k0, b_row);
-            } else if (B_SW64) {
-              if (g.b_box3d) {
-                tma_load_3d_pair(sb, &tmB, fb, 0, k0, b_row / 32);
-              } else {
-#pragma unroll
-                for (int j = 0; j < BNH / 32; ++j) tma_load_2d_pair(sb + j * BOX64_BYTES, &tmB, fb, b_row + j * 32, k0);
-              }
-            } else if (g.b_box3d) {
-              tma_load_3d_pair(sb, &tmB, fb, 0, k0, b_row / 64);
-            } else {
-#pragma unroll
-              for (int j = 0; j < BNH / 64; ++j) tma_load_2d_pair(sb + j * BOX_BYTES, &tmB, fb, b_row + j * 64, k0);
-            }
-            issued |= 1u << stage;
-            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          }
-        }
-      }
-      // The even CTA drains the pair's copies (its `full` phases count both CTAs' bytes).
-      // The odd CTA's copies are covered by those phases; on the abort path its last copy
-      // was issued before a wait that ran for the full time limit.
-      if (even)
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1u) mbar_wait_drain(full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
-    }
+    if (lane == 0) pair_producer<BN, A_MN, B_MN>(&tmA, &tmB, g, c);
   } else if (warp == 1) {
-    if (lane == 0 && even) {
-      // ---------------------------------------------------------- MMA issuer (even CTA)
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      const int items = num_items(g);
-      for (int it = cluster; ok && it < items; it += nclusters) {
-        int m_blk, nb, ne, split, kb0, kb1, slot;
-        item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
-        for (int n = nb; ok && n < ne; ++n) {
-          if (!mbar_wait_cluster(tempty0 + 8 * acc, acc_phase ^ 1u, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait_cluster(full0 + 8 * stage, phase, ctl)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sa = stage0 + stage * STAGE_BYTES;
-            const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, BOX_BYTES, 1024)
-                                       : smem_desc_sw128(sa + k * 32, 16, 1024);
-              // MN-major B, 64-byte swizzle: 64-byte rows, 8-row groups 512 B apart, atoms 4 KB
-              // apart, 16 rows = 1 KB per step.
-              const uint64_t bd = !B_MN ? smem_desc_sw128(sb + k * 32, 16, 1024)
-                                  : B_SW64 ? smem_desc(sb + k * 1024, BOX64_BYTES, 512, 4u)
-                                           : smem_desc_sw128(sb + k * 2048, BOX_BYTES, 1024);
-              tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
-            }
-            tc_commit_pair_mc(empty0 + 8 * stage, 0x3);  // frees the slot in both CTAs
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          }
-          if (!ok) break;
-          tc_commit_pair_mc(tfull0 + 8 * acc, 0x3);  // both halves of the tile are complete
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
-        }
-      }
-      tc_commit_pair(drain);
-      mbar_wait_drain(drain, 0u, g.limit_ns);
-    }
+    if (lane == 0 && even) pair_mma<BN, A_MN, B_MN>(g, c);
   } else {
-    // ------------------------------------------------------------ epilogue (both CTAs)
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t remote_tempty0 = map_to_rank(tempty0, 0);
-    Epi epi(ep);
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    const int items = num_items(g);
-    for (int it = cluster; ok && it < items; it += nclusters) {
-      int m_blk, nb, ne, split, kb0, kb1, slot;
-      item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
-      const int row0 = m_blk * kBM2 + static_cast<int>(rank) * kBM;
-      if constexpr (std::is_same<Epi, EpiF32>::value || std::is_same<Epi, EpiF32Bf16>::value) {
-        if (slot >= 0)
-          epi.begin_part(g.kpart + static_cast<size_t>(slot) * (kBM2 * BN), BN, row0,
-                         static_cast<int>(rank) * kBM + row, row);
-        else
-          epi.begin_unit(row0, nb, split, row);
-      } else {
-        epi.begin_unit(row0, nb, split, row);
-      }
-      for (int n = nb; n < ne; ++n) {
-        const bool got = mbar_wait_cluster(tfull0 + 8 * acc, acc_phase, ctl);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-        tc_fence_after();
-        epi.template tile<BN>(tmem_base + lane_base + static_cast<uint32_t>(acc * BN), n, row);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(remote_tempty0 + 8 * acc);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      }
-      if (ok) epi.end_unit(split, row);
-    }
+    pair_epilogue<BN, Epi>(g, ep, c, warp, lane);
   }
 
   __syncthreads();

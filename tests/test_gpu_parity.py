@@ -86,6 +86,7 @@ CASES = {
     "max_k": (136, 64, 3000, 1024, 1.0, 256, 0.0, 7),
     "min_d": (300, 8, 2000, 16, 1.0, 128, 0.1, 8),
     "d4096": (264, 4096, 2600, 24, 2.0, 512, 0.0, 9),
+    "d8200": (130, 8200, 700, 8, 1.0, 256, 0.0, 14),  # 33 d-tiles, the last 8 columns wide
     "cold_tau": (200, 128, 3000, 16, 0.05, 256, 0.0, 10),
     "hot_tau": (200, 128, 3000, 16, 20.0, 256, 0.0, 11),
     "vocab_below_one_tile": (300, 96, 100, 20, 1.0, 64, 0.0, 12),
