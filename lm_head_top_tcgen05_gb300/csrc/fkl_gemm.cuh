@@ -425,36 +425,168 @@ using EpiF32 = EpiF32T<false>;
 using EpiF32Bf16 = EpiF32T<true>;
 
 // ------------------------------------------------------------------ the kernel
+// Shared-memory layout of the one-SM kernel for a B tile of BN rows.
+template <int BN>
+struct SmLayout {
+  static constexpr int STAGES = stages_for(BN);
+  static constexpr uint32_t A_BYTES = kBM * kBK * 2;  // 16 KB
+  static constexpr uint32_t B_BYTES = BN * kBK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t BOX_BYTES = 64 * kBK * 2;  // one 64 x 64 MN-major box, 8 KB
+};
+
+// What every role of a CTA needs: the shared-memory ring and barriers, the TMEM
+// accumulators and the bounded-wait control.
+struct SmCtx {
+  uint32_t stage0, full0, empty0, tfull0, tempty0, drain;
+  uint32_t tmem_base;
+  WaitCtl ctl;
+};
+
+// TMA producer (lane 0 of warp 0).
+template <int BN, bool A_MN, bool B_MN>
+__device__ __forceinline__ void sm_producer(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmShape& g,
+                                            const SmCtx& c) {
+  using L = SmLayout<BN>;
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, issued_par = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+    int m_blk, nb, ne, split;
+    unit_range(g, u, m_blk, nb, ne, split);
+    for (int n = nb; ok && n < ne; ++n) {
+      for (int kb = 0; kb < g.k_blocks; ++kb) {
+        if (!mbar_wait(c.empty0 + 8 * stage, phase ^ 1u, c.ctl)) { ok = false; break; }
+        const uint32_t fb = c.full0 + 8 * stage;
+        const uint32_t sa = c.stage0 + stage * L::STAGE_BYTES;
+        const uint32_t sb = sa + L::A_BYTES;
+        const int k0 = kb * kBK;
+        mbar_arrive_expect_tx(fb, L::STAGE_BYTES);
+        if (!A_MN) {
+          tma_load_2d(sa, tmA, fb, k0, m_blk * kBM);
+        } else if (g.a_box3d) {
+          tma_load_3d(sa, tmA, fb, 0, k0, m_blk * (kBM / 64));
+        } else {
+          tma_load_2d(sa, tmA, fb, m_blk * kBM, k0);
+          tma_load_2d(sa + L::BOX_BYTES, tmA, fb, m_blk * kBM + 64, k0);
+        }
+        if (!B_MN) {
+          tma_load_2d(sb, tmB, fb, k0, n * BN);
+        } else if (g.b_box3d) {
+          tma_load_3d(sb, tmB, fb, 0, k0, n * (BN / 64));
+        } else {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * L::BOX_BYTES, tmB, fb, n * BN + j * 64, k0);
+        }
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+  }
+  // Every copy this thread started must land before the CTA may exit.
+  for (int s = 0; s < L::STAGES; ++s)
+    if ((issued >> s) & 1u) mbar_wait_drain(c.full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
+}
+
+// MMA issuer (lane 0 of warp 1): 128 x BN x 16 MMAs into one of two TMEM accumulators.
+template <int BN, bool A_MN, bool B_MN>
+__device__ __forceinline__ void sm_mma(const GemmShape& g, const SmCtx& c) {
+  using L = SmLayout<BN>;
+  constexpr uint32_t IDESC = instr_desc_bf16(kBM, BN, A_MN, B_MN);
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+    int m_blk, nb, ne, split;
+    unit_range(g, u, m_blk, nb, ne, split);
+    for (int n = nb; ok && n < ne; ++n) {
+      if (!mbar_wait(c.tempty0 + 8 * acc, acc_phase ^ 1u, c.ctl)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = c.tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < g.k_blocks; ++kb) {
+        if (!mbar_wait(c.full0 + 8 * stage, phase, c.ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = c.stage0 + stage * L::STAGE_BYTES;
+        const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          // K-major: the 16-element step moves 32 bytes along the swizzled 128-byte row.
+          // MN-major: it moves 16 rows of 128 bytes; 64-wide MN blocks are 8 KB apart.
+          const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, L::BOX_BYTES, 1024)
+                                   : smem_desc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, L::BOX_BYTES, 1024)
+                                   : smem_desc_sw128(sb + k * 32, 16, 1024);
+          tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+        }
+        tc_commit(c.empty0 + 8 * stage);  // slot is free once these MMAs have read it
+        if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit(c.tfull0 + 8 * acc);  // accumulator complete
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  // Every MMA issued must finish before TMEM is released.
+  tc_commit(c.drain);
+  mbar_wait_drain(c.drain, 0u, g.limit_ns);
+}
+
+// Epilogue (warps 2-5): each warp reads its 32 TMEM lanes of a finished tile and runs the
+// fused epilogue.
+template <int BN, class Epi>
+__device__ __forceinline__ void sm_epilogue(const GemmShape& g, const typename Epi::Params& ep, const SmCtx& c,
+                                            int warp, int lane) {
+  const int row = (warp & 3) * 32 + lane;  // TMEM lane = row of the 128-row tile
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  Epi epi(ep);
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
+    int m_blk, nb, ne, split;
+    unit_range(g, u, m_blk, nb, ne, split);
+    epi.begin_unit(m_blk * kBM, nb, split, row);
+    for (int n = nb; n < ne; ++n) {
+      const bool got = mbar_wait(c.tfull0 + 8 * acc, acc_phase, c.ctl);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      tc_fence_after();
+      epi.template tile<BN>(c.tmem_base + lane_base + static_cast<uint32_t>(acc * BN), n, row);
+      tc_fence_before();
+      mbar_arrive(c.tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (ok) epi.end_unit(split, row);
+  }
+}
+
 template <int BN, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmShape g, const __grid_constant__ typename Epi::Params ep) {
-  constexpr int STAGES = stages_for(BN);
-  constexpr uint32_t A_BYTES = kBM * kBK * 2;  // 16 KB
-  constexpr uint32_t B_BYTES = BN * kBK * 2;
-  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t BOX_BYTES = 64 * kBK * 2;  // one 64 x 64 MN-major box, 8 KB
-  constexpr uint32_t IDESC = instr_desc_bf16(kBM, BN, A_MN, B_MN);
+  using L = SmLayout<BN>;
   static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators must fit in TMEM");
   static_assert(!B_MN || BN % 64 == 0, "MN-major B is loaded in 64-column boxes");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);  // [0] TMEM base, [1] abort
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::STAGES * L::STAGE_BYTES);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * L::STAGES + 5);  // [0] TMEM base, [1] abort
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t stage0 = smem_addr(smem);
   const uint32_t full0 = smem_addr(bars);
-  const uint32_t empty0 = full0 + 8 * STAGES;
-  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t empty0 = full0 + 8 * L::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * L::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -480,114 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = misc[0];
   const WaitCtl ctl{reinterpret_cast<volatile uint32_t*>(&misc[1]), g.status, g.limit_ns};
 
+  const SmCtx c{stage0, full0, empty0, tfull0, tempty0, drain, tmem_base, ctl};
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, issued = 0, issued_par = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
-        int m_blk, nb, ne, split;
-        unit_range(g, u, m_blk, nb, ne, split);
-        for (int n = nb; ok && n < ne; ++n) {
-          for (int kb = 0; kb < g.k_blocks; ++kb) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, ctl)) { ok = false; break; }
-            const uint32_t fb = full0 + 8 * stage;
-            const uint32_t sa = stage0 + stage * STAGE_BYTES;
-            const uint32_t sb = sa + A_BYTES;
-            const int k0 = kb * kBK;
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            if (!A_MN) {
-              tma_load_2d(sa, &tmA, fb, k0, m_blk * kBM);
-            } else if (g.a_box3d) {
-              tma_load_3d(sa, &tmA, fb, 0, k0, m_blk * (kBM / 64));
-            } else {
-              tma_load_2d(sa, &tmA, fb, m_blk * kBM, k0);
-              tma_load_2d(sa + BOX_BYTES, &tmA, fb, m_blk * kBM + 64, k0);
-            }
-            if (!B_MN) {
-              tma_load_2d(sb, &tmB, fb, k0, n * BN);
-            } else if (g.b_box3d) {
-              tma_load_3d(sb, &tmB, fb, 0, k0, n * (BN / 64));
-            } else {
-#pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmB, fb, n * BN + j * 64, k0);
-            }
-            issued |= 1u << stage;
-            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          }
-        }
-      }
-      // Every copy this thread started must land before the CTA may exit.
-      for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1u) mbar_wait_drain(full0 + 8 * s, (issued_par >> s) & 1u, g.limit_ns);
-    }
+    if (lane == 0) sm_producer<BN, A_MN, B_MN>(&tmA, &tmB, g, c);
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
-        int m_blk, nb, ne, split;
-        unit_range(g, u, m_blk, nb, ne, split);
-        for (int n = nb; ok && n < ne; ++n) {
-          if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, ctl)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kb = 0; kb < g.k_blocks; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, ctl)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sa = stage0 + stage * STAGE_BYTES;
-            const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              // K-major: the 16-element step moves 32 bytes along the swizzled 128-byte row.
-              // MN-major: it moves 16 rows of 128 bytes; 64-wide MN blocks are 8 KB apart.
-              const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, BOX_BYTES, 1024)
-                                       : smem_desc_sw128(sa + k * 32, 16, 1024);
-              const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, BOX_BYTES, 1024)
-                                       : smem_desc_sw128(sb + k * 32, 16, 1024);
-              tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-            }
-            tc_commit(empty0 + 8 * stage);  // slot is free once these MMAs have read it
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          }
-          if (!ok) break;
-          tc_commit(tfull0 + 8 * acc);  // accumulator complete
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
-        }
-      }
-      // Every MMA issued must finish before TMEM is released.
-      tc_commit(drain);
-      mbar_wait_drain(drain, 0u, g.limit_ns);
-    }
+    if (lane == 0) sm_mma<BN, A_MN, B_MN>(g, c);
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int row = (warp & 3) * 32 + lane;  // TMEM lane = row of the 128-row tile
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    Epi epi(ep);
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < g.num_units; u += gridDim.x) {
-      int m_blk, nb, ne, split;
-      unit_range(g, u, m_blk, nb, ne, split);
-      epi.begin_unit(m_blk * kBM, nb, split, row);
-      for (int n = nb; n < ne; ++n) {
-        const bool got = mbar_wait(tfull0 + 8 * acc, acc_phase, ctl);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-        tc_fence_after();
-        epi.template tile<BN>(tmem_base + lane_base + static_cast<uint32_t>(acc * BN), n, row);
-        tc_fence_before();
-        mbar_arrive(tempty0 + 8 * acc);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      }
-      if (ok) epi.end_unit(split, row);
-    }
+    sm_epilogue<BN, Epi>(g, ep, c, warp, lane);
   }
 
   __syncthreads();
