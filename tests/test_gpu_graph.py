@@ -23,8 +23,9 @@ def fkl(cuda_device):
     return m
 
 
-@pytest.mark.parametrize("divergence", ["kl", "jsd"])
-def test_graph_replay_matches_eager(fkl, divergence):
+@pytest.mark.parametrize("divergence,grad_dtype", [("kl", torch.float32), ("jsd", torch.float32),
+                                                   ("kl", torch.bfloat16)])
+def test_graph_replay_matches_eager(fkl, divergence, grad_dtype):
     x = workloads.make_random(600, 320, 9000, 32, tau=1.3, chunk=128, seed=70, mask_frac=0.1)
     y = workloads.make_random(600, 320, 9000, 32, tau=1.3, chunk=128, seed=71, mask_frac=0.2)
     dev = torch.device("cuda")
@@ -33,9 +34,9 @@ def test_graph_replay_matches_eager(fkl, divergence):
     T, d = H.shape
     V, K = W.shape[0], idx.shape[1]
     ws = fkl.Workspace(dev)
-    ws.get(fkl.workspace_size(T, d, V, K, x.chunk), dev)
-    dH = torch.empty(T, d, device=dev)
-    dW = torch.empty(V, d, device=dev)
+    ws.get(fkl.workspace_size(T, d, V, K, x.chunk, grad_dtype == torch.bfloat16), dev)
+    dH = torch.empty(T, d, device=dev, dtype=grad_dtype)
+    dW = torch.empty(V, d, device=dev, dtype=grad_dtype)
     s_ids = torch.empty(T, K, device=dev) if divergence != "kl" else None
     out = {}
 
@@ -43,7 +44,7 @@ def test_graph_replay_matches_eager(fkl, divergence):
         loss, lse = fkl.forward(H, W, idx, z, m, x.tau, x.chunk, workspace=ws, divergence=divergence,
                                 student_topk_logits=s_ids)
         fkl.backward(H, W, idx, z, m, lse, None, x.tau, x.chunk, workspace=ws, out=(dH, dW),
-                     divergence=divergence, student_topk_logits=s_ids)
+                     divergence=divergence, student_topk_logits=s_ids, grad_dtype=grad_dtype)
         out["loss"] = loss
 
     def eager(inp):
