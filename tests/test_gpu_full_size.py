@@ -199,3 +199,43 @@ def test_full_size_bf16_gradients(fkl, name):
     assert torch.equal(dW16.view(torch.int16), ref_w.view(torch.int16))
     del H, W, idx, z, m, dH16, dW16, ref_h, ref_w
     torch.cuda.empty_cache()
+
+
+def test_full_size_memory_has_no_txv_tensor(fkl):
+    # the 32K step in the benchmark's configuration: beyond the inputs, outputs and the
+    # caller's workspace nothing is allocated (the library allocates no device memory, and
+    # no T x V tensor exists anywhere); the whole peak stays far below one bf16 T x V grid
+    w = workloads.WORKLOADS["gptoss20b_32k"]
+    x = workloads.make_inputs(w)
+    dev = "cuda"
+    H, W = x.H.to(dev), x.W.to(dev)
+    idx, z, m = x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev)
+    dH = torch.empty(w.T, w.d, device=dev)
+    dW = torch.empty(w.V, w.d, device=dev)
+    ws = fkl.Workspace(dev)
+    ws.get(fkl.workspace_size(w.T, w.d, w.V, w.K, w.chunk), dev)
+
+    def step():
+        loss, lse = fkl.forward(H, W, idx, z, m, w.tau, w.chunk, workspace=ws)
+        fkl.backward(H, W, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW))
+        return loss
+
+    # first call of the shape: kernels and tensor maps set up, and every module this test
+    # launches from loaded (module loading takes device memory outside any allocator)
+    loss = step()
+    torch.cuda.synchronize()
+    assert fkl.read_status(ws) == 0 and bool(torch.isfinite(loss))
+    del loss
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]
+    torch.cuda.reset_peak_memory_stats(dev)
+    loss = step()
+    torch.cuda.synchronize()
+    assert fkl.read_status(ws) == 0 and bool(torch.isfinite(loss))
+    peak = torch.cuda.max_memory_allocated(dev)
+    assert peak - base < 1 << 20                       # loss and lse only
+    assert abs(torch.cuda.mem_get_info(dev)[0] - free0) < 4 << 20   # nothing allocated outside torch
+    assert peak < w.T * w.V * 2                        # far below one bf16 logits grid
+    del H, W, idx, z, m, dH, dW, ws
+    torch.cuda.empty_cache()
