@@ -369,3 +369,16 @@ def test_bf16_gradients_edge_cases(fkl):
     fkl.forward(H, W, idx, z, m, x.tau, x.chunk)
     torch.cuda.synchronize()
     assert fkl.read_status(device="cuda") == 0
+
+
+def test_vocabulary_of_one(fkl):
+    # V = 1: student and teacher both put all mass on the one entry, so the loss and the
+    # gradients are zero; the kernels get there through lse = s and q = exp(s - lse) = 1 in
+    # fp32, so zero up to rounding
+    x = workloads.make_random(70, 64, 1, 1, tau=1.0, chunk=64, seed=15)
+    g = run_gpu(fkl, x)
+    ref = run_oracle(x)
+    assert g["status"] == 0 and ref["loss"] == 0
+    assert abs(g["loss"]) <= 1e-5
+    assert np.max(np.abs(g["lse"] - ref["lse"])) <= LSE_ATOL
+    assert np.max(np.abs(g["dH"])) <= 1e-5 and np.max(np.abs(g["dW"])) <= 1e-5
