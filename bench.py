@@ -125,6 +125,13 @@ def cpu_oracle_rate(x, rows: int, divergence: str = "kl", div_param=None):
     return rows / dt, dt, cores, np.__version__
 
 
+def loss_config(w, T, d, V, K, args) -> dict:
+    """The `config` of the loss's JSON line, the same for both arms."""
+    return {"workload": w.name, "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "chunk": w.chunk,
+            "divergence": args.divergence, "grad_dtype": args.grad_dtype,
+            "l2": "inputs larger than L2 (W is 1.16 GB); no flush"}
+
+
 def run_reference(args, rank):
     """The comparison arm: the float64 oracle on the host cores, bounded samples of the batch."""
     import workloads
@@ -145,8 +152,7 @@ def run_reference(args, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * w.T / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "d": w.d, "V": w.V, "K": w.K, "tau": w.tau,
-                   "chunk": w.chunk},
+        "config": loss_config(w, w.T, w.d, w.V, w.K, args),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "blas_threads": blas_threads(),
                          "kind": "oracle",
                          "sample": f"first {args.cpu_rows} tokens of the batch per step, full "
@@ -562,9 +568,7 @@ def main():
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "chunk": w.chunk,
-                   "divergence": args.divergence, "grad_dtype": args.grad_dtype,
-                   "l2": "inputs larger than L2 (W is 1.16 GB); no flush"},
+        "config": loss_config(w, T, d, V, K, args),
         "ms_per_step_median": step_ms_median,
         "tflops": tflops,
         "tensor_frac_step": tflops / sustained,
