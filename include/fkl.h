@@ -272,7 +272,7 @@ int32_t fkl_trace_read(float* ms, int32_t* kind, double* flops, int32_t capacity
  * row of s = Ht Wt^T (fp32 accumulation) and their ids, ordered by logit descending, ties by
  * the lower id: topk_idx int32 [T, K] and topk_logits fp32 [T, K] - the cache that
  * fkl_forward reads.  The T x V logits are never written.  A first pass over every s-th
- * vocabulary row (s = 4 for large V; fewer when V is small) finds a per-row lower bound of
+ * vocabulary row (s = 8 for large V; fewer when V is small) finds a per-row lower bound of
  * the K-th largest logit; a second, full projection collects the logits at or above it (at
  * most max(512, 4 s K) per row; more, which needs massive ties or a teacher whose largest
  * logits all avoid the sampled rows, is reported as FKL_ERR_TOPK_OVERFLOW with id -1 and
@@ -288,7 +288,7 @@ fkl_status fkl_teacher_topk(const uint16_t* Ht, const uint16_t* Wt, int64_t T, i
  * fkl_teacher_topk with a cap on the bound pass's sampling stride: max_bound_stride = 1 reads
  * every vocabulary row in the first pass (its bound is then the K-th largest of every split's
  * largest logits, the tightest one, and the second pass collects at most about 4K per row),
- * 2 or 4 allow sampling, 0 is the default (4).  A run that reported FKL_ERR_TOPK_OVERFLOW
+ * 2, 4 or 8 allow sampling, 0 is the default (8).  A run that reported FKL_ERR_TOPK_OVERFLOW
  * because of sampling succeeds with 1.  The workspace of fkl_teacher_topk_workspace_size
  * serves every stride.  Other errors as fkl_teacher_topk, plus FKL_ERR_INVALID_ARG for
  * another max_bound_stride.

@@ -260,7 +260,7 @@ def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int = 100,
     """Offline teacher cache: (topk_idx int32 [T, K], topk_logits float32 [T, K]) of the K
     largest teacher logits Ht Wt^T per row, by logit descending (ties: lower id first).
 
-    ``max_bound_stride`` caps the first pass's vocabulary sampling (0: default 4; 1: every
+    ``max_bound_stride`` caps the first pass's vocabulary sampling (0: default 8; 1: every
     row, for a teacher whose sampled run reported FKL_ERR_TOPK_OVERFLOW)."""
     if not (Ht.is_cuda and Wt.is_cuda) or Ht.dtype != torch.bfloat16 or Wt.dtype != torch.bfloat16:
         raise TypeError("Ht and Wt must be bfloat16 CUDA tensors")

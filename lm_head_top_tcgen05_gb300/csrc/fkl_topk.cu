@@ -36,7 +36,7 @@ namespace fkl {
 
 constexpr int kTopR = 8;                // logits kept per (row, split) in the bound pass
 constexpr int kMaxBoundSplits = 32;     // splits of the bound pass
-constexpr int kMaxBoundStride = 4;      // the bound pass reads every s-th vocabulary row, s <= 4
+constexpr int kMaxBoundStride = 8;      // the bound pass reads every s-th vocabulary row, s <= 8
 constexpr int64_t kAllCandidatesV = 4096;
 
 struct TopRParams {
@@ -224,7 +224,15 @@ __global__ void __launch_bounds__(kBoundWarps * 32)
 
 constexpr int kSelectThreads = 128;
 
-// One block per row: ranks the row's candidates, writes the first K in order.
+// Inverse of rank_key's logit part.
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+  const uint32_t b = ~static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7fffffffu) : ~b);
+}
+
+// One block per row: sorts the row's candidate keys in shared memory with a bitonic network
+// (padded to a power of two with the largest key, which no candidate has) and writes the
+// first K in order.
 __global__ void __launch_bounds__(kSelectThreads)
     select_kernel(const int2* __restrict__ cand, const int* __restrict__ cnt, int cap, int K, int64_t T,
                   int32_t* __restrict__ out_idx, float* __restrict__ out_val, uint32_t* __restrict__ status) {
@@ -243,17 +251,30 @@ __global__ void __launch_bounds__(kSelectThreads)
     return;
   }
   const int2* c = cand + t * cap;
-  for (int i = threadIdx.x; i < total; i += kSelectThreads) keys[i] = rank_key(__int_as_float(c[i].x), c[i].y);
+  int n = 1;
+  while (n < total) n <<= 1;
+  for (int i = threadIdx.x; i < n; i += kSelectThreads)
+    keys[i] = i < total ? rank_key(__int_as_float(c[i].x), c[i].y) : ~0ull;
   __syncthreads();
-  for (int i = threadIdx.x; i < total; i += kSelectThreads) {
-    const unsigned long long ki = keys[i];
-    int rank = 0;
-    for (int j = 0; j < total; ++j) rank += keys[j] < ki;
-    if (rank < K) {
-      const int2 e = c[i];
-      oi[rank] = e.y;
-      ov[rank] = __int_as_float(e.x);
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kSelectThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = keys[i], b = keys[l];
+          if ((a > b) == ((i & k) == 0)) {
+            keys[i] = b;
+            keys[l] = a;
+          }
+        }
+      }
+      __syncthreads();
     }
+  }
+  for (int k = threadIdx.x; k < K; k += kSelectThreads) {
+    const unsigned long long key = keys[k];
+    oi[k] = static_cast<int32_t>(static_cast<uint32_t>(key));
+    ov[k] = key_logit(key);
   }
 }
 
@@ -277,7 +298,7 @@ static int64_t kept_values(int64_t n) {
   return (tiles < kMaxBoundSplits ? tiles : kMaxBoundSplits) * kTopR;
 }
 
-// max_stride: the largest sampling stride of the bound pass the caller allows (1, 2 or 4).
+// max_stride: the largest sampling stride of the bound pass the caller allows (1, 2, 4 or 8).
 static bool make_topk_plan(int64_t T, int64_t d, int64_t V, int64_t K, TopkPlan* p, int max_stride = kMaxBoundStride) {
   if (T < 0 || T >= (int64_t{1} << 31) || d < 8 || d % 8 != 0 || d >= (int64_t{1} << 20)) return false;
   if (V < 1 || V > (int64_t{1} << 30) || K < 1 || K > V) return false;
@@ -325,8 +346,9 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
                                           int64_t K, int32_t max_bound_stride, int32_t* topk_idx, float* topk_logits,
                                           void* workspace, size_t ws_bytes, void* stream) {
   set_last_error_message("");
-  if (max_bound_stride != 0 && max_bound_stride != 1 && max_bound_stride != 2 && max_bound_stride != 4)
-    return topk_fail(FKL_ERR_INVALID_ARG, "max_bound_stride must be 0 (default), 1, 2 or 4");
+  if (max_bound_stride != 0 && max_bound_stride != 1 && max_bound_stride != 2 && max_bound_stride != 4 &&
+      max_bound_stride != 8)
+    return topk_fail(FKL_ERR_INVALID_ARG, "max_bound_stride must be 0 (default), 1, 2, 4 or 8");
   TopkPlan pl;
   if (!make_topk_plan(T, d, V, K, &pl, max_bound_stride == 0 ? kMaxBoundStride : max_bound_stride))
     return topk_fail(FKL_ERR_INVALID_ARG,
@@ -395,7 +417,9 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
   if (launch_gemm2_t<kVocabTile, false, false, EpiCand>(mH, mW, g2, cp, sms, st) != cudaSuccess)
     return topk_fail(FKL_ERR_CUDA, "candidate-pass GEMM launch failed");
   trace_launch_end(st, 6, 2.0 * T * V * d);
-  const size_t smem = static_cast<size_t>(pl.cap) * 8;
+  size_t pow2 = 1;
+  while (pow2 < static_cast<size_t>(pl.cap)) pow2 <<= 1;
+  const size_t smem = pow2 * 8;  // the bitonic sort's keys, padded to a power of two
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return topk_fail(FKL_ERR_CUDA, "cudaFuncSetAttribute failed");

@@ -235,7 +235,7 @@ def test_options_struct_layout_matches_header(tmp_path):
 
 def test_teacher_topk_stride_is_checked_on_host(L):
     n = L.fkl_teacher_topk_workspace_size(64, 64, 8192, 16)
-    for bad in (3, 8, -1):
+    for bad in (3, 16, -1):
         assert L.fkl_teacher_topk_ex(16, 16, 64, 64, 8192, 16, bad, 16, 16, 256, n, None) == INVALID
 
 

@@ -94,7 +94,8 @@ def test_cache_feeds_the_loss(fkl):
 
 
 def test_teacher_whose_top_logits_avoid_the_sampled_rows(fkl):
-    # Every 4th vocabulary row (the rows the default first pass samples) is scaled down: its
+    # Every 4th vocabulary row (every row the default first pass samples is among them) is
+    # scaled down: its
     # bound is loose, far more logits reach it than the buffer holds, and the overflow is
     # reported; the exact first pass (max_bound_stride=1) gives the right cache.
     Ht, Wt = teacher(96, 128, 20000, seed=9)
@@ -108,7 +109,7 @@ def test_teacher_whose_top_logits_avoid_the_sampled_rows(fkl):
     check_cache(Ht, Wt, 100, idx, val)
 
 
-@pytest.mark.parametrize("stride", [1, 2, 4])
+@pytest.mark.parametrize("stride", [1, 2, 4, 8])
 def test_every_bound_stride_gives_the_same_cache(fkl, stride):
     Ht, Wt = teacher(200, 192, 30000, seed=10)
     a = fkl.teacher_topk(Ht.cuda(), Wt.cuda(), 100, max_bound_stride=stride)
