@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kBoundWarps * 32)
   if (lane == 0) theta[t] = th;
 }
 
-constexpr int kSelectThreads = 128;
+constexpr int kSelectThreads = 256;
 
 // Inverse of rank_key's logit part.
 __device__ __forceinline__ float key_logit(unsigned long long key) {
@@ -256,16 +256,16 @@ __global__ void __launch_bounds__(kSelectThreads)
   for (int i = threadIdx.x; i < n; i += kSelectThreads)
     keys[i] = i < total ? rank_key(__int_as_float(c[i].x), c[i].y) : ~0ull;
   __syncthreads();
+  // each step visits the n / 2 compare-exchange pairs (i, i + j) directly
   for (int k = 2; k <= n; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += kSelectThreads) {
-        const int l = i ^ j;
-        if (l > i) {
-          const unsigned long long a = keys[i], b = keys[l];
-          if ((a > b) == ((i & k) == 0)) {
-            keys[i] = b;
-            keys[l] = a;
-          }
+      for (int q = threadIdx.x; q < n / 2; q += kSelectThreads) {
+        const int i = 2 * q - (q & (j - 1));
+        const int l = i + j;
+        const unsigned long long a = keys[i], b = keys[l];
+        if ((a > b) == ((i & k) == 0)) {
+          keys[i] = b;
+          keys[l] = a;
         }
       }
       __syncthreads();
