@@ -106,10 +106,27 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   p->off_arow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
   p->off_kpart = off;
   if (T > 0) off = align_up(off + static_cast<size_t>(kKsplitSlots) * 256 * 256 * 4, 256);
+  // bf16 gradients: with several token blocks, walk the slabs in the outer loop when its
+  // fp32 sums (all of dH, one slab of dW) are smaller than the other order's (one block of
+  // dH, all of dW); the summation orders are the same either way
+  p->slab_outer = false;
+  size_t hsum = 0, wsum = 0;
+  if (bf16_grads && T > 0) {
+    hsum = static_cast<size_t>(p->Ct) * d * 4;
+    if (p->nt > 1) {
+      wsum = static_cast<size_t>(V) * d * 4;
+      const size_t h2 = static_cast<size_t>(T) * d * 4, w2 = static_cast<size_t>(p->Vmax) * d * 4;
+      if (h2 + w2 < hsum + wsum) {
+        p->slab_outer = true;
+        hsum = h2;
+        wsum = w2;
+      }
+    }
+  }
   p->off_hsum = off;
-  if (bf16_grads && T > 0) off = align_up(off + static_cast<size_t>(p->Ct) * d * 4, 256);
+  if (hsum) off = align_up(off + hsum, 256);
   p->off_wsum = off;
-  if (bf16_grads && p->nt > 1) off = align_up(off + static_cast<size_t>(V) * d * 4, 256);
+  if (wsum) off = align_up(off + wsum, 256);
   p->total = off;
   return true;
 }
@@ -569,7 +586,8 @@ struct GradOut {
 
 // Where the dW product of token block b writes slab rows [v0, v0 + w): the caller's fp32 dW
 // (summed over token blocks in order), or, for bf16 gradients, fp32 sums in the workspace
-// (several token blocks) that the last block adds to its tile and rounds to bf16.
+// (several token blocks; all of dW, or the current slab's rows when slabs are the outer
+// loop) that the last block adds to its tile and rounds to bf16.
 static F32Params dw_output(const Plan& pl, const GradOut& out, int accum, float* wsum, int64_t b, int64_t v0,
                            int64_t w, int64_t d) {
   F32Params p;
@@ -580,7 +598,7 @@ static F32Params dw_output(const Plan& pl, const GradOut& out, int accum, float*
     p.vec_ok = aligned(out.dW, 32) ? 1 : 0;
     return p;
   }
-  p.out = pl.nt > 1 ? wsum + v0 * d : nullptr;
+  p.out = pl.nt == 1 ? nullptr : pl.slab_outer ? wsum : wsum + v0 * d;
   p.accumulate = b > 0 ? 1 : 0;
   p.vec_ok = 1;
   if (b == pl.nt - 1) {
@@ -591,7 +609,8 @@ static F32Params dw_output(const Plan& pl, const GradOut& out, int accum, float*
 
 // Where the dH product of slab j writes the rows [r0, r0 + rows) of its token block: the
 // caller's fp32 dH (summed over slabs in order), or, for bf16 gradients, an fp32 sum in the
-// workspace that the last slab adds to its tile and rounds to bf16.
+// workspace (the current block's rows, or all of dH when slabs are the outer loop) that the
+// last slab adds to its tile and rounds to bf16.
 static F32Params dh_output(const Plan& pl, const GradOut& out, int accum, float* hsum, int64_t j, int64_t r0,
                            int64_t rows, int64_t d) {
   F32Params p;
@@ -602,7 +621,7 @@ static F32Params dh_output(const Plan& pl, const GradOut& out, int accum, float*
     p.vec_ok = aligned(out.dH, 32) ? 1 : 0;
     return p;
   }
-  p.out = hsum;
+  p.out = pl.slab_outer ? hsum + r0 * d : hsum;
   p.accumulate = j > 0 ? 1 : 0;
   p.vec_ok = 1;
   if (j == pl.nslabs - 1) {
@@ -611,89 +630,102 @@ static F32Params dh_output(const Plan& pl, const GradOut& out, int accum, float*
   return p;
 }
 
-// The backward's GEMMs, after the light kernels have prepared the pairs, the token weights
-// and the scales in the workspace.  All three products use two-SM tiles (256 rows per CTA
-// pair, B split between the CTAs) over blocks of Ct tokens x Vc vocabulary columns, token
-// blocks outer: dW of a slab accumulates over the token blocks and dH of a token block over
-// the slabs, both in a fixed order (deterministic).
-static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const uint16_t* H, const uint16_t* W,
-                                      const float* lse, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
-                                      const DivSpec& dv, int accum, uint8_t* ws, const GradOut& out,
-                                      cudaStream_t st) {
+// One block of the backward: token block b x vocabulary slab j (the dS recompute, its dW
+// product and its dH product, each K-split fixup after its product).  All three products use
+// two-SM tiles (256 rows per CTA pair, B split between the CTAs).
+static fkl_status run_block(const Plan& pl, const DevInfo& di, const uint16_t* H, const uint16_t* W,
+                           const float* lse, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
+                           const DivSpec& dv, int accum, uint8_t* ws, const GradOut& out, int64_t b, int64_t j,
+                           cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int2* pairs = reinterpret_cast<const int2*>(ws + pl.off_pairs);
   const float* arow = reinterpret_cast<const float*>(ws + pl.off_arow);
   uint16_t* ds = reinterpret_cast<uint16_t*>(ws + pl.off_ds);
   float* kpart = reinterpret_cast<float*>(ws + pl.off_kpart);
-  float* hsum = reinterpret_cast<float*>(ws + pl.off_hsum);  // bf16 gradients: dH of a block over slabs
-  float* wsum = reinterpret_cast<float*>(ws + pl.off_wsum);  // bf16 gradients: dW over token blocks
+  float* hsum = reinterpret_cast<float*>(ws + pl.off_hsum);  // bf16 gradients: dH sums over slabs
+  float* wsum = reinterpret_cast<float*>(ws + pl.off_wsum);  // bf16 gradients: dW sums over token blocks
   cudaError_t e;
   const int bnd = choose_bn_d(d, true);
   const int64_t Vc = pl.Vc;
   const float* wrow = reinterpret_cast<const float*>(ws + pl.off_wrow);
-  for (int64_t b = 0; b < pl.nt; ++b) {
-    const int64_t r0 = b * pl.Ct;
-    const int64_t rows = (T - r0) < pl.Ct ? (T - r0) : pl.Ct;
-    const uint16_t* Hb = H + r0 * d;
-    CUtensorMap mH_k, mH_mn;
-    bool h3d = false;
-    if (!encode_map_bf16(&mH_k, Hb, d, rows, d * 2, 64, 128) || !encode_b_mn_pair(&mH_mn, Hb, d, rows, d * 2, bnd, true, &h3d))
-      return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H block %lld", (long long)b);
-    for (int64_t j = 0; j < pl.nslabs; ++j) {
-      const int64_t v0 = j * Vc;
-      const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
-      const uint16_t* Wj = W + v0 * d;
-      CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
-      // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
-      // 3-D view may span round_up(w, 64) columns.
-      bool w3d = false;
-      const bool wmap = encode_b_mn_pair(&mW_mn, Wj, d, w, d * 2, bnd, true, &w3d);
-      const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, rows, Vc * 2, 128);
-      if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) || !wmap ||
-          (!d3d && !encode_map_bf16(&mD_mn, ds, w, rows, Vc * 2, 64, 64)) ||
-          !encode_map_bf16(&mD_k, ds, w, rows, Vc * 2, 64, 128))
-        return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for block (%lld, %lld)", (long long)b, (long long)j);
+  const int64_t r0 = b * pl.Ct;
+  const int64_t rows = (T - r0) < pl.Ct ? (T - r0) : pl.Ct;
+  const uint16_t* Hb = H + r0 * d;
+  CUtensorMap mH_k, mH_mn;
+  bool h3d = false;
+  if (!encode_map_bf16(&mH_k, Hb, d, rows, d * 2, 64, 128) || !encode_b_mn_pair(&mH_mn, Hb, d, rows, d * 2, bnd, true, &h3d))
+    return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H block %lld", (long long)b);
+  const int64_t v0 = j * Vc;
+  const int64_t w = (V - v0) < Vc ? (V - v0) : Vc;
+  const uint16_t* Wj = W + v0 * d;
+  CUtensorMap mW_k, mW_mn, mD_mn, mD_k;
+  // The dS buffer holds zeros in the columns [w, round_up(w, 256)) of every row, so its
+  // 3-D view may span round_up(w, 64) columns.
+  bool w3d = false;
+  const bool wmap = encode_b_mn_pair(&mW_mn, Wj, d, w, d * 2, bnd, true, &w3d);
+  const bool d3d = encode_map_mn3d(&mD_mn, ds, cdiv(w, 64) * 64, rows, Vc * 2, 128);
+  if (!encode_map_bf16(&mW_k, Wj, d, w, d * 2, 64, kVocabTile / 2) || !wmap ||
+      (!d3d && !encode_map_bf16(&mD_mn, ds, w, rows, Vc * 2, 64, 64)) ||
+      !encode_map_bf16(&mD_k, ds, w, rows, Vc * 2, 64, 128))
+    return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for block (%lld, %lld)", (long long)b, (long long)j);
 
-      // dS[block] = g tau w_t (q - ptilde), recomputing S = H_block W_slab^T.
-      const int m_tiles = (int)cdiv(rows, 256), n_tiles = (int)cdiv(w, kVocabTile);
-      GemmShape g3 = make_shape(rows, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2, group_rows(m_tiles)),
-                                &hdr->status, 256);
-      g3.group_m = group_rows(g3.m_tiles);
-      DsParams dp;
-      dp.pairs = pairs + r0 * K; dp.lse = lse + r0; dp.wrow = wrow + r0;
-      dp.arow = dv.kind != FKL_DIV_KL ? arow + r0 : nullptr;
-      dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
-      dp.T = (int)rows; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
-      dp.scale2 = kLog2e / tau;
-      const double block_flops = 2.0 * rows * w * d;
-      trace_launch_begin(st);
-      if ((e = launch_gemm2_ds(mH_k, mW_k, g3, dp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "dS GEMM");
-      trace_launch_end(st, 1, block_flops);
+  // dS[block] = g tau w_t (q - ptilde), recomputing S = H_block W_slab^T.
+  const int m_tiles = (int)cdiv(rows, 256), n_tiles = (int)cdiv(w, kVocabTile);
+  GemmShape g3 = make_shape(rows, w, d, kVocabTile, plan_splits(m_tiles, n_tiles, di.sms / 2, group_rows(m_tiles)),
+                            &hdr->status, 256);
+  g3.group_m = group_rows(g3.m_tiles);
+  DsParams dp;
+  dp.pairs = pairs + r0 * K; dp.lse = lse + r0; dp.wrow = wrow + r0;
+  dp.arow = dv.kind != FKL_DIV_KL ? arow + r0 : nullptr;
+  dp.hdr = hdr; dp.ds = ds; dp.ld_ds = Vc;
+  dp.T = (int)rows; dp.K = (int)K; dp.V = (int)V; dp.v0 = (int)v0; dp.slab_w = (int)w;
+  dp.scale2 = kLog2e / tau;
+  const double block_flops = 2.0 * rows * w * d;
+  trace_launch_begin(st);
+  if ((e = launch_gemm2_ds(mH_k, mW_k, g3, dp, di.sms, st)) != cudaSuccess) return cuda_fail(e, "dS GEMM");
+  trace_launch_end(st, 1, block_flops);
 
-      // dW[slab] (+)= dS[block]^T H_block  (token blocks in order).
-      GemmShape g4 = make_shape(w, d, rows, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
-      g4.a_box3d = d3d ? 1 : 0;
-      g4.b_box3d = h3d ? 1 : 0;
-      const F32Params p4 = dw_output(pl, out, accum, wsum, b, v0, w, d);
-      plan_ksplit(&g4, di.sms / 2, kpart, kKsplitSlots);
-      trace_launch_begin(st);
-      if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
-        return cuda_fail(e, "dW GEMM");
-      trace_launch_end(st, 2, block_flops);
-      if ((e = run_fixup(bnd, g4, p4, st)) != cudaSuccess) return cuda_fail(e, "dW K-split fixup");
+  // dW[slab] (+)= dS[block]^T H_block  (token blocks in order).
+  GemmShape g4 = make_shape(w, d, rows, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
+  g4.a_box3d = d3d ? 1 : 0;
+  g4.b_box3d = h3d ? 1 : 0;
+  const F32Params p4 = dw_output(pl, out, accum, wsum, b, v0, w, d);
+  plan_ksplit(&g4, di.sms / 2, kpart, kKsplitSlots);
+  trace_launch_begin(st);
+  if ((e = launch_gemm2_f32(bnd, true, true, mD_mn, mH_mn, g4, p4, di.sms, st)) != cudaSuccess)
+    return cuda_fail(e, "dW GEMM");
+  trace_launch_end(st, 2, block_flops);
+  if ((e = run_fixup(bnd, g4, p4, st)) != cudaSuccess) return cuda_fail(e, "dW K-split fixup");
 
-      // dH[block] (+)= dS[block] W[slab]  (slabs in order).
-      GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
-      g5.b_box3d = w3d ? 1 : 0;
-      const F32Params p5 = dh_output(pl, out, accum, hsum, j, r0, rows, d);
-      plan_ksplit(&g5, di.sms / 2, kpart, kKsplitSlots);
-      trace_launch_begin(st);
-      if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
-        return cuda_fail(e, "dH GEMM");
-      trace_launch_end(st, 3, block_flops);
-      if ((e = run_fixup(bnd, g5, p5, st)) != cudaSuccess) return cuda_fail(e, "dH K-split fixup");
+  // dH[block] (+)= dS[block] W[slab]  (slabs in order).
+  GemmShape g5 = make_shape(rows, d, w, bnd, (int)cdiv(d, bnd), &hdr->status, 256);
+  g5.b_box3d = w3d ? 1 : 0;
+  const F32Params p5 = dh_output(pl, out, accum, hsum, j, r0, rows, d);
+  plan_ksplit(&g5, di.sms / 2, kpart, kKsplitSlots);
+  trace_launch_begin(st);
+  if ((e = launch_gemm2_f32(bnd, false, true, mD_k, mW_mn, g5, p5, di.sms, st)) != cudaSuccess)
+    return cuda_fail(e, "dH GEMM");
+  trace_launch_end(st, 3, block_flops);
+  if ((e = run_fixup(bnd, g5, p5, st)) != cudaSuccess) return cuda_fail(e, "dH K-split fixup");
+  return FKL_OK;
+}
+
+// The backward's GEMMs, after the light kernels have prepared the pairs, the token weights
+// and the scales in the workspace: blocks of Ct tokens x Vc vocabulary columns, token blocks
+// outer (slabs outer for bf16 gradients when the plan says so; the same summation orders).
+// dW of a slab accumulates over the token blocks and dH of a token block over the slabs, both
+// in a fixed order (deterministic).
+static fkl_status run_backward_blocks(const Plan& pl, const DevInfo& di, const uint16_t* H, const uint16_t* W,
+                                      const float* lse, int64_t T, int64_t d, int64_t V, int64_t K, float tau,
+                                      const DivSpec& dv, int accum, uint8_t* ws, const GradOut& out,
+                                      cudaStream_t st) {
+  const int64_t outer = pl.slab_outer ? pl.nslabs : pl.nt, inner = pl.slab_outer ? pl.nt : pl.nslabs;
+  for (int64_t o = 0; o < outer; ++o)
+    for (int64_t n = 0; n < inner; ++n) {
+      const int64_t b = pl.slab_outer ? n : o, j = pl.slab_outer ? o : n;
+      const fkl_status s = run_block(pl, di, H, W, lse, T, d, V, K, tau, dv, accum, ws, out, b, j, st);
+      if (s != FKL_OK) return s;
     }
-  }
   return FKL_OK;
 }
 

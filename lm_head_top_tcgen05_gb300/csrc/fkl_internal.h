@@ -39,14 +39,18 @@ struct Plan {
   int64_t Vc;      // vocabulary columns per backward slab (multiple of kVocabTile)
   int64_t Vmax;    // widest slab the dS buffer holds (Vc <= Vmax)
   int64_t nslabs;  // vocabulary slabs of the backward
+  bool slab_outer; // bf16 gradients with several token blocks: slabs in the outer loop
   int64_t nb;      // row blocks of the combine step (256 rows each)
   size_t off_pairs, off_crow, off_wrow, off_scnt, off_part, off_bsum, off_bcnt, off_ds;
   size_t off_slot;  // int32 [T][K]: original slot of each sorted pair
   size_t off_sg;    // fp32 [T][K]: student logit at each sorted pair (other divergences)
   size_t off_arow;  // fp32 [T]: per-row factor a_t of dS (other divergences)
   size_t off_kpart; // fp32 partial tiles of K-split dW / dH units
-  size_t off_hsum;  // bf16 gradients only: fp32 [Ct][d], dH of the current token block over slabs
-  size_t off_wsum;  // bf16 gradients with several token blocks: fp32 [V][d], dW over token blocks
+  // bf16 gradients only: fp32 sums of dH over slabs and of dW over token blocks.  Token
+  // blocks outer: dH of the current block [Ct][d] and all of dW [V][d]; slabs outer (when
+  // that needs less): all of dH [T][d] and dW of the current slab [Vmax][d].
+  size_t off_hsum;
+  size_t off_wsum;
   size_t total;
 };
 

@@ -126,6 +126,13 @@ def test_bf16_backward_checks_and_workspace(L):
     assert nt1 == 1 and L.fkl_backward_bf16_workspace_size(T1, d, V, K, chunk) >= \
         L.fkl_workspace_size(T1, d, V, K, chunk) + Ct1 * d * 4
     assert L.fkl_backward_bf16_workspace_size(T, 12, V, K, chunk) == 0
+    # long sequences against a larger vocabulary: the slabs go outer, and the fp32 sums (all
+    # of dH, one slab of dW) are smaller than one token block of dH plus all of dW
+    T2, V2 = 2000, 3000
+    Ct2, nt2, Vc2, ns2, Vmax2 = _plan(L, T2, d, V2, K, 256)
+    assert nt2 > 1 and ns2 > 1
+    extra = L.fkl_backward_bf16_workspace_size(T2, d, V2, K, 256) - L.fkl_workspace_size(T2, d, V2, K, 256)
+    assert T2 * d * 4 + Vmax2 * d * 4 <= extra < Ct2 * d * 4 + V2 * d * 4
     o = FklOptions()
     o.accumulate = 3
     # bf16 gradients do not accumulate; the fp32 workspace is too small for bf16 gradients

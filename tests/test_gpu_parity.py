@@ -326,6 +326,8 @@ def _bf16_bits(t):
     (4000, 64, 2999, 16, 512, "kl"),      # several token blocks: dW summed over blocks in fp32
     (700, 200, 5000, 16, 100000, "kl"),   # one vocabulary slab: dH written once
     (513, 96, 4100, 12, 64, "jsd"),       # another divergence
+    (2000, 64, 3000, 16, 256, "kl"),      # 3 token blocks x 4 slabs walked slabs outer (less fp32 scratch)
+    (3000, 96, 5000, 12, 256, "jsd"),     # slabs outer, another divergence
 ])
 def test_bf16_gradients_are_the_rounded_fp32_ones(fkl, T, d, V, K, chunk, div):
     # fkl_backward_bf16 keeps fp32 sums and rounds once: bit for bit the fp32 result rounded
