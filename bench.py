@@ -222,8 +222,8 @@ def blas_threads():
 # one ncu capture of a launch of its slab shape (slab width 11264; profiles/
 # bwd_gemms_gptoss20b_32k_slab.md), scaled by work to the mean launch; the forward's from a
 # one-pass capture of the full-size launch itself (profiles/fwd_gemm_gptoss20b_32k_smallV.md).
-TRAFFIC_SOURCES_SHA = "53e079b7c6c7da53"
-TRAFFIC_BYTES = {0: 30.596e9, 1: 1.675e9, 2: 2.259e9, 3: 2.538e9}
+TRAFFIC_SOURCES_SHA = "4f89e5f1eb1250cd"
+TRAFFIC_BYTES = {0: 44.654e9, 1: 1.898e9, 2: 3.095e9, 3: 3.060e9}
 TRAFFIC_FLOPS = {0: 2.0 * 32768 * 201088 * 2880, 1: 2.0 * 32768 * 11264 * 2880,
                  2: 2.0 * 32768 * 11264 * 2880, 3: 2.0 * 32768 * 11264 * 2880}
 
