@@ -23,8 +23,12 @@ d=2880, V=201088, K=100).  Prints one JSON line.
   sample of the same workload (the first rows of the batch, full vocabulary).
 * --impl reference: the oracle alone, on the host cores, as the comparison arm.
 
-Under torchrun each rank runs its own batch on its own GPU (weak scaling); the only
-collective is the max over ranks of the timing.
+Under torchrun (N > 1) each rank holds one token shard of a global batch on its own GPU
+(weak scaling: T tokens per rank), as a data-parallel trainer does: every step sums the
+ranks' valid-token counts with an NCCL all-reduce before the loss (each rank divides by the
+batch's count) and sums dW and the loss over the ranks after the backward
+(lm_head_top_tcgen05_gb300.data_parallel.ShardedStep).  With one GPU the step is the plain
+single-batch forward + backward.
 """
 from __future__ import annotations
 
@@ -183,6 +187,8 @@ KERNEL_NAMES = {0: "gemm2_kernel<256,0,0,EpiFwd> (two-SM)", 1: "gemm2_kernel<256
 # backward prep, 3 token-weight kernels, gradient scale, poison check.  A divergence other
 # than KL adds one per-row kernel to each pass.
 UNTRACED_LAUNCHES_PER_STEP = 12
+# Token-sharded data parallelism (N > 1) adds the local count's two kernels per step.
+LOCAL_COUNT_LAUNCHES = 2
 
 # Dense bf16 tensor-core rate of one Blackwell SM: 4096 FMA = 8192 FLOP per clock (NVIDIA's
 # nominal 2.25 PFLOP/s for GB300 is 152 SMs x 8192 x 1.807 GHz).  The nominal roofline of a
@@ -219,9 +225,8 @@ def blas_threads():
 
 # DRAM bytes (read + write) per launch of each GEMM kind on the 32K workload (T=32768,
 # d=2880, V=201088), valid only for the CUDA sources they were taken on: the backward's from
-# one ncu capture of a launch of its slab shape (slab width 11264; profiles/
-# bwd_gemms_gptoss20b_32k_slab.md), scaled by work to the mean launch; the forward's from a
-# one-pass capture of the full-size launch itself (profiles/fwd_gemm_gptoss20b_32k_smallV.md).
+# one ncu capture of a launch of its slab shape (slab width 11264), scaled by work to the mean
+# launch; the forward's from a one-pass capture of the full-size launch itself.
 TRAFFIC_SOURCES_SHA = "4f89e5f1eb1250cd"
 TRAFFIC_BYTES = {0: 44.654e9, 1: 1.898e9, 2: 3.095e9, 3: 3.060e9}
 TRAFFIC_FLOPS = {0: 2.0 * 32768 * 201088 * 2880, 1: 2.0 * 32768 * 11264 * 2880,
@@ -440,17 +445,36 @@ def main():
     div = dict(divergence=args.divergence, div_param=args.div_param)
     s_ids = torch.empty((T, K), dtype=torch.float32, device=dev) if args.divergence != "kl" else None
 
-    def step():
-        loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids, **div)
-        fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
+    # N > 1: token-sharded data parallelism (count all-reduce before the loss, dW and loss
+    # all-reduce after it); one GPU: the plain step
+    dp = None
+    if world > 1:
+        from lm_head_top_tcgen05_gb300.data_parallel import ShardedStep
+
+        dp = ShardedStep()
+
+    def run_step(Hd, idd, zd, md, ev=None):
+        """One step over the given device inputs; returns the loss (a device scalar)."""
+        if dp is not None:
+            loss, _, _ = dp(Hd, Wt, idd, zd, md, w.tau, w.chunk, workspace=ws, out=(dH, dW), grad_dtype=gdt,
+                            student_topk_logits=s_ids, **div)
+            return loss
+        loss, lse = fkl.forward(Hd, Wt, idd, zd, md, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids, **div)
+        if ev is not None:
+            ev.record(stream)
+        fkl.backward(Hd, Wt, idd, zd, md, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
                      student_topk_logits=s_ids, grad_dtype=gdt, **div)
         return loss
+
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return run_step(H, idx, z, m)
 
     for _ in range(args.warmup):
         step()
     barrier()
     assert fkl.read_status(ws) == 0, "device status not ok after warm-up"
-    stream = torch.cuda.current_stream(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     nslabs = int(fkl.lib().fkl_backward_slabs(T, d, V, K, w.chunk))
     # per step: the forward, three products per backward block and at most one K-split
@@ -464,11 +488,7 @@ def main():
         start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            loss, lse = fkl.forward(H, Wt, idx, z, m, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids,
-                                    **div)
-            ev[i][1].record(stream)
-            fkl.backward(H, Wt, idx, z, m, lse, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
-                         student_topk_logits=s_ids, grad_dtype=gdt, **div)
+            loss = run_step(H, idx, z, m, ev=ev[i][1])
             ev[i][2].record(stream)
         end.record(stream)
         barrier()
@@ -477,8 +497,10 @@ def main():
     kernels = trace_summary(fkl.lib(), trace_cap)
     status = fkl.read_status(ws)
     peak_bytes = torch.cuda.max_memory_allocated(dev)
-    fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
-    bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
+    fwd_ms = bwd_ms = None
+    if dp is None:
+        fwd_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
+        bwd_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
     step_ms_median = statistics.median(ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps))
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     loss_val = loss.item()
@@ -515,9 +537,7 @@ def main():
         def e2e_compute(b):
             stream.wait_event(copied[b])
             Hd, idd, zd, md = bufs[b]
-            l, s = fkl.forward(Hd, Wt, idd, zd, md, w.tau, w.chunk, workspace=ws, student_topk_logits=s_ids, **div)
-            fkl.backward(Hd, Wt, idd, zd, md, s, None, w.tau, w.chunk, workspace=ws, out=(dH, dW),
-                         student_topk_logits=s_ids, grad_dtype=gdt, **div)
+            l = run_step(Hd, idd, zd, md)
             free[b].record(stream)
             hloss.copy_(l, non_blocking=True)
 
@@ -539,7 +559,8 @@ def main():
         barrier()
         e2e_t = max_over_ranks(s0.elapsed_time(s1) / 1e3, dev)
         e2e = {"value": world * T * args.steps / e2e_t, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": 4}
+               "d2h_bytes_per_step": 4,
+               "d2h": "loss read back each step; dH and dW stay resident on the device, as in a training loop"}
 
     if world > 1:
         dist.destroy_process_group()
@@ -553,7 +574,8 @@ def main():
     sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     burst = float(peaks["bf16_tflops"])
     traced = sum(v["launches"] + v["fixup_launches"] for v in kernels.values())
-    launches_per_step = UNTRACED_LAUNCHES_PER_STEP + (2 if args.divergence != "kl" else 0) + traced / args.steps
+    launches_per_step = (UNTRACED_LAUNCHES_PER_STEP + (2 if args.divergence != "kl" else 0)
+                         + (LOCAL_COUNT_LAUNCHES if dp is not None else 0) + traced / args.steps)
     clk = clocks.summary()
     dom = max(kernels, key=lambda k: kernels[k]["ms_total"])  # largest share of the step
     nominal = None
@@ -568,7 +590,10 @@ def main():
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": loss_config(w, T, d, V, K, args),
+        "config": dict(loss_config(w, T, d, V, K, args),
+                       parallelism="single GPU" if world == 1 else
+                       f"token-sharded dp{world}: NCCL all-reduce of the valid-token count before the "
+                       f"loss, of dW and the loss after it; T={T} tokens per rank"),
         "ms_per_step_median": step_ms_median,
         "tflops": tflops,
         "tensor_frac_step": tflops / sustained,

@@ -69,7 +69,8 @@ typedef enum fkl_status {
   FKL_ERR_BAD_TOPK_ROW = 7, /* device: a teacher row has no finite logit */
   FKL_ERR_TIMEOUT = 8,      /* device: a pipeline wait exceeded its time limit */
   FKL_ERR_BAD_SEQ_ID = 9,   /* device: a valid token's sequence id is outside [0, num_seqs) */
-  FKL_ERR_TOPK_OVERFLOW = 10 /* device: fkl_teacher_topk found more tied candidates than it holds */
+  FKL_ERR_TOPK_OVERFLOW = 10, /* device: fkl_teacher_topk found more tied candidates than it holds */
+  FKL_ERR_BAD_COUNT = 11      /* device: fkl_options.global_count is below this call's own count */
 } fkl_status;
 
 /*
@@ -113,6 +114,20 @@ typedef enum fkl_status {
  *                NULL.  fkl_backward_ex reads it for every divergence but FKL_DIV_KL (the
  *                gradient needs q at the ids before the vocabulary sweep), so it must then
  *                hold the forward's values for the same inputs; it is ignored for KL.
+ * global_count   device int64 scalar, or NULL (the default: the call's own count).  The count
+ *                that the mean divides by, taken over the whole batch when the batch is split
+ *                over several calls: token shards on data-parallel ranks, or the micro-batches
+ *                of one accumulated step.  It is the number of valid tokens of the whole batch
+ *                (FKL_NORM_TOKENS), or the number of its sequences with a valid token
+ *                (FKL_NORM_SEQUENCES; each sequence must then lie within one call, which is
+ *                how packed sequences are sharded).  The token weights become
+ *                w_t = 1 / global_count or 1 / (global_count * N_s), so the calls' losses add
+ *                up to the batch's loss and their dH rows and summed dW are the batch's
+ *                gradient.  Sum fkl_local_count over the calls (an all-reduce on the device
+ *                across ranks) to get it; it is read on the device, so no host round trip is
+ *                needed.  If it is below the call's own count the device records
+ *                FKL_ERR_BAD_COUNT (loss NaN, gradients NaN).  8-byte aligned.  The forward
+ *                and the backward of one step must be given the same value.
  */
 enum { FKL_NORM_TOKENS = 0, FKL_NORM_SEQUENCES = 1 };
 enum { FKL_ACCUMULATE_DH = 1, FKL_ACCUMULATE_DW = 2 };
@@ -126,7 +141,28 @@ typedef struct fkl_options {
   float div_param;
   int32_t reserved;  /* must be 0 */
   float* student_topk_logits;
+  const int64_t* global_count;
 } fkl_options;
+
+/*
+ * This call's own count, the term of fkl_options.global_count that this shard contributes:
+ * writes to *count (device int64) the number of valid tokens (FKL_NORM_TOKENS, opts NULL or
+ * opts->normalization = 0), or the number of sequences with a valid token
+ * (FKL_NORM_SEQUENCES, from opts->seq_ids / num_seqs).  Summed over the shards of a batch
+ * (with an all-reduce of the device scalar across data-parallel ranks, or a device add over
+ * micro-batches) it gives the batch's global_count.  The pages' GPT-OSS 20B run trains on
+ * one node of several GPUs and reports per-GPU throughput (the post's "Scaling to long
+ * context lengths"); they do not say how its loss is normalised across GPUs.  The plainest
+ * reading, taken here, is the loss of the whole batch: every shard divides by the batch's
+ * count, not its own.
+ *   mask       uint8 [T], 1 = valid; NULL = all valid
+ *   workspace  device buffer of at least 256 + 4 * max(T, 1) bytes, 256-byte aligned (a
+ *              workspace of fkl_workspace_size for the same T is large enough); a sequence
+ *              id out of range is recorded in it for fkl_read_status (FKL_ERR_BAD_SEQ_ID)
+ * Asynchronous on `stream`; 0 <= T < 2^31.
+ */
+fkl_status fkl_local_count(const uint8_t* mask, int64_t T, const fkl_options* opts, int64_t* count,
+                           void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Bytes of workspace that fkl_forward and fkl_backward need for this shape (one buffer
@@ -188,13 +224,18 @@ fkl_status fkl_backward(const uint16_t* H, const uint16_t* W, const int32_t* top
  * cudaMalloc.  The pages have no counterpart for this entry point: it is a packaging
  * option of this library, not part of the method.
  *
- * Same results and arguments as fkl_forward, without `chunk` (the forward does not depend
- * on it) and without a workspace: the scratch lives in a 64 MiB device array inside the
- * library, which every GPU that loads the library keeps until the process exits.  Shapes
- * whose forward scratch exceeds it (about T * (8K + 400) bytes; T up to about 56K tokens at
- * K = 100) are rejected with FKL_ERR_WORKSPACE and a message in fkl_last_error().
- *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ * Same arguments as fkl_forward, without `chunk` (the forward does not depend on it) and
+ * without a workspace: the scratch lives in a 64 MiB device array inside the library, which
+ * every GPU that loads the library keeps until the process exits.  Shapes whose forward
+ * scratch exceeds it (about T * (8K + 400) bytes; T up to about 56K tokens at K = 100) are
+ * rejected with FKL_ERR_WORKSPACE and a message in fkl_last_error().
+ *   - The results equal fkl_forward's within the parity tolerances (loss relative 1e-3, lse
+ *     absolute 1e-3) but not bit for bit: this path runs the one-SM GEMM, whose vocabulary
+ *     splits differ from the two-SM forward's, so the fp32 partial sums merge in another
+ *     order.  Repeated calls on the same inputs give bitwise the same outputs.
+ *   - The first call on a device sets it up (loads the library's module there, checks the
+ *     device and reads its SM count); make that first call before any stream capture.
+ *     Every call looks up the array's device address with the device current.
  *   - All calls share the one array and it keeps the last call's contents (each call
  *     clears what must start at zero): calls that overlap on the GPU - on different
  *     streams or from different threads - race and must be serialised by the caller.

@@ -15,6 +15,13 @@ divergences than KL(teacher || student) over the same top-K support: ``divergenc
 (``div_param`` = b, default 0.5), ``"skew_kl"`` / ``"skew_rkl"`` (``div_param`` = a, default
 0.1) and ``"tv"``; their backward needs the student logits at the cached ids that the
 forward returns in ``student_topk_logits`` (``fused_kl`` keeps them itself).
+
+A batch split over several calls (token shards on data-parallel ranks, or the micro-batches
+of one accumulated step) is normalised by the whole batch's count: sum ``local_count`` over
+the shards (``all_reduce_count`` across ranks) and pass it as ``global_count`` to every
+shard's forward and backward; the shards' losses then add up to the batch's loss, their dH
+rows are the batch's, and their dW summed (the usual data-parallel gradient all-reduce, or
+``accumulate=True``) is the batch's dW.
 """
 from __future__ import annotations
 
@@ -29,7 +36,7 @@ from ._lib import (DIVERGENCES, FKL_ACCUMULATE_DH, FKL_ACCUMULATE_DW, FKL_NORM_S
 _DEFAULT_PARAM = {"kl": 0.0, "jsd": 0.5, "skew_kl": 0.1, "skew_rkl": 0.1, "tv": 0.0}
 
 __all__ = ["workspace_size", "Workspace", "forward", "backward", "read_status", "fused_kl",
-           "FusedKL", "FklError", "STATUS", "teacher_topk"]
+           "FusedKL", "FklError", "STATUS", "teacher_topk", "local_count", "all_reduce_count"]
 
 
 def workspace_size(T: int, d: int, V: int, K: int, chunk: int, bf16_grads: bool = False) -> int:
@@ -118,15 +125,26 @@ def _student_buf(t: Optional[torch.Tensor], T: int, K: int, device) -> Optional[
     return t
 
 
+def _count_tensor(t: Optional[torch.Tensor], device) -> Optional[torch.Tensor]:
+    if t is None:
+        return None
+    if t.dtype != torch.int64 or t.numel() != 1 or t.device != device:
+        raise ValueError(f"global_count must be a one-element int64 tensor on {device}")
+    return t.reshape(()).contiguous()
+
+
 def _options(T: int, seq_ids: Optional[torch.Tensor], num_seqs: Optional[int], accumulate: int = 0,
              divergence: str = "kl", div_param: Optional[float] = None,
-             student_topk_logits: Optional[torch.Tensor] = None):
-    """fkl_options: sequence-mean normaliser (seq_ids given), accumulation flags, divergence."""
+             student_topk_logits: Optional[torch.Tensor] = None, global_count: Optional[torch.Tensor] = None):
+    """fkl_options: sequence-mean normaliser (seq_ids given), accumulation flags, divergence,
+    the whole batch's count (global_count given)."""
     o = FklOptions()
     o.accumulate = accumulate
     o.divergence, o.div_param = _divergence(divergence, div_param)
     if student_topk_logits is not None:
         o.student_topk_logits = student_topk_logits.data_ptr()
+    if global_count is not None:
+        o.global_count = global_count.data_ptr()
     if seq_ids is not None:
         if seq_ids.dtype != torch.int32 or tuple(seq_ids.shape) != (T,) or not seq_ids.is_cuda:
             raise ValueError("seq_ids must be a CUDA int32 tensor of shape [T]")
@@ -141,21 +159,25 @@ def forward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logit
             mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048,
             workspace: Optional[Workspace] = None, seq_ids: Optional[torch.Tensor] = None,
             num_seqs: Optional[int] = None, divergence: str = "kl", div_param: Optional[float] = None,
-            student_topk_logits: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+            student_topk_logits: Optional[torch.Tensor] = None,
+            global_count: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Loss (0-dim float32) and lse [T] (float32) on H's device and current stream.
 
     With ``seq_ids`` (int32 [T], the packed sequence of each token) the loss is the mean
     over sequences of each sequence's token mean; otherwise the mean over valid tokens.
     ``student_topk_logits`` (float32 [T, K], optional) receives the student's logit at each
-    cached slot; the backward of every divergence but "kl" needs it."""
+    cached slot; the backward of every divergence but "kl" needs it.  ``global_count``
+    (int64 scalar on the device) divides by the whole batch's count instead of this call's
+    own (module docstring)."""
     mask = _check_inputs(H, W, topk_idx, topk_logits, mask)
     T, d = H.shape
     V, K = W.shape[0], topk_idx.shape[1]
     student_topk_logits = _student_buf(student_topk_logits, T, K, H.device)
+    global_count = _count_tensor(global_count, H.device)
     ws = _ws_for(workspace, workspace_size(T, d, V, K, chunk), H.device)
     loss = torch.empty((), dtype=torch.float32, device=H.device)
     lse = torch.empty(T, dtype=torch.float32, device=H.device)
-    opts, seq_ids = _options(T, seq_ids, num_seqs, 0, divergence, div_param, student_topk_logits)
+    opts, seq_ids = _options(T, seq_ids, num_seqs, 0, divergence, div_param, student_topk_logits, global_count)
     st = lib().fkl_forward_ex(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask), T, d, V, K,
                               float(tau), chunk, ctypes.byref(opts), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
                               _stream(H.device))
@@ -170,13 +192,14 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
              num_seqs: Optional[int] = None, accumulate: bool = False, divergence: str = "kl",
              div_param: Optional[float] = None,
              student_topk_logits: Optional[torch.Tensor] = None,
-             grad_dtype: torch.dtype = torch.float32) -> Tuple[torch.Tensor, torch.Tensor]:
+             grad_dtype: torch.dtype = torch.float32,
+             global_count: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """dH [T, d] and dW [V, d], the gradient of g * loss (g = grad_loss or 1), in float32 or,
     with ``grad_dtype=torch.bfloat16``, in bfloat16 (fp32 sums rounded once by the library).
 
     ``accumulate=True`` adds into the float32 tensors given in ``out`` (gradient
     accumulation).  For every divergence but "kl", ``student_topk_logits`` is the forward's
-    output of that name."""
+    output of that name.  ``global_count`` as in ``forward`` (the same value)."""
     if grad_dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("grad_dtype must be torch.float32 or torch.bfloat16")
     bf16 = grad_dtype == torch.bfloat16
@@ -186,6 +209,7 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
     T, d = H.shape
     V, K = W.shape[0], topk_idx.shape[1]
     student_topk_logits = _student_buf(student_topk_logits, T, K, H.device)
+    global_count = _count_tensor(global_count, H.device)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (T,) or not lse.is_cuda:
         raise ValueError("lse must be a CUDA float32 tensor of shape [T]")
     if grad_loss is not None:
@@ -202,7 +226,8 @@ def backward(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logi
             if g.dtype != grad_dtype or tuple(g.shape) != shape or not g.is_contiguous() or g.device != H.device:
                 raise ValueError(f"out gradients must be contiguous {grad_dtype} {shape} on {H.device}")
     flags = (FKL_ACCUMULATE_DH | FKL_ACCUMULATE_DW) if accumulate else 0
-    opts, seq_ids = _options(T, seq_ids, num_seqs, flags, divergence, div_param, student_topk_logits)
+    opts, seq_ids = _options(T, seq_ids, num_seqs, flags, divergence, div_param, student_topk_logits,
+                             global_count)
     fn, name = (lib().fkl_backward_bf16, "fkl_backward_bf16") if bf16 else (lib().fkl_backward_ex, "fkl_backward_ex")
     st = fn(_ptr(H), _ptr(W), _ptr(topk_idx), _ptr(topk_logits), _ptr(mask), _ptr(lse.contiguous()),
             _ptr(grad_loss), T, d, V, K, float(tau), chunk, ctypes.byref(opts), _ptr(dH), _ptr(dW), _ptr(ws),
@@ -218,20 +243,51 @@ def read_status(workspace: Optional[Workspace] = None, device=None) -> int:
     return int(lib().fkl_read_status(_ptr(workspace.buf), _stream(workspace.buf.device)))
 
 
+def local_count(mask: Optional[torch.Tensor], T: int, device=None, seq_ids: Optional[torch.Tensor] = None,
+                num_seqs: Optional[int] = None, workspace: Optional[Workspace] = None) -> torch.Tensor:
+    """This shard's count (int64 scalar on the device, computed by the library): its valid
+    tokens, or with ``seq_ids`` its sequences that have a valid token.  The sum over the
+    shards of a batch is the ``global_count`` of each shard's forward and backward."""
+    if mask is not None:
+        if mask.dtype not in (torch.uint8, torch.bool) or tuple(mask.shape) != (T,) or not mask.is_cuda:
+            raise ValueError("mask must be a CUDA uint8/bool tensor of shape [T]")
+        mask = mask.contiguous().view(torch.uint8)
+        device = mask.device
+    device = _norm(device if device is not None else "cuda")
+    ws = _ws_for(workspace, 256 + 4 * max(T, 1), device)
+    count = torch.empty((), dtype=torch.int64, device=device)
+    opts, seq_ids = _options(T, seq_ids, num_seqs)
+    st = lib().fkl_local_count(_ptr(mask), T, ctypes.byref(opts), _ptr(count), _ptr(ws), ws.numel(), _stream(device))
+    check(st, "fkl_local_count")
+    return count
+
+
+def all_reduce_count(count: torch.Tensor, group=None) -> torch.Tensor:
+    """Sums a shard's count over the ranks of ``group`` (torch.distributed, in place, on the
+    device with NCCL): the whole batch's ``global_count``.  Without an initialised process
+    group, or with one rank, the count is returned as it is."""
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(count, op=dist.ReduceOp.SUM, group=group)
+    return count
+
+
 class FusedKL(torch.autograd.Function):
     """Autograd wrapper: forward saves lse (and, for divergences other than KL, the student
     logits at the cached ids); backward recomputes the projection chunk by chunk."""
 
     @staticmethod
     def forward(ctx, H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=None, num_seqs=None,
-                divergence="kl", div_param=None):
+                divergence="kl", div_param=None, global_count=None):
         s_ids = None
         if divergence != "kl":
             s_ids = torch.empty(topk_idx.shape, dtype=torch.float32, device=H.device)
         loss, lse = forward(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids=seq_ids, num_seqs=num_seqs,
-                            divergence=divergence, div_param=div_param, student_topk_logits=s_ids)
+                            divergence=divergence, div_param=div_param, student_topk_logits=s_ids,
+                            global_count=global_count)
         ctx.save_for_backward(H, W, topk_idx, topk_logits, lse)
-        ctx.mask, ctx.seq_ids, ctx.num_seqs = mask, seq_ids, num_seqs
+        ctx.mask, ctx.seq_ids, ctx.num_seqs, ctx.global_count = mask, seq_ids, num_seqs, global_count
         ctx.tau, ctx.chunk, ctx.divergence, ctx.div_param, ctx.s_ids = tau, chunk, divergence, div_param, s_ids
         return loss
 
@@ -241,18 +297,22 @@ class FusedKL(torch.autograd.Function):
         # H and W are bf16: the library writes bf16 gradients (fp32 sums, rounded once)
         dH, dW = backward(H, W, topk_idx, topk_logits, ctx.mask, lse, grad, ctx.tau, ctx.chunk,
                           seq_ids=ctx.seq_ids, num_seqs=ctx.num_seqs, divergence=ctx.divergence,
-                          div_param=ctx.div_param, student_topk_logits=ctx.s_ids, grad_dtype=torch.bfloat16)
-        return dH, dW, None, None, None, None, None, None, None, None, None
+                          div_param=ctx.div_param, student_topk_logits=ctx.s_ids, grad_dtype=torch.bfloat16,
+                          global_count=ctx.global_count)
+        return dH, dW, None, None, None, None, None, None, None, None, None, None
 
 
 def fused_kl(H: torch.Tensor, W: torch.Tensor, topk_idx: torch.Tensor, topk_logits: torch.Tensor,
              mask: Optional[torch.Tensor] = None, tau: float = 1.0, chunk: int = 2048,
              seq_ids: Optional[torch.Tensor] = None, num_seqs: Optional[int] = None,
-             divergence: str = "kl", div_param: Optional[float] = None) -> torch.Tensor:
+             divergence: str = "kl", div_param: Optional[float] = None,
+             global_count: Optional[torch.Tensor] = None) -> torch.Tensor:
     """tau^2 * KL(teacher top-K || student) averaged over valid tokens (or, with seq_ids, over
     packed sequences of their token means); differentiable in H and W.  ``divergence`` picks
-    another divergence over the same support ("jsd", "skew_kl", "skew_rkl", "tv")."""
-    return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids, num_seqs, divergence, div_param)
+    another divergence over the same support ("jsd", "skew_kl", "skew_rkl", "tv").  With
+    ``global_count`` this is one shard's term of a batch split over several calls."""
+    return FusedKL.apply(H, W, topk_idx, topk_logits, mask, tau, chunk, seq_ids, num_seqs, divergence, div_param,
+                         global_count)
 
 
 def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int = 100,

@@ -22,6 +22,7 @@ STATUS = {
     8: "FKL_ERR_TIMEOUT",
     9: "FKL_ERR_BAD_SEQ_ID",
     10: "FKL_ERR_TOPK_OVERFLOW",
+    11: "FKL_ERR_BAD_COUNT",
 }
 FKL_OK = 0
 
@@ -31,7 +32,7 @@ class FklOptions(ctypes.Structure):
     _fields_ = [("normalization", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
                 ("seq_ids", ctypes.c_void_p), ("accumulate", ctypes.c_int32), ("divergence", ctypes.c_int32),
                 ("div_param", ctypes.c_float), ("reserved", ctypes.c_int32),
-                ("student_topk_logits", ctypes.c_void_p)]
+                ("student_topk_logits", ctypes.c_void_p), ("global_count", ctypes.c_void_p)]
 
 
 FKL_NORM_TOKENS, FKL_NORM_SEQUENCES = 0, 1
@@ -67,6 +68,7 @@ _SIGNATURES = {
     "fkl_teacher_topk_ex": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, ctypes.c_int32, _P, _P, _P,
                                            ctypes.c_size_t, _P]),
     "fkl_read_status": (ctypes.c_int, [_P, _P]),
+    "fkl_local_count": (ctypes.c_int, [_P, _I64, ctypes.POINTER(FklOptions), _P, _P, ctypes.c_size_t, _P]),
     "fkl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fkl_last_error": (ctypes.c_char_p, []),
     "fkl_test_gemm": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,

@@ -413,6 +413,7 @@ static fkl_status check_options(const fkl_options* o, int64_t T) {
   }
   if (!aligned(o->student_topk_logits, 4))
     return fail(FKL_ERR_ALIGNMENT, "fkl_options.student_topk_logits must be 4-byte aligned");
+  if (!aligned(o->global_count, 8)) return fail(FKL_ERR_ALIGNMENT, "fkl_options.global_count must be 8-byte aligned");
   if (o->normalization == FKL_NORM_TOKENS) return FKL_OK;
   if (o->normalization != FKL_NORM_SEQUENCES) return fail(FKL_ERR_INVALID_ARG, "bad fkl_options.normalization");
   if (o->num_seqs < 1 || o->num_seqs > (T > 0 ? T : 1))
@@ -428,7 +429,7 @@ static cudaError_t run_weights(const fkl_options* o, const uint8_t* mask, int64_
   const bool per_seq = o != nullptr && o->normalization == FKL_NORM_SEQUENCES;
   return launch_weights(mask, per_seq ? o->seq_ids : nullptr, per_seq ? o->num_seqs : 1, per_seq ? 1 : 0, T,
                         reinterpret_cast<int*>(ws + pl.off_scnt), hdr, reinterpret_cast<float*>(ws + pl.off_wrow),
-                        st);
+                        o != nullptr ? o->global_count : nullptr, st);
 }
 
 static fkl_status check_common(const uint16_t* H, const uint16_t* W, const int32_t* idx, const float* z,
@@ -486,6 +487,7 @@ const char* fkl_status_string(int status) {
     case FKL_ERR_TIMEOUT: return "device pipeline wait timed out";
     case FKL_ERR_BAD_SEQ_ID: return "sequence id outside [0, num_seqs)";
     case FKL_ERR_TOPK_OVERFLOW: return "too many tied top-K candidates in a row";
+    case FKL_ERR_BAD_COUNT: return "global count below the call's own count";
     default: return "unknown status";
   }
 }
@@ -833,7 +835,34 @@ fkl_status fkl_read_status(const void* workspace, void* stream) {
   if (h & kStatusBadRowBit) return FKL_ERR_BAD_TOPK_ROW;
   if (h & kStatusBadSeqBit) return FKL_ERR_BAD_SEQ_ID;
   if (h & kStatusTopkOverflowBit) return FKL_ERR_TOPK_OVERFLOW;
+  if (h & kStatusBadCountBit) return FKL_ERR_BAD_COUNT;
   if (h & kStatusTimeoutBit) return FKL_ERR_TIMEOUT;
+  return FKL_OK;
+}
+
+fkl_status fkl_local_count(const uint8_t* mask, int64_t T, const fkl_options* opts, int64_t* count,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (T < 0 || T >= (int64_t{1} << 31)) return fail(FKL_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+  fkl_status s = check_options(opts, T);
+  if (s != FKL_OK) return s;
+  if (count == nullptr) return fail(FKL_ERR_INVALID_ARG, "count must not be NULL");
+  if (!aligned(count, 8)) return fail(FKL_ERR_ALIGNMENT, "count must be 8-byte aligned");
+  if (workspace == nullptr) return fail(FKL_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(FKL_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const size_t need = 256 + 4 * static_cast<size_t>(T > 0 ? T : 1);
+  if (ws_bytes < need) return fail(FKL_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  DevInfo di;
+  if ((s = device_info(&di)) != FKL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  const bool per_seq = opts != nullptr && opts->normalization == FKL_NORM_SEQUENCES;
+  if ((e = launch_local_count(mask, per_seq ? opts->seq_ids : nullptr, per_seq ? opts->num_seqs : 1, per_seq ? 1 : 0,
+                              T, reinterpret_cast<int*>(ws + 256), reinterpret_cast<WsHeader*>(ws), count, st)) !=
+      cudaSuccess)
+    return cuda_fail(e, "count kernels");
   return FKL_OK;
 }
 

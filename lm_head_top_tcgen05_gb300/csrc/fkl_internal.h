@@ -14,6 +14,7 @@ constexpr uint32_t kStatusBadRowBit = 2u;
 constexpr uint32_t kStatusTimeoutBit = 4u;
 constexpr uint32_t kStatusBadSeqBit = 8u;
 constexpr uint32_t kStatusTopkOverflowBit = 16u;
+constexpr uint32_t kStatusBadCountBit = 32u;
 
 // Workspace header (first 256 bytes): status word, valid tokens, sequences with a valid
 // token, and g * tau (the backward's dS scale is g * tau * w_t).
@@ -92,8 +93,14 @@ cudaError_t launch_div_rows(DivSpec dv, const int2* pairs, const int* slot, cons
 cudaError_t launch_div_coef(DivSpec dv, int2* pairs, const int* slot, const float* user_s,
                             const float* lse, int64_t T, int K, float tau, float* arow, cudaStream_t st);
 // Token weights w_t into wrow[T] (and N, S into the header); seq may be NULL (one sequence).
+// global_count (device, may be NULL): the whole batch's count (N, or S per_sequence) in place
+// of this call's own; a value below the call's own count sets kStatusBadCountBit.
 cudaError_t launch_weights(const uint8_t* mask, const int32_t* seq, int num_seqs, int per_sequence,
-                           int64_t T, int* cnt, WsHeader* hdr, float* wrow, cudaStream_t st);
+                           int64_t T, int* cnt, WsHeader* hdr, float* wrow, const int64_t* global_count,
+                           cudaStream_t st);
+// This call's own count (N, or S per_sequence) into *count; cnt holds num_seqs ints of scratch.
+cudaError_t launch_local_count(const uint8_t* mask, const int32_t* seq, int num_seqs, int per_sequence,
+                               int64_t T, int* cnt, WsHeader* hdr, int64_t* count, cudaStream_t st);
 // lse_t and the per-block sums of w_t KL_t (launch_combine_rows), then the loss from the
 // block sums (launch_combine_final); launch_combine runs both.
 cudaError_t launch_combine_rows(const float* part, int nsplit, const float* crow, const float* wrow,

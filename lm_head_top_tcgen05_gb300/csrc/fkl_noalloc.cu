@@ -9,8 +9,11 @@
 // the library keeps this array until the process exits.
 //
 // The array's name is only a host-side stand-in for the device symbol: host code must not
-// hand it to a kernel.  Its device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached.
+// hand it to a kernel.  Its device address is looked up with cudaGetSymbolAddress, with the
+// device current.  The first call on a device does the set-up (the library's module is
+// loaded there, and the device's compute capability and SM count are read and kept); every
+// call repeats the address lookup, which is cheap once the module is loaded and allocates
+// nothing, so that a context re-created after cudaDeviceReset never sees a stale address.
 #include <cstdio>
 #include <mutex>
 
@@ -31,31 +34,32 @@ static fkl_status noalloc_fail(fkl_status s, const char* msg) {
   return s;
 }
 
-// Device address of the static scratch on the current device, looked up on first use.
+// Device address of the static scratch on the current device.  The device check and SM count
+// are taken once per device; the address is looked up on every call.
 static fkl_status scratch_address(uint8_t** out, int* sms) {
   static std::mutex mu;
-  static uint8_t* addr[128] = {};
-  static int sm_count[128] = {};
+  static int sm_count[128] = {};  // 0: this device not set up yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
     return noalloc_fail(FKL_ERR_CUDA, "cudaGetDevice failed");
-  std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
-    int major = 0, minor = 0, n = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return noalloc_fail(FKL_ERR_CUDA, "cudaDeviceGetAttribute failed");
-    if (major != 10 || minor != 3) return noalloc_fail(FKL_ERR_UNSUPPORTED, "device is not sm_103");
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, fkl_static_scratch);
-    if (e != cudaSuccess || p == nullptr)
-      return noalloc_fail(FKL_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
-    addr[dev] = static_cast<uint8_t*>(p);
-    sm_count[dev] = n;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (sm_count[dev] == 0) {
+      int major = 0, minor = 0, n = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return noalloc_fail(FKL_ERR_CUDA, "cudaDeviceGetAttribute failed");
+      if (major != 10 || minor != 3) return noalloc_fail(FKL_ERR_UNSUPPORTED, "device is not sm_103");
+      sm_count[dev] = n;
+    }
+    *sms = sm_count[dev];
   }
-  *out = addr[dev];
-  *sms = sm_count[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, fkl_static_scratch);
+  if (e != cudaSuccess || p == nullptr)
+    return noalloc_fail(FKL_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+  *out = static_cast<uint8_t*>(p);
   return FKL_OK;
 }
 
@@ -108,7 +112,8 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
   }
   if (launch_prep(topk_idx, topk_logits, T, (int)K, (int)V, tau, pairs, nullptr, crow, &hdr->status, st) != cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "prep launch failed");
-  if (launch_weights(mask, nullptr, 1, 0, T, reinterpret_cast<int*>(ws + pl.off_scnt), hdr, wrow, st) != cudaSuccess)
+  if (launch_weights(mask, nullptr, 1, 0, T, reinterpret_cast<int*>(ws + pl.off_scnt), hdr, wrow, nullptr, st) !=
+      cudaSuccess)
     return noalloc_fail(FKL_ERR_CUDA, "weights launch failed");
   CUtensorMap mH, mW;
   if (!encode_map_bf16(&mH, H, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, W, d, V, d * 2, 64, kVocabTile))

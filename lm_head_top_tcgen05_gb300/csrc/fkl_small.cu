@@ -4,7 +4,8 @@
 //             the GEMM epilogues can walk them in step with the vocabulary tiles;
 //   weights   the weight w_t of each token's KL in the loss: 1/N (token mean) or
 //             1/(S N_s) (mean over the S packed sequences of each sequence's token mean),
-//             0 for masked tokens; from integer counts, so deterministic;
+//             0 for masked tokens, with N or S the whole batch's when the batch is split
+//             over several calls; from integer counts, so deterministic;
 //   combine   merges the forward's per-split partials into lse_t and KL_t and reduces
 //             sum_t w_t KL_t in a fixed order (no float atomics: deterministic);
 //   div       the other divergences: D_t from the student logits at the cached ids
@@ -524,8 +525,11 @@ __global__ void __launch_bounds__(kWeightThreads)
 }
 
 // N = sum of the counts, S = number of sequences with a valid token (fixed-order tree sums).
+// With a global count (the whole batch's N, or S per_sequence), it must not be below this
+// call's own.  count_out, if not NULL, receives this call's own count.
 __global__ void __launch_bounds__(kFinalThreads)
-    seq_total_kernel(const int* __restrict__ cnt, int num_seqs, WsHeader* hdr) {
+    seq_total_kernel(const int* __restrict__ cnt, int num_seqs, int per_sequence,
+                     const int64_t* __restrict__ global_count, WsHeader* hdr, int64_t* __restrict__ count_out) {
   __shared__ long long sn[kFinalThreads];
   __shared__ int ss[kFinalThreads];
   long long n = 0;
@@ -547,37 +551,55 @@ __global__ void __launch_bounds__(kFinalThreads)
   if (threadIdx.x == 0) {
     hdr->n_valid = static_cast<int32_t>(sn[0]);
     hdr->n_seqs = ss[0];
+    const long long own = per_sequence ? ss[0] : sn[0];
+    if (global_count != nullptr && *global_count < own) atomicOr(&hdr->status, kStatusBadCountBit);
+    if (count_out != nullptr) *count_out = own;
   }
 }
 
 __global__ void __launch_bounds__(kWeightThreads)
     row_weight_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ seq, int64_t T,
                       int num_seqs, int per_sequence, const int* __restrict__ cnt, const WsHeader* hdr,
-                      float* __restrict__ wrow) {
+                      const int64_t* __restrict__ global_count, float* __restrict__ wrow) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kWeightThreads + threadIdx.x;
   if (t >= T) return;
   float w = 0.f;
   const bool valid = mask == nullptr || mask[t] != 0;
   const int sid = seq ? seq[t] : 0;
   if (valid && sid >= 0 && sid < num_seqs) {
-    if (per_sequence) {
-      w = static_cast<float>(1.0 / (static_cast<double>(hdr->n_seqs) * static_cast<double>(cnt[sid])));
-    } else {
-      w = static_cast<float>(1.0 / static_cast<double>(hdr->n_valid));
+    // the mean's count: the whole batch's when given, else this call's own
+    const double count = global_count != nullptr ? static_cast<double>(*global_count)
+                                                 : static_cast<double>(per_sequence ? hdr->n_seqs : hdr->n_valid);
+    if (count > 0.0) {
+      const double per = per_sequence ? count * static_cast<double>(cnt[sid]) : count;
+      w = static_cast<float>(1.0 / per);
     }
   }
   wrow[t] = w;
 }
 
 cudaError_t launch_weights(const uint8_t* mask, const int32_t* seq, int num_seqs, int per_sequence,
-                           int64_t T, int* cnt, WsHeader* hdr, float* wrow, cudaStream_t st) {
+                           int64_t T, int* cnt, WsHeader* hdr, float* wrow, const int64_t* global_count,
+                           cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(num_seqs) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   const unsigned blocks = static_cast<unsigned>((T + kWeightThreads - 1) / kWeightThreads);
   seq_count_kernel<<<blocks, kWeightThreads, 0, st>>>(mask, seq, T, num_seqs, cnt, &hdr->status);
-  seq_total_kernel<<<1, kFinalThreads, 0, st>>>(cnt, num_seqs, hdr);
-  row_weight_kernel<<<blocks, kWeightThreads, 0, st>>>(mask, seq, T, num_seqs, per_sequence, cnt, hdr, wrow);
+  seq_total_kernel<<<1, kFinalThreads, 0, st>>>(cnt, num_seqs, per_sequence, global_count, hdr, nullptr);
+  row_weight_kernel<<<blocks, kWeightThreads, 0, st>>>(mask, seq, T, num_seqs, per_sequence, cnt, hdr,
+                                                      global_count, wrow);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_local_count(const uint8_t* mask, const int32_t* seq, int num_seqs, int per_sequence,
+                               int64_t T, int* cnt, WsHeader* hdr, int64_t* count, cudaStream_t st) {
+  if (T == 0) return cudaMemsetAsync(count, 0, sizeof(int64_t), st);
+  cudaError_t e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(num_seqs) * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = static_cast<unsigned>((T + kWeightThreads - 1) / kWeightThreads);
+  seq_count_kernel<<<blocks, kWeightThreads, 0, st>>>(mask, seq, T, num_seqs, cnt, &hdr->status);
+  seq_total_kernel<<<1, kFinalThreads, 0, st>>>(cnt, num_seqs, per_sequence, nullptr, hdr, count);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,14 @@ number of sequences with N_s > 0,
 i.e. every token carries the weight w_t = 1 / (S N_{s(t)}) instead of 1 / N, and the gradient
 is the same expression with tau / N replaced by tau * w_t.
 
+A batch split over several calls (token shards on data-parallel GPUs, or micro-batches).  The
+pages' GPT-OSS 20B run trains on one node of several GPUs ("Scaling to long context lengths")
+without saying how the loss is normalised across them; the plainest reading is the loss of the
+whole batch.  ``count`` is then the whole batch's N (or S, each sequence within one shard),
+given to every shard in place of its own: shard r computes tau^2 / count * sum over its valid
+tokens of KL_t, and the shards' losses and gradients add up to the whole batch's.  ``count``
+must not be below the shard's own count.
+
 Everything is float64.  H and W arrive as bfloat16 on the GPU path; ``to_f64`` widens
 them exactly.  Rows are processed in blocks of ``chunk`` rows (a dense [chunk, V] block
 of logits at a time); the result does not depend on ``chunk`` beyond float64 rounding.
@@ -99,13 +107,23 @@ def teacher_probs(topk_logits, tau: float):
     return p, logp
 
 
-def token_weights(mask, T: int, norm: str = "tokens", seq_ids=None) -> np.ndarray:
+def _own_count(n: int, count) -> int:
+    """The mean's count: the batch's ``count`` when given (not below this shard's own n)."""
+    if count is None:
+        return n
+    if int(count) < n:
+        raise ValueError("count is below the shard's own count")
+    return int(count)
+
+
+def token_weights(mask, T: int, norm: str = "tokens", seq_ids=None, count=None) -> np.ndarray:
     """w_t, the weight of token t's KL in the loss (before tau^2): 1/N for valid tokens under
-    the token mean; 1/(S N_s) under the sequence mean; 0 for masked tokens."""
+    the token mean; 1/(S N_s) under the sequence mean; 0 for masked tokens.  ``count``
+    replaces N (or S) by the whole batch's when the batch is split over several calls."""
     msk = np.ones(T, dtype=bool) if mask is None else _np(mask).astype(bool)
     w = np.zeros(T)
     if norm == "tokens":
-        n = int(msk.sum())
+        n = _own_count(int(msk.sum()), count)
         if n:
             w[msk] = 1.0 / n
         return w
@@ -119,7 +137,7 @@ def token_weights(mask, T: int, norm: str = "tokens", seq_ids=None) -> np.ndarra
     counts = {}
     for t in np.flatnonzero(msk):
         counts[int(sid[t])] = counts.get(int(sid[t]), 0) + 1
-    S = len(counts)
+    S = _own_count(len(counts), count)
     for t in np.flatnonzero(msk):
         w[t] = 1.0 / (S * counts[int(sid[t])])
     return w
@@ -144,7 +162,7 @@ def _row_terms(s_blk: np.ndarray, idx_blk: np.ndarray, p_blk: np.ndarray, logp_b
 
 
 def forward(H, W, topk_idx, topk_logits, mask, tau: float, chunk: int = 64,
-            rows: Optional[Sequence[int]] = None, norm: str = "tokens", seq_ids=None):
+            rows: Optional[Sequence[int]] = None, norm: str = "tokens", seq_ids=None, count=None):
     """Loss, per-token lse and per-token KL.
 
     H [T, d] and W [V, d] are float64 arrays (see ``to_f64``); topk_idx [T, K] ints;
@@ -153,7 +171,8 @@ def forward(H, W, topk_idx, topk_logits, mask, tau: float, chunk: int = 64,
     With ``rows`` given, lse and KL are computed only for those rows (returned in that
     order) and the loss is computed only if every valid row is among them; otherwise
     ``loss`` is None.  This keeps exact checks affordable at full vocabulary size.
-    ``norm`` / ``seq_ids`` select the normaliser (module docstring).
+    ``norm`` / ``seq_ids`` select the normaliser and ``count`` the whole batch's count of a
+    split batch (module docstring).
     """
     H = np.asarray(H, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
@@ -178,9 +197,9 @@ def forward(H, W, topk_idx, topk_logits, mask, tau: float, chunk: int = 64,
             loss = 0.0
         elif norm == "tokens":
             valid_sel = msk[sel]
-            loss = float(tau) ** 2 / n_valid * float(np.sum(kl[valid_sel]))
+            loss = float(tau) ** 2 / _own_count(n_valid, count) * float(np.sum(kl[valid_sel]))
         else:
-            wts = token_weights(mask, T, norm, seq_ids)[sel]
+            wts = token_weights(mask, T, norm, seq_ids, count)[sel]
             loss = float(tau) ** 2 * float(np.sum(wts * kl))
     return {"loss": loss, "lse": lse, "kl": kl, "n_valid": n_valid, "rows": sel}
 
@@ -202,7 +221,7 @@ def _ds_block(s_blk, idx_blk, p_blk, valid_blk, tau, scale):
 
 
 def backward(H, W, topk_idx, topk_logits, mask, tau: float, grad: float = 1.0, chunk: int = 64,
-             norm: str = "tokens", seq_ids=None):
+             norm: str = "tokens", seq_ids=None, count=None):
     """dH [T, d] and dW [V, d] in float64, the exact gradient of ``forward``'s loss."""
     H = np.asarray(H, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
@@ -215,7 +234,7 @@ def backward(H, W, topk_idx, topk_logits, mask, tau: float, grad: float = 1.0, c
     dW = np.zeros_like(W)
     if n_valid == 0:
         return dH, dW
-    row_scale = float(grad) * float(tau) * token_weights(mask, T, norm, seq_ids)
+    row_scale = float(grad) * float(tau) * token_weights(mask, T, norm, seq_ids, count)
     p, _ = teacher_probs(topk_logits, tau)
     for b0 in range(0, T, chunk):
         r = slice(b0, min(T, b0 + chunk))
@@ -227,7 +246,7 @@ def backward(H, W, topk_idx, topk_logits, mask, tau: float, grad: float = 1.0, c
 
 
 def dH_rows(H, W, topk_idx, topk_logits, mask, tau: float, rows: Sequence[int], grad: float = 1.0,
-            chunk: int = 64):
+            chunk: int = 64, count=None):
     """Selected rows of dH.  Row t of dH needs only row t of the logits, so this is exact
     at any size."""
     H = np.asarray(H, dtype=np.float64)
@@ -240,7 +259,7 @@ def dH_rows(H, W, topk_idx, topk_logits, mask, tau: float, rows: Sequence[int], 
     out = np.zeros((len(rows), H.shape[1]))
     if n_valid == 0:
         return out
-    scale = float(grad) * float(tau) / n_valid
+    scale = float(grad) * float(tau) / _own_count(n_valid, count)
     p, _ = teacher_probs(_np(topk_logits)[rows], tau)
     for b0 in range(0, len(rows), chunk):
         r = rows[b0:b0 + chunk]
@@ -250,7 +269,7 @@ def dH_rows(H, W, topk_idx, topk_logits, mask, tau: float, rows: Sequence[int], 
 
 
 def dW_rows(H, W, topk_idx, topk_logits, mask, tau: float, vocab_rows: Sequence[int],
-            grad: float = 1.0, chunk: int = 64):
+            grad: float = 1.0, chunk: int = 64, count=None):
     """Selected rows of dW.  Row v of dW sums dS[t, v] H[t] over the valid tokens, so it
     needs lse of every valid token: affordable when few tokens are valid."""
     H = np.asarray(H, dtype=np.float64)
@@ -263,7 +282,7 @@ def dW_rows(H, W, topk_idx, topk_logits, mask, tau: float, vocab_rows: Sequence[
     out = np.zeros((len(vrows), H.shape[1]))
     if n_valid == 0:
         return out
-    scale = float(grad) * float(tau) / n_valid
+    scale = float(grad) * float(tau) / _own_count(n_valid, count)
     valid = np.flatnonzero(msk)
     p, _ = teacher_probs(_np(topk_logits)[valid], tau)
     for b0 in range(0, len(valid), chunk):

@@ -41,6 +41,7 @@ def test_every_declared_symbol_is_exported(L):
 def test_status_strings(L):
     assert L.fkl_status_string(0) == b"ok"
     assert b"teacher id" in L.fkl_status_string(6)
+    assert b"global count" in L.fkl_status_string(11)
     assert L.fkl_status_string(99) == b"unknown status"
 
 
@@ -192,6 +193,28 @@ def test_options_are_checked_on_host(L):
     o = FklOptions()
     o.accumulate = 4
     assert fwd(o) == INVALID
+    o = FklOptions()
+    o.global_count = 20                # an int64 scalar must be 8-byte aligned
+    assert fwd(o) == ALIGN
+
+
+def test_local_count_is_checked_on_host(L):
+    from lm_head_top_tcgen05_gb300._lib import FklOptions
+
+    def cnt(T, opts, count, ws, nbytes):
+        return L.fkl_local_count(None, T, ctypes.byref(opts) if opts is not None else None, count, ws, nbytes, None)
+
+    assert cnt(-1, None, 16, 256, 4096) == INVALID
+    assert cnt(100, None, None, 256, 4096) == INVALID       # no output
+    assert cnt(100, None, 12, 256, 4096) == ALIGN           # int64 output 8-byte aligned
+    assert cnt(100, None, 16, None, 4096) == WS
+    assert cnt(100, None, 16, 128, 4096) == ALIGN           # workspace 256-byte aligned
+    assert cnt(1000, None, 16, 256, 256 + 4 * 1000 - 1) == WS
+    o = FklOptions()
+    o.normalization, o.num_seqs = 1, 3
+    assert cnt(100, o, 16, 256, 4096) == INVALID            # seq_ids missing
+    # a valid call without a GPU fails on the device query, not before
+    assert cnt(100, None, 16, 256, 4096) in (UNSUP, CUDA)
 
 
 def test_divergence_options_are_checked_on_host(L):

@@ -109,6 +109,27 @@ def test_teacher_whose_top_logits_avoid_the_sampled_rows(fkl):
     check_cache(Ht, Wt, 100, idx, val)
 
 
+def test_teacher_topk_production_vocabulary(fkl):
+    # the gpt-oss-like teacher head at its full size (V = 201088, d = 2880, K = 100): the bound
+    # pass samples every 8th vocabulary row (25136 rows, 32 splits of several 256-wide tiles),
+    # so the multi-tile top-8 insertion of the bound pass and the candidate pass at full V are
+    # checked against the float64 oracle on every row
+    Ht, Wt = teacher(320, 2880, 201088, seed=11)
+    idx, val = fkl.teacher_topk(Ht.cuda(), Wt.cuda(), 100)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 0
+    check_cache(Ht, Wt, 100, idx, val)
+
+
+def test_forced_stride_8_matches_oracle(fkl):
+    # stride 8 forced on a smaller vocabulary (15 one-tile splits), against the oracle itself
+    Ht, Wt = teacher(200, 192, 30000, seed=10)
+    idx, val = fkl.teacher_topk(Ht.cuda(), Wt.cuda(), 100, max_bound_stride=8)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device="cuda") == 0
+    check_cache(Ht, Wt, 100, idx, val)
+
+
 @pytest.mark.parametrize("stride", [1, 2, 4, 8])
 def test_every_bound_stride_gives_the_same_cache(fkl, stride):
     Ht, Wt = teacher(200, 192, 30000, seed=10)

@@ -26,6 +26,8 @@ PIN_CALLS = [
     pins.test_sequence_mean_of_one_sequence_is_token_mean,
     pins.test_sequence_mean_weights_unequal_sequences,
     pins.test_sequence_mean_matches_autograd,
+    pins.test_shards_with_the_batch_count_add_up_to_the_batch,
+    pins.test_sequence_shards_with_the_batch_count_add_up_to_the_batch,
 ]
 
 
@@ -83,15 +85,28 @@ def ds_missing_tau(s, idx, p, valid, tau, scale):
 orig_token_weights = dk.token_weights
 
 
-def weights_ignore_mask(mask, T, norm="tokens", seq_ids=None):
-    return orig_token_weights(None, T, norm, seq_ids)
+def weights_ignore_mask(mask, T, norm="tokens", seq_ids=None, count=None):
+    return orig_token_weights(None, T, norm, seq_ids, count)
 
 
-def weights_sequence_by_total_count(mask, T, norm="tokens", seq_ids=None):
-    w = orig_token_weights(mask, T, norm, seq_ids)
+def weights_sequence_by_total_count(mask, T, norm="tokens", seq_ids=None, count=None):
+    w = orig_token_weights(mask, T, norm, seq_ids, count)
     if norm == "sequences":  # divides by the total valid count instead of each sequence's
-        w = orig_token_weights(mask, T, "tokens")
+        w = orig_token_weights(mask, T, "tokens", count=count)
     return w
+
+
+def own_count_ignores_batch_count(n, count):
+    return n  # a split batch normalised by each shard's own count
+
+
+def own_count_in_forward_only(n, count):
+    # the batch's count reaches the loss but not the gradient's scale: dH_rows / dW_rows / the
+    # backward's token weights keep the shard's own count
+    import inspect
+
+    caller = inspect.stack()[1].function
+    return n if caller in ("dH_rows", "dW_rows", "token_weights") else (n if count is None else int(count))
 
 
 def probs_no_teacher_tau(z, tau):
@@ -107,6 +122,7 @@ MUTATIONS = {
     "_row_terms": [row_terms_no_student_tau, row_terms_drop_entropy, row_terms_wrong_index, lse_log2],
     "_ds_block": [ds_sign_flip, ds_scatter_assign, ds_missing_tau],
     "token_weights": [weights_ignore_mask, weights_sequence_by_total_count],
+    "_own_count": [own_count_ignores_batch_count, own_count_in_forward_only],
     "teacher_probs": [probs_no_teacher_tau],
 }
 

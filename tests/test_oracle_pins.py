@@ -322,3 +322,55 @@ def test_sequence_mean_matches_autograd():
     dH, dW = oracle.backward(H, W, idx, z, m, tau, norm="sequences", seq_ids=seq)
     np.testing.assert_allclose(dH, Ht.grad.numpy(), rtol=1e-11, atol=1e-15)
     np.testing.assert_allclose(dW, Wt.grad.numpy(), rtol=1e-11, atol=1e-15)
+
+
+def test_shards_with_the_batch_count_add_up_to_the_batch():
+    # A batch split into three uneven shards with unequal valid counts (as over data-parallel
+    # ranks or micro-batches); every shard divides by the whole batch's N.  The shards' losses
+    # add up to the batch's, their dH rows are the batch's rows, and their dW add up to its dW.
+    H, W, idx, z, m, tau = rand_case(T=11, d=8, V=30, K=5, seed=31, tau=1.3,
+                                     mask=[1, 0, 1, 1, 1, 0, 0, 1, 1, 1, 1])
+    whole = oracle.forward(H, W, idx, z, m, tau)["loss"]
+    dH, dW = oracle.backward(H, W, idx, z, m, tau, grad=0.7)
+    N = int(m.sum())
+    loss, dW_sum = 0.0, np.zeros_like(W)
+    for a, b in [(0, 2), (2, 7), (7, 11)]:
+        sh = (H[a:b], W, idx[a:b], z[a:b], m[a:b], tau)
+        loss += oracle.forward(*sh, count=N)["loss"]
+        h, w = oracle.backward(*sh, grad=0.7, count=N)
+        np.testing.assert_allclose(h, dH[a:b], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(oracle.dH_rows(*sh, rows=np.arange(b - a), grad=0.7, count=N), h,
+                                   rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(oracle.dW_rows(*sh, vocab_rows=np.arange(30), grad=0.7, count=N), w,
+                                   rtol=1e-12, atol=1e-15)
+        dW_sum += w
+    assert loss == pytest.approx(whole, rel=1e-13)
+    np.testing.assert_allclose(dW_sum, dW, rtol=1e-12, atol=1e-15)
+
+
+def test_sequence_shards_with_the_batch_count_add_up_to_the_batch():
+    # packed sequences, each inside one shard; every shard divides by the batch's S
+    seq = np.array([0, 0, 0, 1, 1, 2, 2, 2, 2, 3])
+    H, W, idx, z, m, tau = rand_case(T=10, d=6, V=24, K=4, seed=32, tau=0.9,
+                                     mask=[1, 1, 0, 1, 0, 1, 1, 1, 0, 1])
+    kw = dict(norm="sequences")
+    whole = oracle.forward(H, W, idx, z, m, tau, seq_ids=seq, **kw)["loss"]
+    dH, dW = oracle.backward(H, W, idx, z, m, tau, seq_ids=seq, **kw)
+    loss, dW_sum = 0.0, np.zeros_like(W)
+    for a, b in [(0, 3), (3, 9), (9, 10)]:
+        sh = (H[a:b], W, idx[a:b], z[a:b], m[a:b], tau)
+        loss += oracle.forward(*sh, seq_ids=seq[a:b], count=4, **kw)["loss"]
+        h, w = oracle.backward(*sh, seq_ids=seq[a:b], count=4, **kw)
+        np.testing.assert_allclose(h, dH[a:b], rtol=1e-12, atol=1e-15)
+        dW_sum += w
+    assert loss == pytest.approx(whole, rel=1e-13)
+    np.testing.assert_allclose(dW_sum, dW, rtol=1e-12, atol=1e-15)
+
+
+def test_batch_count_defaults_and_limits():
+    H, W, idx, z, m, tau = rand_case(T=6, seed=33, mask=[1, 1, 0, 1, 1, 1])
+    own = oracle.forward(H, W, idx, z, m, tau)["loss"]
+    assert oracle.forward(H, W, idx, z, m, tau, count=5)["loss"] == own
+    assert oracle.forward(H, W, idx, z, m, tau, count=10)["loss"] == pytest.approx(own / 2, rel=1e-14)
+    with pytest.raises(ValueError):
+        oracle.forward(H, W, idx, z, m, tau, count=4)  # below the shard's own 5 valid tokens
