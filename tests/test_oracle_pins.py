@@ -44,13 +44,24 @@ def rand_case(T=6, d=8, V=32, K=5, seed=0, tau=1.0, mask=None, distinct=True, w_
 def test_closed_form_cases(case):
     H, W = np.array(case["H"], float), np.array(case["W"], float)
     ids, z, mask, tau = np.array(case["ids"]), np.array(case["z"], float), np.array(case["mask"]), case["tau"]
-    norm, seq = case.get("norm", "tokens"), case.get("seq_ids")
-    f = oracle.forward(H, W, ids, z, mask, tau, norm=norm, seq_ids=seq)
+    norm, seq, count = case.get("norm", "tokens"), case.get("seq_ids"), case.get("count")
+    f = oracle.forward(H, W, ids, z, mask, tau, norm=norm, seq_ids=seq, count=count)
     assert f["loss"] == pytest.approx(case["loss"], rel=1e-13, abs=1e-14)
     np.testing.assert_allclose(f["lse"], case["lse"], rtol=1e-13)
-    dH, dW = oracle.backward(H, W, ids, z, mask, tau, norm=norm, seq_ids=seq)
+    dH, dW = oracle.backward(H, W, ids, z, mask, tau, norm=norm, seq_ids=seq, count=count)
     np.testing.assert_allclose(dH, case["dH"], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(dW, case["dW"], rtol=1e-12, atol=1e-14)
+
+
+def test_golden_file_is_its_derivations():
+    # the stored values are what the committed derivation script computes from the formulas
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("make_closed_form_cases",
+                                                  os.path.join(os.path.dirname(GOLDEN), "make_closed_form_cases.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    assert mod.differences() == []
 
 
 @pytest.mark.parametrize("tau", [1.0, 2.0, 0.7])
