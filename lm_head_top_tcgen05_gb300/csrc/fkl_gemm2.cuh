@@ -15,7 +15,13 @@
 //               back by arriving on the even CTA's `tempty` (8 arrivals: 4 warps x 2 CTAs).
 // All three roles walk the same sequence of work items (item_range): whole units, then, for
 // the fp32 products, the K pieces of the last wave's units (GemmShape::split_from), whose
-// partial tiles a fixup kernel adds up afterwards.
+// partial tiles a fixup kernel adds up afterwards.  Items are dealt round-robin to the pairs,
+// or, for long launches (GemmShape::sched), drawn one at a time from a global counter by
+// the even CTA's producer, which hands each to the pair's other roles through a small ring
+// in shared memory.  Pairs run at slightly different speeds (1-2 % from SM to SM); with a
+// fixed deal the difference accumulates over a long launch, the pairs that share a W tile
+// drift apart by tens of tiles and the L2 re-reads W from DRAM, while drawing items keeps
+// the pairs on neighbouring units and balances the last wave.
 // Every wait is bounded as in the one-SM kernel; teardown drains copies and MMAs, meets
 // the other CTA at a cluster barrier and frees TMEM of both CTAs together.
 #pragma once
@@ -33,8 +39,10 @@ __host__ __device__ constexpr int stages2_for(int bn) { return bn == 256 ? 7 : 8
 // 64-byte swizzle: 32-element atoms (a 192-wide tile: 96-wide halves, three atoms).
 __host__ __device__ constexpr bool b_sw64_for(int bn, bool b_mn) { return b_mn && (bn / 2) % 64 != 0; }
 __host__ __device__ constexpr size_t smem2_bytes_for(int bn) {
+  // the operand stages, 1024 bytes of alignment slack, 512 for the barriers and other words
   return static_cast<size_t>(stages2_for(bn)) * (kBM * kBK * 2 + (bn / 2) * kBK * 2) + 1024 + 512;
 }
+static_assert((2 * 8 + 5 + 2 * 4) * 8 + (2 + 4) * 4 <= 512, "barriers and words fit in their 512 bytes");
 
 // Shared-memory layout of the two-SM kernel for a B tile of BN rows (BN / 2 per CTA).
 template <int BN, bool B_MN>
@@ -56,9 +64,70 @@ struct PairCtx {
   bool even;
   int cluster, nclusters;
   uint32_t stage0, full0, empty0, tfull0, tempty0, drain;
+  uint32_t sfull0, sempty0, ring0;  // work-item ring (dynamic scheduling)
   uint32_t tmem_base;
   WaitCtl ctl;
 };
+
+// Work-item ring of a dynamically scheduled launch: slots in each CTA's shared memory, a
+// `sfull` barrier per slot in each CTA (one arrival: the even producer's) and a `sempty`
+// barrier per slot in the even CTA (one arrival per consumer: the even MMA thread, the odd
+// producer and the four epilogue warps of each CTA).
+constexpr int kSchedSlots = 4;
+constexpr uint32_t kSchedConsumers = 10;
+
+// The sequence of work items of one role: `it` is the current item (>= num_items: done).
+struct ItemSeq {
+  int it;
+  int slot;
+  uint32_t parity;
+  __device__ explicit ItemSeq(const PairCtx& c) : it(c.cluster), slot(0), parity(0u) {}
+  __device__ __forceinline__ void advance() {
+    if (++slot == kSchedSlots) {
+      slot = 0;
+      parity ^= 1u;
+    }
+  }
+};
+
+// The even CTA's producer moves to its next item: the next round-robin one, or one drawn from
+// the counter and published to both CTAs' rings.  False when a wait ran out.
+__device__ __forceinline__ bool item_publish(const GemmShape& g, const PairCtx& c, ItemSeq& q) {
+  if (g.sched == nullptr) {
+    q.it += c.nclusters;
+    return true;
+  }
+  const int v = c.nclusters + (atomicAdd(g.sched, 1) - g.sched_base);
+  if (!mbar_wait_acquire_cluster(c.sempty0 + 8 * q.slot, q.parity ^ 1u, c.ctl)) return false;
+  const uint32_t r = c.ring0 + 4 * static_cast<uint32_t>(q.slot);
+  const uint32_t f = c.sfull0 + 8 * static_cast<uint32_t>(q.slot);
+  st_shared_cluster_u32(map_to_rank(r, 0), static_cast<uint32_t>(v));
+  st_shared_cluster_u32(map_to_rank(r, 1), static_cast<uint32_t>(v));
+  mbar_arrive_release_cluster(map_to_rank(f, 0));
+  mbar_arrive_release_cluster(map_to_rank(f, 1));
+  q.advance();
+  q.it = v;
+  return true;
+}
+
+// Every other role moves to its next item.  For a published item the caller then releases
+// the slot with item_release (once per consuming thread or warp, after it has read the
+// item); `slot` receives the slot to release, -1 when there is none.  False when a wait ran out.
+__device__ __forceinline__ bool item_take(const GemmShape& g, const PairCtx& c, ItemSeq& q, int& slot) {
+  slot = -1;
+  if (g.sched == nullptr) {
+    q.it += c.nclusters;
+    return true;
+  }
+  if (!mbar_wait_acquire_cluster(c.sfull0 + 8 * q.slot, q.parity, c.ctl)) return false;
+  q.it = static_cast<int>(ld_shared_u32(c.ring0 + 4 * static_cast<uint32_t>(q.slot)));
+  slot = q.slot;
+  q.advance();
+  return true;
+}
+__device__ __forceinline__ void item_release(const PairCtx& c, int slot) {
+  if (slot >= 0) mbar_arrive_release_cluster(map_to_rank(c.sempty0 + 8 * static_cast<uint32_t>(slot), 0));
+}
 
 // TMA producer (lane 0 of warp 0, both CTAs): loads this CTA's A rows and half of B into the
 // ring; the even CTA's `full` barrier counts the bytes of both CTAs.
@@ -71,9 +140,9 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tmA, const CUte
   uint32_t phase = 0, issued = 0, issued_par = 0;
   bool ok = true;
   const int items = num_items(g);
-  for (int it = c.cluster; ok && it < items; it += c.nclusters) {
+  for (ItemSeq q(c); ok && q.it < items;) {
     int m_blk, nb, ne, split, kb0, kb1, slot;
-    item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
+    item_range(g, q.it, m_blk, nb, ne, split, kb0, kb1, slot);
     const int a_row = m_blk * kBM2 + static_cast<int>(c.rank) * kBM;
     for (int n = nb; ok && n < ne; ++n) {
       const int b_row = n * BN + static_cast<int>(c.rank) * L::BNH;
@@ -113,6 +182,14 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tmA, const CUte
         if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
       }
     }
+    if (!ok) break;
+    if (c.even) {
+      ok = item_publish(g, c, q);
+    } else {
+      int rel;
+      ok = item_take(g, c, q, rel);
+      item_release(c, rel);
+    }
   }
   // The even CTA drains the pair's copies (its `full` phases count both CTAs' bytes).
   // The odd CTA's copies are covered by those phases; on the abort path its last copy
@@ -132,9 +209,9 @@ __device__ __forceinline__ void pair_mma(const GemmShape& g, const PairCtx& c) {
   uint32_t phase = 0, acc_phase = 0;
   bool ok = true;
   const int items = num_items(g);
-  for (int it = c.cluster; ok && it < items; it += c.nclusters) {
+  for (ItemSeq q(c); ok && q.it < items;) {
     int m_blk, nb, ne, split, kb0, kb1, slot;
-    item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
+    item_range(g, q.it, m_blk, nb, ne, split, kb0, kb1, slot);
     for (int n = nb; ok && n < ne; ++n) {
       if (!mbar_wait_cluster(c.tempty0 + 8 * acc, acc_phase ^ 1u, c.ctl)) { ok = false; break; }
       tc_fence_after();
@@ -163,6 +240,10 @@ __device__ __forceinline__ void pair_mma(const GemmShape& g, const PairCtx& c) {
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (!ok) break;
+    int rel;
+    ok = item_take(g, c, q, rel);
+    item_release(c, rel);
   }
   tc_commit_pair(c.drain);
   mbar_wait_drain(c.drain, 0u, g.limit_ns);
@@ -181,9 +262,9 @@ __device__ __forceinline__ void pair_epilogue(const GemmShape& g, const typename
   uint32_t acc_phase = 0;
   bool ok = true;
   const int items = num_items(g);
-  for (int it = c.cluster; ok && it < items; it += c.nclusters) {
+  for (ItemSeq q(c); ok && q.it < items;) {
     int m_blk, nb, ne, split, kb0, kb1, slot;
-    item_range(g, it, m_blk, nb, ne, split, kb0, kb1, slot);
+    item_range(g, q.it, m_blk, nb, ne, split, kb0, kb1, slot);
     const int row0 = m_blk * kBM2 + static_cast<int>(c.rank) * kBM;
     if constexpr (std::is_same<Epi, EpiF32>::value || std::is_same<Epi, EpiF32Bf16>::value) {
       if (slot >= 0)
@@ -205,7 +286,12 @@ __device__ __forceinline__ void pair_epilogue(const GemmShape& g, const typename
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (ok) epi.end_unit(split, row);
+    if (!ok) break;
+    epi.end_unit(split, row);
+    int rel;
+    ok = __all_sync(0xffffffffu, item_take(g, c, q, rel));
+    __syncwarp();
+    if (lane == 0) item_release(c, rel);
   }
 }
 
@@ -222,7 +308,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::STAGES * L::STAGE_BYTES);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * L::STAGES + 5);  // [0] TMEM base, [1] abort
+  // [0] TMEM base, [1] abort, [2, 2 + kSchedSlots) work-item ring
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + 2 * L::STAGES + 5 + 2 * kSchedSlots);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -236,6 +323,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tfull0 = empty0 + 8 * L::STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
+  const uint32_t sfull0 = drain + 8;
+  const uint32_t sempty0 = sfull0 + 8 * kSchedSlots;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::STAGES; ++s) {
@@ -247,6 +336,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(tempty0 + 8 * b, 2 * 4);
     }
     mbar_init(drain, 1);
+    for (int k = 0; k < kSchedSlots; ++k) {
+      mbar_init(sfull0 + 8 * k, 1);
+      mbar_init(sempty0 + 8 * k, kSchedConsumers);
+    }
     misc[1] = 0u;
     fence_barrier_init();
   }
@@ -265,7 +358,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = misc[0];
   const WaitCtl ctl{reinterpret_cast<volatile uint32_t*>(&misc[1]), g.status, g.limit_ns};
 
-  const PairCtx c{rank, even, cluster, nclusters, stage0, full0, empty0, tfull0, tempty0, drain, tmem_base, ctl};
+  const PairCtx c{rank,   even,   cluster, nclusters,          stage0,   full0,    empty0, tfull0,
+                  tempty0, drain, sfull0,  sempty0, smem_addr(&misc[2]), tmem_base, ctl};
   if (warp == 0) {
     if (lane == 0) pair_producer<BN, A_MN, B_MN>(&tmA, &tmB, g, c);
   } else if (warp == 1) {

@@ -17,12 +17,14 @@ constexpr uint32_t kStatusTopkOverflowBit = 16u;
 constexpr uint32_t kStatusBadCountBit = 32u;
 
 // Workspace header (first 256 bytes): status word, valid tokens, sequences with a valid
-// token, and g * tau (the backward's dS scale is g * tau * w_t).
+// token, g * tau (the backward's dS scale is g * tau * w_t), and the counter from which the
+// dynamically scheduled GEMM launches of one call draw their work items.
 struct WsHeader {
   uint32_t status;
   int32_t n_valid;
   int32_t n_seqs;
   float gtau;
+  int32_t items_taken;  // work-item counter of the dynamically scheduled GEMM launches
 };
 
 constexpr int kVocabTile = 256;                   // tile width of the vocabulary axis
@@ -75,6 +77,8 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
 // Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.
 // group: row blocks per group of the unit order (1 = row-major).
 int plan_splits(int m_tiles, int n_tiles, int sms, int group = 1);
+// Vocabulary splits per row block for a dynamically scheduled launch (GemmShape::sched).
+int dynamic_splits(int n_tiles);
 // Sets p->Vc and p->nslabs for a device with `pairs` CTA pairs (see fkl_api.cu).
 void choose_slab_width(Plan* p, int pairs);
 
@@ -136,6 +140,12 @@ struct GemmShape {
   int split_from;
   int ksplit;
   float* kpart;  // [(unit - split_from) * ksplit + piece][256][bn]
+  // Dynamic scheduling (two-SM kernel; NULL: items dealt round-robin).  Each pair starts on
+  // item `cluster`, then draws the next from *sched: item = pairs + (*sched)++ - sched_base.
+  // A launch advances *sched by exactly its number of items, so consecutive launches of one
+  // call give each the running total as sched_base (the counter is zeroed with the header).
+  int* sched;
+  int sched_base;
   uint32_t* status;
   uint64_t limit_ns;
 };

@@ -370,6 +370,8 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  int* items_taken = reinterpret_cast<int*>(ws + 16);  // work-item counter of both passes
+  int sched_base = 0;
   if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "cudaMemsetAsync failed");
   if (T == 0) return FKL_OK;
   float* topr = reinterpret_cast<float*>(ws + pl.off_topr);
@@ -383,13 +385,14 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
   if (!encode_map_bf16(&mH, Ht, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, Wt, d, V, d * 2, 64, kVocabTile / 2) ||
       !encode_map_bf16(&mWs, Wt, d, pl.Vs, d * 2 * pl.stride, 64, kVocabTile / 2))
     return topk_fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  const int pairs = sms / 2;
-  const int m_tiles = static_cast<int>((T + 255) / 256), n_tiles = static_cast<int>((V + kVocabTile - 1) / kVocabTile);
+  const int n_tiles = static_cast<int>((V + kVocabTile - 1) / kVocabTile);
   if (pl.bound_pass) {
     const int s_tiles = static_cast<int>((pl.Vs + kVocabTile - 1) / kVocabTile);
     const int ns = s_tiles < kMaxBoundSplits ? s_tiles : kMaxBoundSplits;
     GemmShape g = make_shape(T, pl.Vs, d, kVocabTile, ns, status, 256);
     g.group_m = group_rows(g.m_tiles);
+    g.sched = items_taken;  // units drawn from the counter (zeroed with the header)
+    sched_base = num_items(g);
     TopRParams tp;
     tp.topr = topr;
     tp.T = static_cast<int>(T);
@@ -404,8 +407,10 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
     fill_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(theta, T, -INFINITY);
   }
   if (cudaGetLastError() != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "bound kernel launch failed");
-  GemmShape g2 = make_shape(T, V, d, kVocabTile, plan_splits(m_tiles, n_tiles, pairs, group_rows(m_tiles)), status, 256);
+  GemmShape g2 = make_shape(T, V, d, kVocabTile, dynamic_splits(n_tiles), status, 256);
   g2.group_m = group_rows(g2.m_tiles);
+  g2.sched = items_taken;  // after the bound pass's items, if it ran
+  g2.sched_base = sched_base;
   CandParams cp;
   cp.theta = theta;
   cp.cnt = cnt;
