@@ -113,6 +113,14 @@ def test_upstream_gradient_scales(fkl):
     assert_parity(run_gpu(fkl, x, grad=-0.37), run_oracle(x, grad=-0.37))
 
 
+def test_zero_upstream_gradient(fkl):
+    # g = 0: every row's factor g tau w_t is 0, so dS and both gradients are exactly zero
+    x = workloads.make_random(300, 128, 3000, 12, seed=9, mask_frac=0.1)
+    out = run_gpu(fkl, x, grad=0.0)
+    assert out["status"] == 0
+    assert not np.any(out["dH"]) and not np.any(out["dW"])
+
+
 def test_deterministic(fkl):
     x = workloads.make_random(300, 200, 5000, 16, tau=2.0, chunk=128, seed=2, mask_frac=0.1)
     a, b = run_gpu(fkl, x), run_gpu(fkl, x)
