@@ -224,13 +224,14 @@ def blas_threads():
     return None
 
 # DRAM bytes (read + write) per launch of each GEMM kind on the 32K workload (T=32768,
-# d=2880, V=201088), valid only for the CUDA sources they were taken on: the backward's from
-# one ncu capture of a launch of its slab shape (slab width 11264), scaled by work to the mean
-# launch; the forward's from a one-pass capture of the full-size launch itself.
-TRAFFIC_SOURCES_SHA = "4f89e5f1eb1250cd"
-TRAFFIC_BYTES = {0: 44.654e9, 1: 1.898e9, 2: 3.095e9, 3: 3.060e9}
-TRAFFIC_FLOPS = {0: 2.0 * 32768 * 201088 * 2880, 1: 2.0 * 32768 * 11264 * 2880,
-                 2: 2.0 * 32768 * 11264 * 2880, 3: 2.0 * 32768 * 11264 * 2880}
+# d=2880, V=201088), valid only for the CUDA sources they were taken on: one ncu capture of
+# every launch of five full-size steps (dram__bytes_read.sum + dram__bytes_write.sum, one
+# pass), averaged over the launches of each kind; TRAFFIC_FLOPS is that kind's mean work per
+# launch, so the bench's own launches take the figures as they are.
+TRAFFIC_SOURCES_SHA = "2674472ca9e3a71e"
+TRAFFIC_BYTES = {0: 18.820e9, 1: 1.834e9, 2: 2.926e9, 3: 3.602e9}
+TRAFFIC_FLOPS = {0: 2.0 * 32768 * 201088 * 2880, 1: 2.0 * 32768 * 201088 * 2880 / 18,
+                 2: 2.0 * 32768 * 201088 * 2880 / 18, 3: 2.0 * 32768 * 201088 * 2880 / 18}
 
 
 # The sources that define the loss's tensor-core GEMMs and how they are launched (tiles,
