@@ -228,8 +228,8 @@ def blas_threads():
 # every launch of five full-size steps (dram__bytes_read.sum + dram__bytes_write.sum, one
 # pass), averaged over the launches of each kind; TRAFFIC_FLOPS is that kind's mean work per
 # launch, so the bench's own launches take the figures as they are.
-TRAFFIC_SOURCES_SHA = "2674472ca9e3a71e"
-TRAFFIC_BYTES = {0: 18.820e9, 1: 1.834e9, 2: 2.926e9, 3: 3.602e9}
+TRAFFIC_SOURCES_SHA = "992ac464f192311e"
+TRAFFIC_BYTES = {0: 15.225e9, 1: 1.848e9, 2: 3.618e9, 3: 4.076e9}
 TRAFFIC_FLOPS = {0: 2.0 * 32768 * 201088 * 2880, 1: 2.0 * 32768 * 201088 * 2880 / 18,
                  2: 2.0 * 32768 * 201088 * 2880 / 18, 3: 2.0 * 32768 * 201088 * 2880 / 18}
 

@@ -38,7 +38,8 @@ static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; 
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p, bool bf16_grads) {
+bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p, bool bf16_grads,
+               int max_splits) {
   if (T < 0 || T >= (int64_t{1} << 31)) return false;
   if (d < 8 || d % 8 != 0 || d >= (int64_t{1} << 20)) return false;
   if (V < 1 || V > (int64_t{1} << 30)) return false;
@@ -96,7 +97,7 @@ bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* 
   p->off_crow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
   p->off_wrow = off;  off = align_up(off + static_cast<size_t>(T) * 4, 256);
   p->off_scnt = off;  off = align_up(off + static_cast<size_t>(T > 0 ? T : 1) * 4, 256);
-  p->off_part = off;  off = align_up(off + static_cast<size_t>(T) * 3 * kMaxSplit * 4, 256);
+  p->off_part = off;  off = align_up(off + static_cast<size_t>(T) * 3 * max_splits * 4, 256);
   const size_t nbb = static_cast<size_t>(p->nb > 0 ? p->nb : 1);
   p->off_bsum = off;  off = align_up(off + nbb * 8, 256);
   p->off_bcnt = off;  off = align_up(off + nbb * 4, 256);
@@ -136,14 +137,24 @@ static int64_t split_cost(int m_tiles, int n_tiles, int sms, int s) {
   return cdiv(static_cast<int64_t>(m_tiles) * s, sms) * cdiv(n_tiles, s);
 }
 
-int dynamic_splits(int n_tiles) {
+int dynamic_splits(int m_tiles, int n_tiles, int pairs) {
   // Pairs that draw their units from a counter balance the launch themselves, so the only
-  // quantum left is one unit at the very end: the shortest units (the most splits the
-  // partials hold) give the least idle time.  Measured on the 32K forward (same-process A/B
-  // with items drawn): 32 splits (units of about 25 tiles) took 3.3 % less time than 10
-  // (units of 79 tiles), whose last unit left most pairs idle for about 1 ms; the unit start
-  // (a binary search in the row's sorted teacher ids) and end (three stores) are negligible.
-  return n_tiles < kMaxSplit ? n_tiles : kMaxSplit;
+  // quantum left is one unit at the very end, and the pairs that share a W tile read it
+  // within about half a unit's duration of each other: the shortest units (the most splits
+  // the partials hold) give the least idle time and the fewest W re-reads.  Measured on the
+  // 32K forward (same-process A/Bs with units drawn): 32 splits (units of about 25 tiles) took
+  // 3.3 % less time than 10 (units of 79 tiles, whose last unit left most pairs idle for about
+  // 1 ms); 64 splits (12 tiles) another 1.8 % (DRAM reads 19-20 -> 10.5-11.2 GB per launch).
+  // A unit's start (a binary search in the row's sorted teacher ids, the hand-off of its
+  // index) and end (three stores) are not free, though: units stay at least kMinUnitTiles
+  // long (on a 22528-word vocabulary, 64 splits of 1-2 tiles kept the tensor pipe 87 % busy
+  // against 90 % for 32), unless that leaves fewer than two units per pair.
+  constexpr int kMinUnitTiles = 4;
+  int s = (n_tiles + kMinUnitTiles - 1) / kMinUnitTiles;
+  const int fill = static_cast<int>((2LL * pairs + m_tiles - 1) / m_tiles);
+  if (s < fill) s = fill;
+  if (s > n_tiles) s = n_tiles;
+  return s < kMaxSplit ? s : kMaxSplit;
 }
 
 int plan_splits(int m_tiles, int n_tiles, int sms, int group) {
@@ -157,7 +168,7 @@ int plan_splits(int m_tiles, int n_tiles, int sms, int group) {
   int lo = (sms + 31) / 32;
   if (lo > n_tiles) lo = n_tiles;
   if (lo < 1) lo = 1;
-  int hi = n_tiles < kMaxSplit ? n_tiles : kMaxSplit;
+  int hi = n_tiles < kMaxDealtSplit ? n_tiles : kMaxDealtSplit;
   auto cost = [&](int s) { return split_cost(m_tiles, n_tiles, sms, s); };
   int best = lo;
   for (int s = lo; s <= hi; ++s)
@@ -554,8 +565,8 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
       return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for H or W");
     // Units drawn from a counter (the header was zeroed above: this is the call's first
     // dynamically scheduled launch, sched_base 0), in groups of row blocks, split-major.
-    const int n_tiles = (int)cdiv(V, kVocabTile);
-    GemmShape g = make_shape(T, V, d, kVocabTile, dynamic_splits(n_tiles), &hdr->status, 256);
+    const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(V, kVocabTile);
+    GemmShape g = make_shape(T, V, d, kVocabTile, dynamic_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
     g.group_m = group_rows(g.m_tiles);
     g.sched = &hdr->items_taken;
     const int nsplit = g.nsplit;

@@ -28,7 +28,8 @@ struct WsHeader {
 };
 
 constexpr int kVocabTile = 256;                   // tile width of the vocabulary axis
-constexpr int kMaxSplit = 32;                     // most vocabulary splits per row block
+constexpr int kMaxSplit = 64;                     // most vocabulary splits per row block (partials)
+constexpr int kMaxDealtSplit = 32;                // most splits of a launch whose units are dealt round-robin
 constexpr int64_t kMaxTokenBlocks = 64;           // most token blocks of the backward
 constexpr uint64_t kWaitLimitNs = 5000000000ull;  // per pipeline wait
 constexpr float kLog2e = 1.4426950408889634f;      // log2(e): natural-log scale to base 2
@@ -72,13 +73,16 @@ void trace_launch_begin(cudaStream_t st);
 void trace_launch_end(cudaStream_t st, int kind, double flops);
 
 // bf16_grads: also lay out the fp32 sums that bf16 gradient outputs need (fkl_backward_bf16).
-bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p, bool bf16_grads = false);
+// max_splits: vocabulary splits the forward's partials hold per row.
+bool make_plan(int64_t T, int64_t d, int64_t V, int64_t K, int64_t chunk, Plan* p, bool bf16_grads = false,
+               int max_splits = kMaxSplit);
 
 // Vocabulary splits per 128-row block for a persistent launch over m_tiles x n_tiles.
 // group: row blocks per group of the unit order (1 = row-major).
 int plan_splits(int m_tiles, int n_tiles, int sms, int group = 1);
-// Vocabulary splits per row block for a dynamically scheduled launch (GemmShape::sched).
-int dynamic_splits(int n_tiles);
+// Vocabulary splits per row block for a dynamically scheduled launch (GemmShape::sched) over
+// m_tiles x n_tiles on `pairs` CTA pairs.
+int dynamic_splits(int m_tiles, int n_tiles, int pairs);
 // Sets p->Vc and p->nslabs for a device with `pairs` CTA pairs (see fkl_api.cu).
 void choose_slab_width(Plan* p, int pairs);
 

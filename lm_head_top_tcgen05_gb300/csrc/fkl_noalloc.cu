@@ -73,7 +73,8 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
                                           float* lse, void* stream) {
   set_last_error_message("");
   Plan pl;
-  if (!make_plan(T, d, V, K, 1, &pl)) return noalloc_fail(FKL_ERR_INVALID_ARG, "unsupported shape");
+  // the one-SM forward deals its units round-robin: at most kMaxDealtSplit partials per row
+  if (!make_plan(T, d, V, K, 1, &pl, false, kMaxDealtSplit)) return noalloc_fail(FKL_ERR_INVALID_ARG, "unsupported shape");
   if (!(tau > 0.f) || tau == INFINITY) return noalloc_fail(FKL_ERR_INVALID_ARG, "tau must be finite and > 0");
   if (W == nullptr || loss == nullptr || (T > 0 && (H == nullptr || topk_idx == nullptr || topk_logits == nullptr || lse == nullptr)))
     return noalloc_fail(FKL_ERR_INVALID_ARG, "a required pointer is NULL");

@@ -385,7 +385,7 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
   if (!encode_map_bf16(&mH, Ht, d, T, d * 2, 64, 128) || !encode_map_bf16(&mW, Wt, d, V, d * 2, 64, kVocabTile / 2) ||
       !encode_map_bf16(&mWs, Wt, d, pl.Vs, d * 2 * pl.stride, 64, kVocabTile / 2))
     return topk_fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  const int n_tiles = static_cast<int>((V + kVocabTile - 1) / kVocabTile);
+  const int m_tiles = static_cast<int>((T + 255) / 256), n_tiles = static_cast<int>((V + kVocabTile - 1) / kVocabTile);
   if (pl.bound_pass) {
     const int s_tiles = static_cast<int>((pl.Vs + kVocabTile - 1) / kVocabTile);
     const int ns = s_tiles < kMaxBoundSplits ? s_tiles : kMaxBoundSplits;
@@ -407,7 +407,7 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
     fill_kernel<<<static_cast<unsigned>((T + 255) / 256), 256, 0, st>>>(theta, T, -INFINITY);
   }
   if (cudaGetLastError() != cudaSuccess) return topk_fail(FKL_ERR_CUDA, "bound kernel launch failed");
-  GemmShape g2 = make_shape(T, V, d, kVocabTile, dynamic_splits(n_tiles), status, 256);
+  GemmShape g2 = make_shape(T, V, d, kVocabTile, dynamic_splits(m_tiles, n_tiles, sms / 2), status, 256);
   g2.group_m = group_rows(g2.m_tiles);
   g2.sched = items_taken;  // after the bound pass's items, if it ran
   g2.sched_base = sched_base;

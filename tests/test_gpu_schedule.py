@@ -30,6 +30,17 @@ def counter(ws):
     return int(ws.buf[16:20].view(torch.int32).item())
 
 
+def drawn_splits(m_tiles, n_tiles, pairs):
+    """Splits of a drawn launch: units of at least 4 tiles unless that leaves fewer than two
+    units per pair, at most one per tile and at most 64."""
+    s = max(-(-n_tiles // 4), -(-2 * pairs // m_tiles))
+    return min(s, n_tiles, 64)
+
+
+def pairs():
+    return torch.cuda.get_device_properties(0).multi_processor_count // 2
+
+
 @pytest.mark.parametrize("T,V", [(1000, 20000), (4096, 50000), (10, 300), (256, 256)])
 def test_forward_takes_one_value_per_unit(fkl, T, V):
     x = workloads.make_random(T, 128, V, 8, seed=T + V)
@@ -39,12 +50,12 @@ def test_forward_takes_one_value_per_unit(fkl, T, V):
     torch.cuda.synchronize()
     assert fkl.read_status(ws) == 0
     m_tiles, n_tiles = (T + 255) // 256, (V + 255) // 256
-    assert counter(ws) == m_tiles * min(32, n_tiles)  # units: row blocks x vocabulary splits
+    assert counter(ws) == m_tiles * drawn_splits(m_tiles, n_tiles, pairs())  # row blocks x splits
 
 
 def test_teacher_passes_share_the_counter(fkl):
     # the bound pass over every 8th vocabulary row (3750 rows: 15 tiles, one split each),
-    # then the candidate pass over all 30000 (118 tiles in 32 splits): the counter ends at the
+    # then the candidate pass over all 30000 (118 tiles): the counter ends at the
     # sum of both launches' units
     T, V = 600, 30000
     g = torch.Generator().manual_seed(12)
@@ -57,7 +68,7 @@ def test_teacher_passes_share_the_counter(fkl):
     m_tiles = (T + 255) // 256
     vs = (V + 7) // 8                      # rows the bound pass samples at stride 8
     bound_units = m_tiles * min(32, (vs + 255) // 256)
-    cand_units = m_tiles * min(32, (V + 255) // 256)
+    cand_units = m_tiles * drawn_splits(m_tiles, (V + 255) // 256, pairs())
     assert counter(ws) == bound_units + cand_units
 
 
