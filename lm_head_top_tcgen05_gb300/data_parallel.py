@@ -82,8 +82,10 @@ class ShardedStep:
     def global_count(self, mask: Optional[torch.Tensor], T: int, device, seq_ids=None, num_seqs=None,
                      workspace=None) -> torch.Tensor:
         """The batch's count: this rank's count summed over the group (steps 1 and 2)."""
+        from . import all_reduce_count
+
         n = self.ops.local_count(mask, T, device, seq_ids, num_seqs, workspace)
-        return _all_reduce_sum(n, self.group)
+        return all_reduce_count(n, self.group)
 
     def __call__(self, H, W, topk_idx, topk_logits, mask=None, tau: float = 1.0, chunk: int = 2048,
                  workspace=None, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
