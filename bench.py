@@ -129,11 +129,15 @@ def cpu_oracle_rate(x, rows: int, divergence: str = "kl", div_param=None):
     return rows / dt, dt, cores, np.__version__
 
 
-def loss_config(w, T, d, V, K, args) -> dict:
+def loss_config(w, T, d, V, K, args, sharded: bool = False) -> dict:
     """The `config` of the loss's JSON line, the same for both arms."""
+    world = args.gpus
     return {"workload": w.name, "T": T, "d": d, "V": V, "K": K, "tau": w.tau, "chunk": w.chunk,
             "divergence": args.divergence, "grad_dtype": args.grad_dtype,
-            "l2": "inputs larger than L2 (W is 1.16 GB); no flush"}
+            "l2": "inputs larger than L2 (W is 1.16 GB); no flush",
+            "parallelism": "single GPU" if not sharded else
+            f"token-sharded dp{world}: NCCL all-reduce of the valid-token count before the loss, of dW and "
+            f"the loss after it; T={T} tokens per rank"}
 
 
 def run_reference(args, rank):
@@ -156,7 +160,7 @@ def run_reference(args, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * w.T / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": loss_config(w, w.T, w.d, w.V, w.K, args),
+        "config": loss_config(w, w.T, w.d, w.V, w.K, args, sharded=args.gpus > 1 or args.sharded),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "blas_threads": blas_threads(),
                          "kind": "oracle",
                          "sample": f"first {args.cpu_rows} tokens of the batch per step, full "
@@ -389,6 +393,9 @@ def main():
                     help="dtype of the dH / dW outputs (default fp32; bf16: fp32 sums rounded once)")
     ap.add_argument("--bound-stride", type=int, default=0,
                     help="teacher_topk: largest vocabulary sampling stride of the bound pass (0: default)")
+    ap.add_argument("--sharded", action="store_true",
+                    help="run the token-sharded data-parallel step (ShardedStep) even on one GPU, where "
+                         "its all-reduces are no-ops (under torchrun with N > 1 it always runs)")
     ap.add_argument("--mode", default="loss", choices=["loss", "teacher_topk"],
                     help="loss: the fused KL fwd+bwd step (the headline); teacher_topk: the offline "
                          "teacher cache producer on the same shapes")
@@ -449,7 +456,7 @@ def main():
     # N > 1: token-sharded data parallelism (count all-reduce before the loss, dW and loss
     # all-reduce after it); one GPU: the plain step
     dp = None
-    if world > 1:
+    if world > 1 or args.sharded:
         from lm_head_top_tcgen05_gb300.data_parallel import ShardedStep
 
         dp = ShardedStep()
@@ -591,10 +598,7 @@ def main():
         "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(loss_config(w, T, d, V, K, args),
-                       parallelism="single GPU" if world == 1 else
-                       f"token-sharded dp{world}: NCCL all-reduce of the valid-token count before the "
-                       f"loss, of dW and the loss after it; T={T} tokens per rank"),
+        "config": loss_config(w, T, d, V, K, args, sharded=dp is not None),
         "ms_per_step_median": step_ms_median,
         "tflops": tflops,
         "tensor_frac_step": tflops / sustained,
