@@ -509,19 +509,22 @@ cudaError_t launch_div_coef(DivSpec dv, int2* pairs, const int* slot, const floa
 constexpr int kWeightThreads = 256;
 
 // Valid tokens per sequence (token mean: everything in sequence 0).  Integer atomics: the
-// counts do not depend on the order of the additions.
+// counts do not depend on the order of the additions.  The lanes of a warp that count into
+// the same sequence add together (one atomic per sequence per warp instead of one per token,
+// which for the token mean would serialise every token on one address).
 __global__ void __launch_bounds__(kWeightThreads)
     seq_count_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ seq, int64_t T,
                      int num_seqs, int* __restrict__ cnt, uint32_t* __restrict__ status) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kWeightThreads + threadIdx.x;
-  if (t >= T) return;
-  if (mask != nullptr && mask[t] == 0) return;
-  const int sid = seq ? seq[t] : 0;
-  if (sid < 0 || sid >= num_seqs) {
-    atomicOr(status, kStatusBadSeqBit);
-    return;
+  int key = -1;  // the sequence this lane counts into, -1 for none
+  if (t < T && (mask == nullptr || mask[t] != 0)) {
+    const int sid = seq ? seq[t] : 0;
+    if (sid < 0 || sid >= num_seqs) atomicOr(status, kStatusBadSeqBit);
+    else key = sid;
   }
-  atomicAdd(&cnt[sid], 1);
+  const unsigned same = __match_any_sync(0xffffffffu, key);
+  const int lane = threadIdx.x & 31;
+  if (key >= 0 && lane == __ffs(same) - 1) atomicAdd(&cnt[key], __popc(same));
 }
 
 // N = sum of the counts, S = number of sequences with a valid token (fixed-order tree sums).
