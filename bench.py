@@ -106,6 +106,36 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class EnergyMeter:
+    """The GPU's total energy counter (NVML, millijoules) around the timed region, read through
+    ctypes; None when NVML or the counter is not available."""
+
+    def __init__(self, index: int):
+        self.fn = None
+        try:
+            import ctypes
+
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(handle)) != 0:
+                return
+            value = ctypes.c_ulonglong()
+
+            def read():
+                ok = nv.nvmlDeviceGetTotalEnergyConsumption(handle, ctypes.byref(value)) == 0
+                return value.value if ok else None
+
+            if read() is not None:
+                self.fn = read
+        except OSError:
+            self.fn = None
+
+    def read(self):
+        return self.fn() if self.fn is not None else None
+
+
 def cpu_oracle_rate(x, rows: int, divergence: str = "kl", div_param=None):
     """Tokens/s of the float64 oracle (forward + backward) on the first `rows` tokens."""
     import numpy as np
@@ -489,8 +519,10 @@ def main():
     # fixup each for dW and dH; one more entry so that a full trace is detected
     trace_cap = args.steps * (1 + 5 * nslabs) + 1
     fkl.check(fkl.lib().fkl_trace_start(trace_cap), "fkl_trace_start")
+    energy = EnergyMeter(local_rank)
     with ClockSampler(local_rank) as clocks:
         barrier()
+        mj0 = energy.read()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
@@ -500,6 +532,7 @@ def main():
             ev[i][2].record(stream)
         end.record(stream)
         barrier()
+        mj1 = energy.read()
     fkl.lib().fkl_trace_stop()
     elapsed = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
     kernels = trace_summary(fkl.lib(), trace_cap)
@@ -618,6 +651,8 @@ def main():
         "kernels": {KIND_NAMES[k]: {kk: round(vv, 4) if isinstance(vv, float) else vv for kk, vv in v.items()}
                     for k, v in kernels.items()},
         "clocks": clk,
+        # this GPU's energy over the timed steps (NVML counter; rank 0's GPU under torchrun)
+        "energy_j_per_step": (mj1 - mj0) / 1e3 / args.steps if mj0 is not None and mj1 is not None else None,
         "gpu_launches": int(round(launches_per_step * args.steps)),
     }
     if e2e is not None:
