@@ -97,7 +97,11 @@ __device__ __forceinline__ bool item_publish(const GemmShape& g, const PairCtx& 
     q.it += c.nclusters;
     return true;
   }
-  const int v = c.nclusters + (atomicAdd(g.sched, 1) - g.sched_base);
+  int v = c.nclusters + (atomicAdd(g.sched, 1) - g.sched_base);
+  // A counter behind this launch's base means an earlier launch of the call stopped early
+  // (its wait ran out and the status word already holds the error): take no further item
+  // rather than one of the first, fixed ones.
+  if (v < c.nclusters) v = num_items(g);
   if (!mbar_wait_acquire_cluster(c.sempty0 + 8 * q.slot, q.parity ^ 1u, c.ctl)) return false;
   const uint32_t r = c.ring0 + 4 * static_cast<uint32_t>(q.slot);
   const uint32_t f = c.sfull0 + 8 * static_cast<uint32_t>(q.slot);
