@@ -138,3 +138,51 @@ def test_sharded_step_single_process(fkl):
     torch.cuda.synchronize()
     assert loss.item() == ref_loss.item()
     assert torch.equal(dH, ref_dH) and torch.equal(dW, ref_dW)
+
+
+def test_jsd_shards_equal_the_whole_batch(fkl):
+    # the batch's count reaches the other divergences' token weights too (forward rows and
+    # the backward's per-row factor): JSD over three shards against the whole batch
+    x = workloads.make_random(700, 160, 4000, 12, tau=1.3, chunk=64, seed=66, mask_frac=0.2)
+    x.mask[:80] = 0
+    dev = "cuda"
+    H, W = x.H.to(dev), x.W.to(dev)
+    idx, z, m = x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev)
+    cuts = [(0, 150), (150, 480), (480, 700)]
+    N = torch.stack([fkl.local_count(m[a:b], b - a) for a, b in cuts]).sum()
+    dH = torch.zeros(700, 160, device=dev)
+    dW = torch.zeros(4000, 160, device=dev)
+    loss = 0.0
+    for a, b in cuts:
+        s_ids = torch.empty(b - a, 12, device=dev)
+        kw = dict(divergence="jsd", div_param=0.4, student_topk_logits=s_ids, global_count=N)
+        l_r, lse_r = fkl.forward(H[a:b], W, idx[a:b], z[a:b], m[a:b], x.tau, x.chunk, **kw)
+        fkl.backward(H[a:b], W, idx[a:b], z[a:b], m[a:b], lse_r, None, x.tau, x.chunk, out=(dH[a:b], dW),
+                     accumulate=True, **kw)
+        loss += l_r.item()
+    torch.cuda.synchronize()
+    assert fkl.read_status(device=dev) == 0
+    H64, W64 = oracle.to_f64(x.H), oracle.to_f64(x.W)
+    ref = oracle.divergences.forward(H64, W64, x.topk_idx, x.topk_logits, x.mask, x.tau, "jsd", 0.4)
+    rdH, rdW = oracle.divergences.backward(H64, W64, x.topk_idx, x.topk_logits, x.mask, x.tau, "jsd", 0.4)
+    assert abs(loss - ref["loss"]) <= LOSS_RTOL * abs(ref["loss"])
+    close(dH.cpu().numpy(), rdH, "dH")
+    close(dW.cpu().numpy(), rdW, "dW")
+
+
+def test_bf16_gradients_of_a_shard_with_the_batch_count(fkl):
+    # a shard's bf16 gradients with the batch's count equal its fp32 ones rounded, bit for bit
+    x = workloads.make_random(600, 128, 3000, 16, seed=67, mask_frac=0.15)
+    dev = "cuda"
+    H, W = x.H.to(dev), x.W.to(dev)
+    idx, z, m = x.topk_idx.to(dev), x.topk_logits.to(dev), x.mask.to(dev)
+    N = fkl.local_count(m, 600) * 3  # as if two more shards of the same count followed
+    loss, lse = fkl.forward(H, W, idx, z, m, 1.0, 64, global_count=N)
+    dH, dW = fkl.backward(H, W, idx, z, m, lse, None, 1.0, 64, global_count=N)
+    dH16, dW16 = fkl.backward(H, W, idx, z, m, lse, None, 1.0, 64, global_count=N, grad_dtype=torch.bfloat16)
+    ref_loss, ref_lse = fkl.forward(H, W, idx, z, m, 1.0, 64)
+    torch.cuda.synchronize()
+    assert fkl.read_status(device=dev) == 0
+    assert torch.equal(dH16.view(torch.int16), dH.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(dW16.view(torch.int16), dW.to(torch.bfloat16).view(torch.int16))
+    assert loss.item() == pytest.approx(ref_loss.item() / 3, rel=1e-6)  # a third of the shard's own mean
