@@ -158,7 +158,8 @@ int dynamic_splits(int m_tiles, int n_tiles, int pairs) {
 }
 
 int plan_splits(int m_tiles, int n_tiles, int sms, int group) {
-  // Pick the number of vocabulary splits per row block that minimises the critical path
+  // For launches whose units are dealt round-robin (the dS recompute, the one-SM forward):
+  // pick the number of vocabulary splits per row block that minimises the critical path
   // (waves of units x tiles per unit).  At least sms/32 splits keep the row blocks in
   // flight at once (each re-read from L2 for every tile of its unit) to a few dozen.  With
   // units in groups of `group` row blocks, a count within 1 % of the best that makes a
