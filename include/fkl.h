@@ -27,9 +27,11 @@
  * by `chunk` (below).
  *
  * Conventions for every entry point:
- *   - Device pointers are CUDA device memory of the current device; all buffers are
- *     row-major and contiguous.  The caller owns every buffer, including the workspace;
- *     the library allocates no device memory.
+ *   - Device pointers are CUDA device memory of the current device (or managed memory);
+ *     all buffers are row-major and contiguous.  A pointer that is not (host memory given
+ *     by mistake) is refused on the host with FKL_ERR_INVALID_ARG before anything is
+ *     enqueued.  The caller owns every buffer, including the workspace; the library
+ *     allocates no device memory.
  *   - H and W are bfloat16 bit patterns (uint16_t).  H, W, dH and dW must be 16-byte
  *     aligned, the workspace 256-byte aligned, everything else 4-byte aligned; d must be a
  *     multiple of 8 (TMA rows are whole 16-byte units).  dH and dW are written with 32-byte
@@ -60,7 +62,7 @@ extern "C" {
 
 typedef enum fkl_status {
   FKL_OK = 0,
-  FKL_ERR_INVALID_ARG = 1,  /* NULL pointer, bad shape, non-positive tau or chunk */
+  FKL_ERR_INVALID_ARG = 1,  /* NULL or non-device pointer, bad shape, non-positive tau or chunk */
   FKL_ERR_ALIGNMENT = 2,    /* a pointer or d breaks the alignment rules above */
   FKL_ERR_UNSUPPORTED = 3,  /* the current device is not sm_103 */
   FKL_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than fkl_workspace_size() */

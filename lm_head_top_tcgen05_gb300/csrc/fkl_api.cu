@@ -30,6 +30,22 @@ static fkl_status fail(fkl_status s, const char* fmt, ...) {
 
 void set_last_error_message(const char* msg) { g_last_error = msg; }
 
+int check_device_memory(const NamedPtr* ptrs, int n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FKL_ERR_CUDA, "cudaGetDevice failed");
+  for (int i = 0; i < n; ++i) {
+    if (ptrs[i].p == nullptr) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptrs[i].p) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(FKL_ERR_INVALID_ARG, "%s is not CUDA memory", ptrs[i].name);
+    }
+    const bool ok = (a.type == cudaMemoryTypeDevice && a.device == dev) || a.type == cudaMemoryTypeManaged;
+    if (!ok) return fail(FKL_ERR_INVALID_ARG, "%s is not device memory of the current device", ptrs[i].name);
+  }
+  return FKL_OK;
+}
+
 static fkl_status cuda_fail(cudaError_t e, const char* what) {
   return fail(FKL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -537,6 +553,14 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
   if (!aligned(loss, 4) || (lse && !aligned(lse, 4))) return fail(FKL_ERR_ALIGNMENT, "loss and lse must be 4-byte aligned");
   DevInfo di;
   if ((s = device_info(&di)) != FKL_OK) return s;
+  {
+    const NamedPtr ptrs[] = {{H, "H"}, {W, "W"}, {topk_idx, "topk_idx"}, {topk_logits, "topk_logits"},
+                             {mask, "mask"}, {loss, "loss"}, {lse, "lse"}, {workspace, "workspace"},
+                             {opts ? opts->seq_ids : nullptr, "fkl_options.seq_ids"},
+                             {opts ? opts->student_topk_logits : nullptr, "fkl_options.student_topk_logits"},
+                             {opts ? opts->global_count : nullptr, "fkl_options.global_count"}};
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 11))) != FKL_OK) return s;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -795,6 +819,14 @@ static fkl_status backward_impl(const uint16_t* H, const uint16_t* W, const int3
     return fail(FKL_ERR_ALIGNMENT, "lse and grad_loss must be 4-byte aligned");
   DevInfo di;
   if ((s = device_info(&di)) != FKL_OK) return s;
+  {
+    const NamedPtr ptrs[] = {{H, "H"}, {W, "W"}, {topk_idx, "topk_idx"}, {topk_logits, "topk_logits"},
+                             {mask, "mask"}, {lse, "lse"}, {grad_loss, "grad_loss"}, {gH, "dH"}, {gW, "dW"},
+                             {workspace, "workspace"}, {opts ? opts->seq_ids : nullptr, "fkl_options.seq_ids"},
+                             {opts ? opts->student_topk_logits : nullptr, "fkl_options.student_topk_logits"},
+                             {opts ? opts->global_count : nullptr, "fkl_options.global_count"}};
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 13))) != FKL_OK) return s;
+  }
   choose_slab_width(&pl, di.sms / 2);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -881,6 +913,11 @@ fkl_status fkl_local_count(const uint8_t* mask, int64_t T, const fkl_options* op
   if (ws_bytes < need) return fail(FKL_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
   DevInfo di;
   if ((s = device_info(&di)) != FKL_OK) return s;
+  {
+    const NamedPtr ptrs[] = {{mask, "mask"}, {count, "count"}, {workspace, "workspace"},
+                             {opts ? opts->seq_ids : nullptr, "fkl_options.seq_ids"}};
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 4))) != FKL_OK) return s;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);

@@ -67,6 +67,18 @@ struct DivSpec {
 // Sets the message that fkl_last_error() returns on the calling thread.
 void set_last_error_message(const char* msg);
 
+// A pointer argument and its name, for check_device_memory.
+struct NamedPtr {
+  const void* p;
+  const char* name;
+};
+// Every pointer that the kernels or the tensor maps will dereference must be device (or
+// managed) memory of the current device.  A host pointer given by mistake is refused here,
+// before anything is enqueued, instead of faulting in a kernel.  NULL entries pass (whether
+// an argument may be NULL is checked by each entry point).  FKL_OK or FKL_ERR_INVALID_ARG
+// (with the argument's name in fkl_last_error()); int for the fkl_status values of fkl.h.
+int check_device_memory(const NamedPtr* ptrs, int n);
+
 // Event pair around one GEMM launch when a trace is active on this thread (fkl_trace.cu).
 // kind: 0 forward, 1 dS recompute, 2 dW, 3 dH.
 void trace_launch_begin(cudaStream_t st);

@@ -95,6 +95,11 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
   int sms = 0;
   fkl_status s = scratch_address(&ws, &sms);
   if (s != FKL_OK) return s;
+  {
+    const NamedPtr ptrs[] = {{H, "H"}, {W, "W"}, {topk_idx, "topk_idx"}, {topk_logits, "topk_logits"},
+                             {mask, "mask"}, {loss, "loss"}, {lse, "lse"}};
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 7))) != FKL_OK) return s;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);

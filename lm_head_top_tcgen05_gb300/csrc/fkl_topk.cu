@@ -367,6 +367,12 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return topk_fail(FKL_ERR_CUDA, "device query failed");
   if (major != 10 || minor != 3) return topk_fail(FKL_ERR_UNSUPPORTED, "device is not sm_103");
+  {
+    const NamedPtr ptrs[] = {{Ht, "Ht"}, {Wt, "Wt"}, {topk_idx, "topk_idx"}, {topk_logits, "topk_logits"},
+                             {workspace, "workspace"}};
+    const int s = check_device_memory(ptrs, 5);
+    if (s != FKL_OK) return static_cast<fkl_status>(s);
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
