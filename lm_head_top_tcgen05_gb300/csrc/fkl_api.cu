@@ -341,10 +341,10 @@ static fkl_status device_info(DevInfo* out) {
   return FKL_OK;
 }
 
-// Row blocks per group in the unit order of the products over the vocabulary (forward,
-// dS recompute, the teacher cache's passes): units run split-major within a group, so the
-// 76 pairs running together cover 38 row blocks of about 2 vocabulary splits and share
-// each W tile in L2.  Against row-major order (about 6 row blocks per W tile) this cut the
+// Row blocks per group in the unit order of the products over the vocabulary (the dS
+// recompute and the teacher cache's passes; the forward takes fwd_group_rows below): units
+// run split-major within a group, so the 76 pairs running together cover 38 row blocks of
+// about 2 vocabulary splits and share each W tile in L2.  Against row-major order (about 6 row blocks per W tile) this cut the
 // forward's DRAM reads 4.4x at the 32K shapes.  In same-process A/Bs, 38 beat 19 by 0.9 %
 // per step at 32K and 1.5 % at 256K (forward 6 % faster there), and 76 was 7-8 % slower
 // than 38 (76 row blocks of H no longer stay in L2).  dW and dH keep row-major order, in
@@ -352,6 +352,21 @@ static fkl_status device_info(DevInfo* out) {
 constexpr int kGroupRows = 38;
 
 int group_rows(int m_tiles) { return kGroupRows < m_tiles ? kGroupRows : m_tiles; }
+
+// Row blocks per group for the forward, whose units are drawn from a counter.  An SM keeps
+// what it reads in its own die's half of L2: a buffer that all SMs re-read stays resident
+// up to about 64 MB on a GB300, not the 126 MB of L2 in all.  A group's H blocks and the W
+// tiles in flight must fit in that half, so the forward takes a quarter of the pair count
+// (19 row blocks; the pairs running together then cover four whole vocabulary splits).  In
+// a same-process sweep of 12-38 row blocks this read the least DRAM on every workload (per
+// launch: 9.2 against 13.8-15.4 GB for 38 at the 32K shapes, 73-74 against 132-141 GB at
+// 256K, 27-28 against 107-118 GB on the packed 64K x 4096 workload; counts that do not
+// divide the pair count read more), and the forward took 2.0 % less time at 256K and 6.5 %
+// less on the packed workload, the same at 8K and 32K.
+int fwd_group_rows(int m_tiles, int pairs) {
+  const int g = pairs >= 4 ? pairs / 4 : 1;
+  return g < m_tiles ? g : m_tiles;
+}
 
 // Tile width along d for the dW and dH products: the width with the least estimated time,
 // counting padded columns and the measured relative cost per column of each width on GB300
@@ -592,7 +607,7 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
     // dynamically scheduled launch, sched_base 0), in groups of row blocks, split-major.
     const int m_tiles = (int)cdiv(T, 256), n_tiles = (int)cdiv(V, kVocabTile);
     GemmShape g = make_shape(T, V, d, kVocabTile, dynamic_splits(m_tiles, n_tiles, di.sms / 2), &hdr->status, 256);
-    g.group_m = group_rows(g.m_tiles);
+    g.group_m = fwd_group_rows(g.m_tiles, di.sms / 2);
     g.sched = &hdr->items_taken;
     const int nsplit = g.nsplit;
     FwdParams fp;

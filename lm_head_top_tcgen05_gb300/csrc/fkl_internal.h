@@ -176,6 +176,8 @@ void plan_ksplit(GemmShape* g, int pairs, float* kpart, int slots);
 
 // Row blocks per group of the unit order for products over the vocabulary (see fkl_api.cu).
 int group_rows(int m_tiles);
+// Row blocks per group of the forward's drawn units (see fkl_api.cu).
+int fwd_group_rows(int m_tiles, int pairs);
 
 // rows_per_unit: 128 for the one-SM kernel, 256 for the two-SM (CTA pair) kernel.
 GemmShape make_shape(int64_t M, int64_t N, int64_t Kd, int bn, int nsplit, uint32_t* status,
