@@ -353,9 +353,9 @@ constexpr int kGroupRows = 38;
 
 int group_rows(int m_tiles) { return kGroupRows < m_tiles ? kGroupRows : m_tiles; }
 
-// Row blocks per group for the forward, whose units are drawn from a counter.  An SM keeps
-// what it reads in its own die's half of L2: a buffer that all SMs re-read stays resident
-// up to about 64 MB on a GB300, not the 126 MB of L2 in all.  A group's H blocks and the W
+// Row blocks per group for the forward, whose units are drawn from a counter.  A buffer
+// that SMs re-read stays resident in L2 up to about 64 MB on a GB300, not the 126 MB of L2
+// in all, whichever SMs read it (half of L2 serves any set of SMs).  A group's H blocks and the W
 // tiles in flight must fit in that half, so the forward takes a quarter of the pair count
 // (19 row blocks; the pairs running together then cover four whole vocabulary splits).  In
 // a same-process sweep of 12-38 row blocks this read the least DRAM on every workload (per
