@@ -341,28 +341,28 @@ static fkl_status device_info(DevInfo* out) {
   return FKL_OK;
 }
 
-// Row blocks per group in the unit order of the products over the vocabulary (the dS
-// recompute and the teacher cache's passes; the forward takes fwd_group_rows below): units
-// run split-major within a group, so the 76 pairs running together cover 38 row blocks of
-// about 2 vocabulary splits and share each W tile in L2.  Against row-major order (about 6 row blocks per W tile) this cut the
-// forward's DRAM reads 4.4x at the 32K shapes.  In same-process A/Bs, 38 beat 19 by 0.9 %
-// per step at 32K and 1.5 % at 256K (forward 6 % faster there), and 76 was 7-8 % slower
-// than 38 (76 row blocks of H no longer stay in L2).  dW and dH keep row-major order, in
-// which each A block is read once.
+// Row blocks per group in the unit order of the dS recompute and the teacher cache's passes
+// (the forward takes fwd_group_rows below): units run split-major within a group, so the 76
+// pairs running together cover 38 row blocks of about 2 vocabulary splits and share each W
+// tile in L2.  Against row-major order (about 6 row blocks per W tile) grouping cut the DRAM
+// reads of the 32K products 2-4x.  In same-process A/Bs groups of 19 were 0.3 % slower than
+// 38 for the dS recompute at 32K and about 1 % slower for the teacher's passes at the production
+// shape, and 76 was 7-8 % slower than 38 (76 row blocks of H no longer stay in L2).  dW and
+// dH keep row-major order, in which each A block is read once.
 constexpr int kGroupRows = 38;
 
 int group_rows(int m_tiles) { return kGroupRows < m_tiles ? kGroupRows : m_tiles; }
 
 // Row blocks per group for the forward, whose units are drawn from a counter.  A buffer
 // that SMs re-read stays resident in L2 up to about 64 MB on a GB300, not the 126 MB of L2
-// in all, whichever SMs read it (half of L2 serves any set of SMs).  A group's H blocks and the W
-// tiles in flight must fit in that half, so the forward takes a quarter of the pair count
-// (19 row blocks; the pairs running together then cover four whole vocabulary splits).  In
-// a same-process sweep of 12-38 row blocks this read the least DRAM on every workload (per
-// launch: 9.2 against 13.8-15.4 GB for 38 at the 32K shapes, 73-74 against 132-141 GB at
-// 256K, 27-28 against 107-118 GB on the packed 64K x 4096 workload; counts that do not
-// divide the pair count read more), and the forward took 2.0 % less time at 256K and 6.5 %
-// less on the packed workload, the same at 8K and 32K.
+// in all, whichever SMs read it (half of L2 serves any set of SMs).  A group's H blocks and
+// the W tiles in flight must fit in that half, so the forward takes a quarter of the pair
+// count (19 row blocks; the pairs running together then cover four whole vocabulary
+// splits).  In a same-process sweep of 12-38 row blocks this read the least DRAM on every
+// workload (per launch: 9.2 against 13.8-15.4 GB for 38 at the 32K shapes, 73-74 against
+// 132-141 GB at 256K, 27-28 against 107-118 GB on the packed 64K x 4096 workload; counts
+// that do not divide the pair count read more), and the forward took 2.0 % less time at
+// 256K and 6.5 % less on the packed workload, the same at 8K and 32K.
 int fwd_group_rows(int m_tiles, int pairs) {
   const int g = pairs >= 4 ? pairs / 4 : 1;
   return g < m_tiles ? g : m_tiles;
@@ -574,7 +574,7 @@ fkl_status fkl_forward_ex(const uint16_t* H, const uint16_t* W, const int32_t* t
                              {opts ? opts->seq_ids : nullptr, "fkl_options.seq_ids"},
                              {opts ? opts->student_topk_logits : nullptr, "fkl_options.student_topk_logits"},
                              {opts ? opts->global_count : nullptr, "fkl_options.global_count"}};
-    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 11))) != FKL_OK) return s;
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs))) != FKL_OK) return s;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -840,7 +840,7 @@ static fkl_status backward_impl(const uint16_t* H, const uint16_t* W, const int3
                              {workspace, "workspace"}, {opts ? opts->seq_ids : nullptr, "fkl_options.seq_ids"},
                              {opts ? opts->student_topk_logits : nullptr, "fkl_options.student_topk_logits"},
                              {opts ? opts->global_count : nullptr, "fkl_options.global_count"}};
-    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 13))) != FKL_OK) return s;
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs))) != FKL_OK) return s;
   }
   choose_slab_width(&pl, di.sms / 2);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -931,7 +931,7 @@ fkl_status fkl_local_count(const uint8_t* mask, int64_t T, const fkl_options* op
   {
     const NamedPtr ptrs[] = {{mask, "mask"}, {count, "count"}, {workspace, "workspace"},
                              {opts ? opts->seq_ids : nullptr, "fkl_options.seq_ids"}};
-    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 4))) != FKL_OK) return s;
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs))) != FKL_OK) return s;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);

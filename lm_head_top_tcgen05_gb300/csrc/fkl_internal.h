@@ -78,6 +78,10 @@ struct NamedPtr {
 // an argument may be NULL is checked by each entry point).  FKL_OK or FKL_ERR_INVALID_ARG
 // (with the argument's name in fkl_last_error()); int for the fkl_status values of fkl.h.
 int check_device_memory(const NamedPtr* ptrs, int n);
+template <int N>
+int check_device_memory(const NamedPtr (&ptrs)[N]) {
+  return check_device_memory(ptrs, N);
+}
 
 // Event pair around one GEMM launch when a trace is active on this thread (fkl_trace.cu).
 // kind: 0 forward, 1 dS recompute, 2 dW, 3 dH.

@@ -98,7 +98,7 @@ extern "C" fkl_status fkl_forward_noalloc(const uint16_t* H, const uint16_t* W, 
   {
     const NamedPtr ptrs[] = {{H, "H"}, {W, "W"}, {topk_idx, "topk_idx"}, {topk_logits, "topk_logits"},
                              {mask, "mask"}, {loss, "loss"}, {lse, "lse"}};
-    if ((s = static_cast<fkl_status>(check_device_memory(ptrs, 7))) != FKL_OK) return s;
+    if ((s = static_cast<fkl_status>(check_device_memory(ptrs))) != FKL_OK) return s;
   }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -370,7 +370,7 @@ extern "C" fkl_status fkl_teacher_topk_ex(const uint16_t* Ht, const uint16_t* Wt
   {
     const NamedPtr ptrs[] = {{Ht, "Ht"}, {Wt, "Wt"}, {topk_idx, "topk_idx"}, {topk_logits, "topk_logits"},
                              {workspace, "workspace"}};
-    const int s = check_device_memory(ptrs, 5);
+    const int s = check_device_memory(ptrs);
     if (s != FKL_OK) return static_cast<fkl_status>(s);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
