@@ -262,8 +262,8 @@ def blas_threads():
 # every launch of five full-size steps (dram__bytes_read.sum + dram__bytes_write.sum, one
 # pass), averaged over the launches of each kind; TRAFFIC_FLOPS is that kind's mean work per
 # launch, so the bench's own launches take the figures as they are.
-TRAFFIC_SOURCES_SHA = "ca9226be3fcfe191"
-TRAFFIC_BYTES = {0: 9.092e9, 1: 1.960e9, 2: 3.034e9, 3: 3.631e9}
+TRAFFIC_SOURCES_SHA = "d536741306180354"
+TRAFFIC_BYTES = {0: 9.214e9, 1: 1.610e9, 2: 2.439e9, 3: 3.129e9}
 TRAFFIC_FLOPS = {0: 2.0 * 32768 * 201088 * 2880, 1: 2.0 * 32768 * 201088 * 2880 / 18,
                  2: 2.0 * 32768 * 201088 * 2880 / 18, 3: 2.0 * 32768 * 201088 * 2880 / 18}
 
